@@ -1,0 +1,586 @@
+"""Pins of the CPU oracle against what the paper and the mathematics fix.
+
+Each test checks an oracle function against something other than the oracle itself:
+a library routine (numpy's Philox, torch's number-format conversions, numpy
+reductions, sorts and einsum), a closed form, an invariant stated by the paper, a
+hand-derived table (tests/golden/), or brute force on tiny inputs.
+
+Paper: "SPIN: Shadow Predictive Indexer for Sparse Attention" (arXiv 2610.09025).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_indexer_spin_gb300 import synthetic as syn
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _table(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append([int(x) for x in line.split()])
+    return rows
+
+
+def tiny_cfg(o, **kw):
+    base = dict(n_req=2, max_slots=300, max_rows=4, n_heads=2, head_dim=4, kv_heads=2,
+                q_dtype="f32", k_dtype="f32", top_k=16, rho_bp=4000, gamma_bp=500,
+                alpha=0.9, combine="max", seed=7)
+    base.update(kw)
+    return o.make_cfg(**base)
+
+
+# --------------------------------------------------------------------------- Philox
+
+def _numpy_philox(ctr, key):
+    """numpy's Philox4x64-10 advances its 256-bit counter before each block; start one
+    below the wanted counter."""
+    c = list(ctr)
+    i = 0
+    while c[i] == 0:
+        c[i] = (1 << 64) - 1
+        i += 1
+    c[i] -= 1
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64))
+    st = bg.state
+    st["state"]["counter"] = np.array(c, dtype=np.uint64)
+    st["buffer_pos"] = 4
+    bg.state = st
+    return [int(x) for x in bg.random_raw(4)]
+
+
+@pytest.mark.parametrize("ctr,key", [
+    ([1, 0, 0, 0], [0, 0]),
+    ([5, 0, 3, 17], [0x0123456789ABCDEF, 42]),
+    ([0, 1, 0, 0], [7, 0]),                      # exercises the counter carry in numpy
+    ([2**64 - 1, 2**63, 99, 2**40], [2**64 - 1, 2**64 - 1]),
+    ([123456, 3, 95, 2047], [2026, 1]),
+])
+def test_philox_matches_numpy(oracle_mod, ctr, key):
+    assert oracle_mod.philox4x64_10(ctr, key) == _numpy_philox(ctr, key)
+
+
+def test_explore_key_is_high_word0(oracle_mod):
+    out = oracle_mod.philox4x64_10([11, 2, 5, 300], [99, 3])
+    assert oracle_mod.explore_key(99, 3, 11, 2, 5, 300) == out[0] >> 32
+
+
+# --------------------------------------------------------------------- number formats
+
+def test_e4m3_decode_all_codes(oracle_mod):
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    for code in range(256):
+        got = oracle_mod.decode_e4m3(code)
+        want = float(ref[code])
+        if math.isnan(want):
+            assert math.isnan(got)
+        else:
+            assert got == want and math.copysign(1, got) == math.copysign(1, want), code
+
+
+def test_bf16_decode(oracle_mod):
+    rng = np.random.default_rng(0)
+    bits = np.concatenate([np.arange(0, 65536, 97), rng.integers(0, 65536, 4000)]).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64)
+    for b, r in zip(bits.tolist(), ref.tolist()):
+        got = oracle_mod.decode_bf16(b)
+        if math.isnan(r):
+            assert math.isnan(got)
+        else:
+            assert got == r
+
+
+# ---------------------------------------------------------------- budget, exploration
+
+@pytest.mark.parametrize("row", _table("budget_table.txt"))
+def test_budget_table(oracle_mod, row):
+    B, K, rho, m = row
+    assert oracle_mod.budget(B, K, rho) == m
+
+
+@pytest.mark.parametrize("row", _table("explore_count_table.txt"))
+def test_explore_count_table(oracle_mod, row):
+    m, f, g, e = row
+    assert oracle_mod.explore_count(m, f, g) == e
+
+
+def test_budget_properties(oracle_mod):
+    # capped by B, at least min(B, ceil(K/b)), monotone non-increasing in rho
+    for B in (1, 2, 7, 64, 65, 1000, 2048):
+        for K in (1, 64, 256, 2048):
+            prev = None
+            for rho in range(0, 10001, 250):
+                m = oracle_mod.budget(B, K, rho)
+                assert 1 <= m <= B
+                assert m >= min(B, -(-K // 64))
+                assert m >= min(B, -(-(10000 - rho) * B // 10000))
+                if prev is not None:
+                    assert m <= prev
+                prev = m
+            assert oracle_mod.budget(B, K, 0) == B
+
+
+# ------------------------------------------------------------------- block scores
+
+def _blockwise_max(x, n):
+    starts = np.arange(0, n, 64)
+    return np.maximum.reduceat(x[:n], starts)
+
+
+@pytest.mark.parametrize("n", [1, 63, 64, 65, 130, 257])
+def test_block_scores_reduce_to_vertical_max(oracle_mod, n):
+    """D = -inf everywhere: Eq. 1 gives V[i], Eq. 2 the blockwise max of V."""
+    cfg = tiny_cfg(oracle_mod)
+    rng = np.random.default_rng(n)
+    V = rng.standard_normal(cfg.max_slots).astype(np.float32)
+    D = np.full(oracle_mod.d_len(cfg), -np.inf, dtype=np.float32)
+    q = n - 1 + 2
+    S = oracle_mod.block_scores(cfg, V, D, n, q)
+    np.testing.assert_array_equal(S, _blockwise_max(V, n))
+
+
+@pytest.mark.parametrize("n", [1, 64, 100, 257])
+def test_block_scores_reduce_to_diagonal_max(oracle_mod, n):
+    """V = -inf: S[j] is the max of D over the offsets q - i of block j's slots."""
+    cfg = tiny_cfg(oracle_mod)
+    rng = np.random.default_rng(100 + n)
+    V = np.full(cfg.max_slots, -np.inf, dtype=np.float32)
+    D = rng.standard_normal(oracle_mod.d_len(cfg)).astype(np.float32)
+    q = n + 1
+    S = oracle_mod.block_scores(cfg, V, D, n, q)
+    diag = D[q - np.arange(n)]              # value seen by slot i
+    np.testing.assert_array_equal(S, _blockwise_max(diag, n))
+
+
+def test_block_scores_sum_mode_with_zero_diagonal(oracle_mod):
+    cfg = tiny_cfg(oracle_mod, combine="sum")
+    rng = np.random.default_rng(3)
+    V = rng.standard_normal(cfg.max_slots).astype(np.float32)
+    D = np.zeros(oracle_mod.d_len(cfg), dtype=np.float32)
+    S = oracle_mod.block_scores(cfg, V, D, 200, 205)
+    np.testing.assert_array_equal(S, _blockwise_max(V, 200))
+
+
+def test_block_scores_brute_force_tiny(oracle_mod):
+    """Brute force over a 3-block context (one block partial), both combiners."""
+    for combine in ("max", "sum"):
+        cfg = tiny_cfg(oracle_mod, combine=combine)
+        rng = np.random.default_rng(9)
+        n, q = 150, 152
+        V = rng.standard_normal(cfg.max_slots).astype(np.float32)
+        D = rng.standard_normal(oracle_mod.d_len(cfg)).astype(np.float32)
+        S = oracle_mod.block_scores(cfg, V, D, n, q)
+        assert len(S) == 3
+        for j in range(3):
+            vals = []
+            for i in range(64 * j, min(64 * (j + 1), n)):
+                a, b = float(V[i]), float(D[q - i])
+                vals.append(max(a, b) if combine == "max" else float(np.float32(a) + np.float32(b)))
+            assert S[j] == max(vals)
+
+
+# ------------------------------------------------------------------- selection
+
+def _random_state(o, cfg, rng, warm=1):
+    V = rng.standard_normal((cfg.n_req, cfg.max_slots)).astype(np.float32)
+    D = rng.standard_normal((cfg.n_req, o.d_len(cfg))).astype(np.float32)
+    return V, D, np.full(cfg.n_req, warm, dtype=np.int32)
+
+
+def _check_selection(o, cfg, V, D, n, q, sel, rho_bp, row=0):
+    """Invariants of §3.2 / §3.2.1 against an independent numpy ranking."""
+    B = -(-n // 64)
+    m = o.budget(B, cfg.top_k, rho_bp)
+    f = 2 if B > 1 else 1
+    e = o.explore_count(m, f, cfg.gamma_bp)
+    t = max(m - f - e, 0) if m > f else 0
+    assert len(sel) == max(m, f)
+    assert list(sel) == sorted(set(sel))
+    assert 0 in sel and (B - 1) in sel
+    S = o.block_scores(cfg, V, D, n, q + row)
+    free = np.array([j for j in range(B) if j not in (0, B - 1)], dtype=np.int64)
+    order = free[np.lexsort((free, -S[free].astype(np.float64)))]
+    top = set(order[:t].tolist())
+    assert top <= set(sel)
+    explored = set(sel) - top - {0, B - 1}
+    assert len(explored) == (e if m > f else 0)
+    assert not (explored & top)
+    return top, explored
+
+
+@pytest.mark.parametrize("n,rho", [(4096, 4000), (4100, 4000), (130, 4000), (2000, 2000),
+                                   (640, 9000), (64, 4000), (65, 5000)])
+def test_selection_invariants(oracle_mod, n, rho):
+    o = oracle_mod
+    cfg = tiny_cfg(o, n_req=3, max_slots=4200, top_k=256 if n > 1000 else 64, gamma_bp=1000)
+    rng = np.random.default_rng(n + rho)
+    V, D, warm = _random_state(o, cfg, rng)
+    n_slots = np.array([n, max(1, n - 37), n], dtype=np.int32)
+    q_pos = n_slots - 1
+    q_pos[2] += 3
+    blocks, nb, _, _, ok = o.select_blocks(cfg, V, D, warm, n_slots, q_pos, 1, rho, 5, 2)
+    assert ok
+    for r in range(cfg.n_req):
+        sel = blocks[r, 0, : nb[r, 0]]
+        _check_selection(o, cfg, V[r], D[r], int(n_slots[r]), int(q_pos[r]), sel, rho)
+
+
+def test_rho_zero_and_cold_are_dense(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, n_req=2, max_slots=2000, top_k=64)
+    rng = np.random.default_rng(1)
+    V, D, warm = _random_state(o, cfg, rng)
+    n_slots = np.array([1999, 777], dtype=np.int32)
+    blocks, nb, _, _, ok = o.select_blocks(cfg, V, D, warm, n_slots, n_slots - 1, 1, 0)
+    assert ok
+    for r in range(2):
+        B = -(-int(n_slots[r]) // 64)
+        assert list(blocks[r, 0, : nb[r, 0]]) == list(range(B))
+    warm[:] = 0
+    blocks, nb, _, _, ok = o.select_blocks(cfg, V, D, warm, n_slots, n_slots - 1, 1, 6000)
+    for r in range(2):
+        B = -(-int(n_slots[r]) // 64)
+        assert list(blocks[r, 0, : nb[r, 0]]) == list(range(B))
+
+
+def test_exploration_uniform_chi_square(oracle_mod):
+    """Random exploration picks e distinct blocks uniformly among the non-selected ones:
+    frequencies over many steps against e / (#candidates), chi-square at p = 1e-4."""
+    o = oracle_mod
+    n = 64 * 60
+    cfg = tiny_cfg(o, n_req=1, max_slots=n + 8, top_k=64, gamma_bp=2000)
+    V = np.linspace(0, 1, cfg.max_slots, dtype=np.float32)[None, :].copy()  # fixed ranking
+    D = np.full((1, o.d_len(cfg)), -1e30, dtype=np.float32)
+    warm = np.ones(1, dtype=np.int32)
+    ns = np.array([n], dtype=np.int32)
+    counts = np.zeros(60)
+    steps = 3000
+    top = None
+    for s in range(steps):
+        blocks, nb, _, _, ok = o.select_blocks(cfg, V, D, warm, ns, ns - 1, 1, 5000, s, 0)
+        t, ex = _check_selection(o, cfg, V[0], D[0], n, n - 1, blocks[0, 0, : nb[0, 0]], 5000)
+        top = t if top is None else top
+        assert t == top
+        for j in ex:
+            counts[j] += 1
+    cand = [j for j in range(1, 59) if j not in top]
+    e = o.explore_count(o.budget(60, 64, 5000), 2, 2000)
+    expected = steps * e / len(cand)
+    chi2 = float(((counts[cand] - expected) ** 2 / expected).sum())
+    from scipy.stats import chi2 as chi2_dist
+    assert chi2 < chi2_dist.ppf(1 - 1e-4, len(cand) - 1), chi2
+    assert counts[list(top)].sum() == 0
+
+
+def test_union_is_or_of_rows(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, n_req=2, max_slots=3000, top_k=128, max_rows=4)
+    rng = np.random.default_rng(5)
+    V, D, warm = _random_state(o, cfg, rng)
+    ns = np.array([2900, 1500], dtype=np.int32)
+    blocks, nb, union, nu, ok = o.select_blocks(cfg, V, D, warm, ns, ns - 1, 4, 4000, 3, 1)
+    assert ok
+    for r in range(2):
+        rows = [set(blocks[r, k, : nb[r, k]].tolist()) for k in range(4)]
+        for k in range(4):
+            _check_selection(o, cfg, V[r], D[r], int(ns[r]), int(ns[r] - 1),
+                             blocks[r, k, : nb[r, k]], 4000, row=k)
+        assert list(union[r, : nu[r]]) == sorted(set().union(*rows))
+        assert nu[r] >= nb[r, 0]
+
+
+def test_invalid_request_is_skipped(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, n_req=2, max_slots=500)
+    V, D, warm = o.new_state(cfg)
+    ns = np.array([400, 400], dtype=np.int32)
+    qp = np.array([399, 10], dtype=np.int32)       # request 1: q < N - 1
+    blocks, nb, _, _, ok = o.select_blocks(cfg, V, D, warm, ns, qp, 1)
+    assert not ok and nb[1, 0] == 0 and nb[0, 0] == 7
+
+
+# ------------------------------------------------------------------------- scores
+
+def _decode_torch(raw, dtype):
+    if dtype == "f32":
+        return raw.astype(np.float64)
+    if dtype == "bf16":
+        return torch.from_numpy(raw.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    return torch.from_numpy(raw.copy()).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _brute_scores(cfg_kw, q, w, pool, scale, bt, blist, nlist, ns, rows):
+    """Dense numpy einsum in float64 over torch-decoded inputs."""
+    H, d, kvh = cfg_kw["n_heads"], cfg_kw["head_dim"], cfg_kw["kv_heads"]
+    qd = _decode_torch(q, cfg_kw["q_dtype"]).reshape(q.shape[0], rows, H, d)
+    kd = _decode_torch(pool, cfg_kw["k_dtype"]).reshape(pool.shape[0], 64, kvh, d)
+    R, MB = bt.shape[0], blist.shape[1]
+    out = np.zeros((R, rows, MB * 64))
+    for r in range(R):
+        for k in range(nlist[r]):
+            blk = blist[r, k]
+            page = bt[r, blk]
+            keys = kd[page]                                   # [64][kvh][d]
+            if kvh == 1:
+                keys = np.broadcast_to(keys, (64, H, d))
+            dots = np.einsum("shc,xhc->xsh", keys, qd[r])      # [rows][64][H]
+            if scale is not None:
+                dots = dots * scale[page][None, :, None].astype(np.float64)
+            z = (np.maximum(dots, 0) * w[r][:, None, :].astype(np.float64)).sum(-1)
+            valid = (blk * 64 + np.arange(64)) < ns[r]
+            out[r, :, k * 64:(k + 1) * 64] = np.where(valid[None, :], z, 0.0)
+    return out
+
+
+@pytest.mark.parametrize("qd,kd,kvh,rows", [("f32", "f32", 2, 1), ("bf16", "bf16", 2, 3),
+                                             ("bf16", "e4m3", 1, 1), ("f32", "bf16", 1, 4),
+                                             ("bf16", "e4m3", 2, 2)])
+def test_scores_brute_force_tiny(oracle_mod, qd, kd, kvh, rows):
+    o = oracle_mod
+    kw = dict(n_req=2, max_slots=200, max_rows=4, n_heads=2, head_dim=4, kv_heads=kvh,
+              q_dtype=qd, k_dtype=kd, top_k=16, rho_bp=0, gamma_bp=0, alpha=0.5)
+    cfg = o.make_cfg(**kw)
+    wl = syn.Workload("tiny", n_req=2, n_layers=1, n0=130, n_heads=2, head_dim=4,
+                      kv_heads=kvh, q_dtype=qd, k_dtype=kd, top_k=16, rho_bp=0, gamma_bp=0,
+                      alpha=0.5, steps=4, rows=rows, heavy=3, rope_dims=2, shuffle=True,
+                      mean_accept=2.0 if rows > 1 else 0.0)
+    inp = syn.SyntheticInputs(wl, "cpu")
+    cfg = o.make_cfg(**{**kw, "max_slots": wl.max_slots})
+    q, w, qp = inp.step_inputs()
+    qn, wn = syn.raw_numpy(q), w.numpy()
+    pool = syn.raw_numpy(inp.k_pool[0])
+    scale = None if inp.k_scale[0] is None else inp.k_scale[0].numpy()
+    bt = inp.block_table.numpy()
+    MB = o.max_blocks(cfg)
+    ns = np.array([130, 67], dtype=np.int32)
+    blist = np.full((2, MB), -1, dtype=np.int32)
+    blist[0, :3] = [0, 1, 2]
+    blist[1, :2] = [0, 1]
+    nlist = np.array([3, 2], dtype=np.int32)
+    sc, mags, ok = o.indexer_score(cfg, qn, wn, pool, scale, bt, blist, nlist, ns, rows,
+                                   want_mags=True)
+    assert ok
+    ref = _brute_scores(kw, qn, wn, pool, scale, bt, blist, nlist, ns, rows)
+    np.testing.assert_allclose(sc.astype(np.float64), ref, rtol=0, atol=1e-6 * (1 + mags.max()))
+    assert np.all(mags * (1 + 2.0 ** -23) >= np.abs(sc))   # |z| <= magnitude, up to float rounding
+
+
+def test_scores_integer_inputs_exact(oracle_mod):
+    """Integer-valued q, k, w: every sum is exact, so the float result equals numpy's."""
+    o = oracle_mod
+    kw = dict(n_req=1, max_slots=192, max_rows=2, n_heads=3, head_dim=8, kv_heads=3,
+              q_dtype="f32", k_dtype="f32", top_k=8, rho_bp=0, gamma_bp=0, alpha=0.5)
+    cfg = o.make_cfg(**kw)
+    rng = np.random.default_rng(4)
+    q = rng.integers(-4, 5, (1, 2, 3, 8)).astype(np.float32)
+    w = rng.integers(-2, 4, (1, 2, 3)).astype(np.float32)
+    pool = rng.integers(-5, 6, (3, 64, 3, 8)).astype(np.float32)
+    bt = np.array([[2, 0, 1]], dtype=np.int32)
+    blist = np.array([[0, 1, 2]], dtype=np.int32)
+    ns = np.array([150], dtype=np.int32)
+    sc, ok = o.indexer_score(cfg, q, w, pool, None, bt, blist, np.array([3], np.int32), ns, 2)
+    ref = _brute_scores(kw, q, w, pool, None, bt, blist, np.array([3]), ns, 2)
+    np.testing.assert_array_equal(sc.astype(np.float64), ref)
+
+
+def test_score_slot_matches_block_scores(oracle_mod):
+    o = oracle_mod
+    kw = dict(n_req=1, max_slots=128, max_rows=1, n_heads=4, head_dim=16, kv_heads=1,
+              q_dtype="bf16", k_dtype="e4m3", top_k=8, rho_bp=0, gamma_bp=0, alpha=0.5)
+    cfg = o.make_cfg(**kw)
+    rng = np.random.default_rng(2)
+    q = rng.integers(0, 65535, (1, 1, 4, 16)).astype(np.uint16) & 0xBFFF   # finite bf16
+    w = rng.random((1, 1, 4)).astype(np.float32)
+    pool = rng.integers(0, 126, (2, 64, 1, 16)).astype(np.uint8)
+    scale = rng.random((2, 64)).astype(np.float32)
+    bt = np.array([[1, 0]], dtype=np.int32)
+    sc, ok = o.indexer_score(cfg, q, w, pool, scale, bt, np.array([[0, 1]], np.int32),
+                             np.array([2], np.int32), np.array([128], np.int32), 1)
+    for i in (0, 5, 63, 64, 127):
+        page, s = bt[0, i // 64], i % 64
+        z, _ = o.score_slot(cfg, q[0], w[0], pool[page, s], scale[page, s], 1)
+        assert z[0] == sc[0, 0, i]
+
+
+# -------------------------------------------------------------------------- top-K
+
+def test_topk_brute_force_with_ties(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, n_req=2, max_slots=700, top_k=50)
+    MB = o.max_blocks(cfg)
+    rng = np.random.default_rng(8)
+    rows = 2
+    scores = np.round(rng.standard_normal((2, rows, MB * 64)) * 3).astype(np.float32)
+    scores[scores == 0] = -0.0                     # -0 and +0 compare equal
+    blist = np.full((2, MB), -1, dtype=np.int32)
+    sel0 = np.array([0, 2, 3, 7, 10])
+    blist[0, :5] = sel0
+    blist[1, :2] = [0, 1]
+    nlist = np.array([5, 2], dtype=np.int32)
+    ns = np.array([680, 100], dtype=np.int32)
+    idx, ok = o.topk(cfg, scores, blist, nlist, ns, rows)
+    assert ok
+    for r in range(2):
+        for row in range(rows):
+            ids, vals = [], []
+            for k in range(nlist[r]):
+                for s in range(64):
+                    i = blist[r, k] * 64 + s
+                    if i < ns[r]:
+                        ids.append(i)
+                        vals.append(scores[r, row, k * 64 + s])
+            ids, vals = np.array(ids), np.array(vals, dtype=np.float64)
+            order = np.lexsort((ids, -vals))[: cfg.top_k]
+            want = np.sort(ids[order])
+            want = np.concatenate([want, -np.ones(cfg.top_k - len(want), dtype=np.int64)])
+            np.testing.assert_array_equal(idx[r, row], want)
+    assert (idx[1, 0] >= 0).sum() == 50 and (idx[1, 0, :] < 100).all()
+
+
+def test_topk_pads_when_few_slots(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, n_req=1, max_slots=200, top_k=100)
+    MB = o.max_blocks(cfg)
+    scores = np.arange(MB * 64, dtype=np.float32)[None, None, :]
+    blist = np.zeros((1, MB), dtype=np.int32)
+    idx, ok = o.topk(cfg, scores, blist, np.array([1], np.int32), np.array([40], np.int32))
+    np.testing.assert_array_equal(idx[0, 0, :40], np.arange(40))
+    assert (idx[0, 0, 40:] == -1).all()
+
+
+# ---------------------------------------------------------------------------- EMA
+
+def test_ema_closed_form_constant_observation(oracle_mod):
+    """n equal observations z from V0: V_n = a^n V0 + (1 - a^n) z (exact in reals)."""
+    o = oracle_mod
+    for alpha in (0.5, 0.9):
+        cfg = tiny_cfg(o, n_req=1, max_slots=128, alpha=alpha)
+        MB = o.max_blocks(cfg)
+        V, D, warm = o.new_state(cfg)
+        rng = np.random.default_rng(1)
+        V0 = rng.standard_normal(V.shape).astype(np.float32)
+        V[:] = V0
+        z = rng.standard_normal(MB * 64).astype(np.float32)
+        blist = np.array([[0, 1]], dtype=np.int32)
+        ns = np.array([128], np.int32)
+        for step in range(1, 41):
+            D[:] = 0
+            assert o.replay_ema(cfg, V, D, warm, z[None, None, :], blist,
+                                np.array([2], np.int32), ns, np.array([127], np.int32))
+            a_n = np.float64(alpha) ** step
+            want = a_n * V0.astype(np.float64) + (1 - a_n) * z.astype(np.float64)
+            err = np.abs(V.astype(np.float64) - want)
+            scale = np.abs(V0).astype(np.float64) + np.abs(z).astype(np.float64)
+            assert (err <= 4 * step * 2.0 ** -24 * scale + 1e-30).all()
+            # D: one observation from 0: (1 - a) z at offset q - i
+            dwant = (1 - np.float64(np.float32(alpha))) * z.astype(np.float64)
+            np.testing.assert_allclose(D[0, 127 - np.arange(128)], dwant, rtol=2e-7, atol=0)
+        assert warm[0] == 1
+
+
+def test_mtp_replay_closed_form_and_prefix(oracle_mod):
+    """Prefix-valid replay (§3.2.2): after rows 0..a,
+    V = a^(a+1) V0 + (1-a) sum_r a^(a-r) z_r; rows above a leave no trace."""
+    o = oracle_mod
+    cfg = tiny_cfg(o, n_req=3, max_slots=256, alpha=0.9, max_rows=4)
+    MB = o.max_blocks(cfg)
+    rng = np.random.default_rng(12)
+    V0 = rng.standard_normal((3, cfg.max_slots)).astype(np.float32)
+    D0 = rng.standard_normal((3, o.d_len(cfg))).astype(np.float32)
+    scores = rng.standard_normal((3, 4, MB * 64)).astype(np.float32)
+    blist = np.full((3, MB), -1, dtype=np.int32)
+    blist[:, :2] = [1, 3]
+    nlist = np.full(3, 2, dtype=np.int32)
+    ns = np.full(3, 250, dtype=np.int32)
+    qp = ns - 1
+    acc = np.array([0, 2, 3], dtype=np.int32)
+    V, D, warm = V0.copy(), D0.copy(), np.zeros(3, np.int32)
+    assert o.replay_ema(cfg, V, D, warm, scores, blist, nlist, ns, qp, 4, acc)
+    al = np.float64(0.9)
+    for r in range(3):
+        a = acc[r]
+        for k, blk in enumerate(blist[r, :2]):
+            for s in range(64):
+                i = blk * 64 + s
+                if i >= 250:
+                    assert V[r, i] == V0[r, i]
+                    continue
+                zs = [np.float64(scores[r, row, k * 64 + s]) for row in range(a + 1)]
+                want = al ** (a + 1) * np.float64(V0[r, i]) + (1 - al) * sum(
+                    al ** (a - row) * zs[row] for row in range(a + 1))
+                assert abs(V[r, i] - want) <= 1e-6 * (abs(want) + 1)
+        untouched = np.ones(cfg.max_slots, bool)
+        untouched[64:128] = False
+        untouched[192:250] = False
+        np.testing.assert_array_equal(V[r, untouched], V0[r, untouched])
+        # D closed form: offset o collects rows r' <= a whose slot q + r' - o is scored
+        for off in range(0, 260):
+            hits = []
+            for row in range(a + 1):
+                i = qp[r] + row - off
+                if 0 <= i < 250 and (i // 64) in (1, 3):
+                    k = 0 if i // 64 == 1 else 1
+                    hits.append(np.float64(scores[r, row, k * 64 + i % 64]))
+            want = np.float64(D0[r, off])
+            for h in hits:
+                want = al * want + (1 - al) * h
+            assert abs(D[r, off] - want) <= 1e-6 * (abs(want) + 1)
+
+
+def test_replay_a0_equals_single_row(oracle_mod):
+    o = oracle_mod
+    cfg4 = tiny_cfg(o, n_req=2, max_slots=256, max_rows=4)
+    MB = o.max_blocks(cfg4)
+    rng = np.random.default_rng(3)
+    V0 = rng.standard_normal((2, cfg4.max_slots)).astype(np.float32)
+    D0 = rng.standard_normal((2, o.d_len(cfg4))).astype(np.float32)
+    scores = rng.standard_normal((2, 4, MB * 64)).astype(np.float32)
+    blist = np.tile(np.array([0, 2, 3, 3], np.int32), (2, 1))
+    nlist = np.array([3, 2], np.int32)
+    ns = np.array([200, 190], np.int32)
+    qp = ns - 1
+    Va, Da, wa = V0.copy(), D0.copy(), np.zeros(2, np.int32)
+    o.replay_ema(cfg4, Va, Da, wa, scores, blist, nlist, ns, qp, 4, np.zeros(2, np.int32))
+    Vb, Db, wb = V0.copy(), D0.copy(), np.zeros(2, np.int32)
+    o.replay_ema(cfg4, Vb, Db, wb, np.ascontiguousarray(scores[:, :1]), blist, nlist, ns, qp, 1)
+    assert Va.tobytes() == Vb.tobytes() and Da.tobytes() == Db.tobytes()
+
+
+# --------------------------------------------------------------- whole step (rho = 0)
+
+def test_rho_zero_step_equals_dense_topk(oracle_mod):
+    """At 0 % target sparsity every block is scored, so SPIN's top-K must equal the dense
+    indexer's top-K (integer-valued inputs make both score sets exact)."""
+    o = oracle_mod
+    rng = np.random.default_rng(21)
+    R, H, d, n = 2, 3, 8, 1000
+    kw = dict(n_req=R, max_slots=1100, max_rows=1, n_heads=H, head_dim=d, kv_heads=1,
+              q_dtype="f32", k_dtype="f32", top_k=100, rho_bp=0, gamma_bp=500, alpha=0.9)
+    cfg = o.make_cfg(**kw)
+    MB = o.max_blocks(cfg)
+    pool = rng.integers(-3, 4, (R * MB, 64, 1, d)).astype(np.float32)
+    bt = rng.permutation(R * MB).astype(np.int32).reshape(R, MB)
+    V, D, warm = o.new_state(cfg)
+    V[:] = rng.standard_normal(V.shape)
+    warm[:] = 1
+    stepper = o.OracleStep(cfg)
+    for step in range(3):
+        q = rng.integers(-3, 4, (R, 1, H, d)).astype(np.float32)
+        w = rng.integers(0, 3, (R, 1, H)).astype(np.float32)
+        ns = np.array([n + step, n - 300 + step], np.int32)
+        out = stepper.run(V, D, warm, q, w, pool, None, bt, ns, ns - 1, 1, step)
+        assert out["ok"]
+        for r in range(R):
+            N = int(ns[r])
+            keys = pool[bt[r, np.arange(N) // 64], np.arange(N) % 64, 0]      # [N][d]
+            z = (np.maximum(np.einsum("nc,hc->nh", keys.astype(np.float64),
+                                      q[r, 0].astype(np.float64)), 0) * w[r, 0]).sum(-1)
+            order = np.lexsort((np.arange(N), -z))[:100]
+            np.testing.assert_array_equal(out["topk"][r, 0], np.sort(order))
