@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Benchmark of the SPIN decode-time indexer step on GB300.
+
+One step = one decode step of every layer of the workload: block selection, indexer score
+over the selected blocks, top-K and EMA update (select -> score -> top-K -> commit for the
+multi-row MTP workload), all through the C ABI.  Default workload: the DeepSeek-V3.2-like
+indexer (1 request, 4 layers, 131072 slots, 64 heads x 128 dims, a bf16 key per head,
+K = 2048) at 40 % target block sparsity.
+
+Prints one JSON line.  `value` is scored slots per second over all ranks (scored slots =
+slots of the selected blocks, times query rows); `e2e` repeats the measurement with the
+step's inputs copied from pinned host memory and the top-K indices copied back inside the
+timed region.  --impl reference times the CPU oracle instead (a bounded sample per step).
+
+Multi-GPU: replicas only (the indexer step has no exchange between requests or layers);
+each rank runs the whole workload on its own GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sparse_attention_indexer_spin_gb300 import synthetic as syn  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["spin", "reference"], default="spin")
+    p.add_argument("--config", default="v32", choices=sorted(syn.CONFIGS))
+    p.add_argument("--rho", type=int, default=None, help="target sparsity in basis points")
+    p.add_argument("--cpu-steps", type=int, default=8, help="oracle steps of the CPU baseline")
+    p.add_argument("--no-dense", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        except Exception:
+            uuid = None
+        self.uuid = uuid
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "sparse_attention_indexer_spin_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, kernel_file):
+    """DRAM bytes per launch of the score kernel from the committed ncu summary, if it was
+    taken on the current source of that kernel."""
+    path = os.path.join(ROOT, "profiles", "score_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash([kernel_file, "spin_common.cuh"]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------- CUDA workload
+
+class Workload:
+    def __init__(self, wl: syn.Workload, n_steps: int, rho_bp: int, share: "Workload" = None):
+        from sparse_attention_indexer_spin_gb300 import spin
+        self.spin = spin
+        self.wl = wl = wl.replace(steps=max(wl.steps, n_steps), rho_bp=rho_bp)
+        self.cfg = spin.make_config(**wl.config_fields())
+        self.rows = wl.rows
+        self.n_steps = n_steps
+        if share is not None:
+            # same inputs, own configuration and state (used for the dense comparison)
+            for k in ("inp", "L", "q", "w", "n_slots", "q_pos", "accepted"):
+                setattr(self, k, getattr(share, k))
+            self._alloc()
+            return
+        self.inp = syn.SyntheticInputs(wl, "cuda")
+        self.L = self.inp.n_layers
+        # per-step inputs: a ring of query sets, N and q positions for every step
+        ring = min(n_steps, 32)
+        self.q, self.w = [], []
+        for _ in range(ring):
+            ql, wl_ = [], []
+            for _layer in range(self.L):
+                q, w, _ = self.inp.step_inputs()
+                ql.append(q)
+                wl_.append(w)
+            self.q.append(ql)
+            self.w.append(wl_)
+        ns, acc = [], []
+        for s in range(n_steps):
+            ns.append(self.inp.n_slots.clone())
+            a = self.inp.draw_accepted().cuda() if self.rows > 1 else None
+            acc.append(a)
+            self.inp.advance(s, a)
+        self.n_slots = torch.stack(ns)                          # [steps][R]
+        self.q_pos = (self.n_slots - 1).clamp_min(0).to(torch.int32).contiguous()
+        self.accepted = acc
+        self._alloc()
+
+    def _alloc(self):
+        spin, n_steps, wl = self.spin, self.n_steps, self.wl
+        self.states = [spin.LayerState(self.cfg) for _ in range(self.L)]
+        self.buf = spin.StepBuffers(self.cfg, self.rows)
+        R, MB = wl.n_req, self.cfg.max_blocks
+        # per (step, layer) selections so the scored-slot count can be read back afterwards
+        self.blocks = torch.full((n_steps, self.L, R, self.rows, MB), -1, dtype=torch.int32, device="cuda")
+        self.n_blocks = torch.zeros((n_steps, self.L, R, self.rows), dtype=torch.int32, device="cuda")
+        self.unions = torch.full((n_steps, self.L, R, MB), -1, dtype=torch.int32, device="cuda")
+        self.n_unions = torch.zeros((n_steps, self.L, R), dtype=torch.int32, device="cuda")
+        self.reset()
+
+    def reset(self):
+        for st in self.states:
+            self.spin.init_state(self.cfg, st.V, st.D, st.Vmax, st.warm)
+
+    def launches_per_step(self):
+        return self.L * 5  # block scores, select, score, top-K, EMA
+
+    def step(self, s, ev_score=None, q_override=None, w_override=None, on_topk=None):
+        spin, cfg, buf, inp = self.spin, self.cfg, self.buf, self.inp
+        rows = self.rows
+        ns, qp = self.n_slots[s], self.q_pos[s]
+        for layer in range(self.L):
+            st = self.states[layer]
+            q = q_override[layer] if q_override is not None else self.q[s % len(self.q)][layer]
+            w = w_override[layer] if w_override is not None else self.w[s % len(self.w)][layer]
+            blocks, nb = self.blocks[s, layer], self.n_blocks[s, layer]
+            un, nu = (self.unions[s, layer], self.n_unions[s, layer]) if rows > 1 else (None, None)
+            spin.select_blocks(cfg, st.V, st.D, st.Vmax, st.warm, ns, qp, rows, None, s, layer,
+                               blocks, nb, un, nu, buf.workspace, buf.status)
+            lst, nl = (blocks, nb) if rows == 1 else (un, nu)
+            if ev_score is not None:
+                ev_score[0][layer].record()
+            spin.indexer_score(cfg, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
+                               inp.block_table, lst, nl, ns, rows, buf.scores, buf.status)
+            if ev_score is not None:
+                ev_score[1][layer].record()
+            spin.topk(cfg, buf.scores, lst, nl, ns, rows, buf.topk, buf.status)
+            if on_topk is not None:
+                on_topk(layer)
+            if rows == 1:
+                spin.update_ema(cfg, st.V, st.D, st.Vmax, st.warm, buf.scores, lst, nl, ns, qp,
+                                buf.status)
+            else:
+                spin.commit_mtp(cfg, st.V, st.D, st.Vmax, st.warm, buf.scores, rows, lst, nl, ns, qp,
+                                self.accepted[s], buf.status)
+
+    def scored_slots(self, steps):
+        """Slots scored per (step, layer) launch, times rows, from the recorded lists."""
+        out = []
+        ns_all = self.n_slots.cpu().numpy()
+        lists = (self.blocks[:, :, :, 0] if self.rows == 1 else self.unions).cpu().numpy()
+        counts = (self.n_blocks[:, :, :, 0] if self.rows == 1 else self.n_unions).cpu().numpy()
+        for s in steps:
+            for layer in range(self.L):
+                tot = 0
+                for r in range(self.wl.n_req):
+                    blks = lists[s, layer, r, : counts[s, layer, r]].astype(np.int64)
+                    tot += int(np.minimum(64, ns_all[s, r] - 64 * blks).clip(min=0).sum())
+                out.append(tot * self.rows)
+        return out
+
+    def key_bytes_per_slot(self):
+        wl = self.wl
+        elt = {"f32": 4, "bf16": 2, "e4m3": 1}[wl.k_dtype]
+        return wl.kv_heads * wl.head_dim * elt + (4 if wl.k_dtype == "e4m3" else 0)
+
+
+def time_steps(wk, steps, with_score_events=False):
+    """Run `steps` (list of step indices) and return (elapsed ms, per-score-launch ms list)."""
+    ev_pairs = []
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s in steps:
+        ev = None
+        if with_score_events:
+            ev = ([torch.cuda.Event(enable_timing=True) for _ in range(wk.L)],
+                  [torch.cuda.Event(enable_timing=True) for _ in range(wk.L)])
+            ev_pairs.append(ev)
+        wk.step(s, ev)
+    t1.record()
+    torch.cuda.synchronize()
+    score_ms = [a.elapsed_time(b) for ev in ev_pairs for a, b in zip(ev[0], ev[1])]
+    return t0.elapsed_time(t1), score_ms
+
+
+def time_e2e(wk, steps):
+    """Same steps with per-step inputs staged from pinned host memory and the top-K read
+    back to pinned host memory inside the timed region."""
+    L = wk.L
+    host_q = [[q.cpu().pin_memory() for q in ql] for ql in wk.q]
+    host_w = [[w.cpu().pin_memory() for w in wl_] for wl_ in wk.w]
+    host_ns = wk.n_slots.cpu().pin_memory()
+    dev_q = [torch.empty_like(q) for q in wk.q[0]]
+    dev_w = [torch.empty_like(w) for w in wk.w[0]]
+    host_topk = torch.empty((L,) + tuple(wk.buf.topk.shape), dtype=torch.int32).pin_memory()
+    h2d = sum(q.numel() * q.element_size() for q in host_q[0]) + \
+        sum(w.numel() * w.element_size() for w in host_w[0]) + host_ns[0].numel() * 4
+    d2h = host_topk.numel() * 4
+
+    def read_back(layer):
+        host_topk[layer].copy_(wk.buf.topk, non_blocking=True)
+
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s in steps:
+        i = s % len(host_q)
+        for layer in range(L):
+            dev_q[layer].copy_(host_q[i][layer], non_blocking=True)
+            dev_w[layer].copy_(host_w[i][layer], non_blocking=True)
+        wk.n_slots[s].copy_(host_ns[s], non_blocking=True)
+        wk.step(s, None, dev_q, dev_w, read_back)
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+# --------------------------------------------------------------------- CPU (oracle)
+
+def oracle_sample(wl: syn.Workload, inp_host, state, n_steps, blocks_per_step, seed_step=0):
+    """Time the CPU oracle on a bounded sample of the workload: per step, the selection of
+    one layer for request 0 over its whole context, then score, top-K and EMA over the
+    first `blocks_per_step` selected blocks.  Returns (slots/s, seconds, slots)."""
+    from oracle import oracle as o
+    ocfg = o.make_cfg(**{**wl.config_fields(), "n_req": 1})
+    V, D, warm = state
+    pool, scale, bt, q_list, w_list, ns, qp = inp_host
+    MB = o.max_blocks(ocfg)
+    slots = 0
+    t0 = time.perf_counter()
+    for s in range(n_steps):
+        blocks, nb, union, nu, _ = o.select_blocks(ocfg, V, D, warm, ns, qp, wl.rows, -1, seed_step + s, 0)
+        lst = union if wl.rows > 1 else np.ascontiguousarray(blocks[:, 0])
+        cnt = (nu if wl.rows > 1 else nb[:, 0]).copy()
+        cnt[0] = min(int(cnt[0]), blocks_per_step)
+        q, w = q_list[s % len(q_list)], w_list[s % len(w_list)]
+        sc, _ = o.indexer_score(ocfg, q, w, pool, scale, bt, lst, cnt, ns, wl.rows)
+        o.topk(ocfg, sc, lst, cnt, ns, wl.rows)
+        acc = np.zeros(1, np.int32) if wl.rows > 1 else None
+        o.replay_ema(ocfg, V, D, warm, sc, lst, cnt, ns, qp, wl.rows, acc)
+        blk = lst[0, : cnt[0]].astype(np.int64)
+        slots += int(np.minimum(64, int(ns[0]) - 64 * blk).clip(min=0).sum()) * wl.rows
+    dt = time.perf_counter() - t0
+    return slots / dt, dt, slots
+
+
+def host_inputs_for_oracle(wk_or_inp, wl, layer=0):
+    inp = wk_or_inp
+    pages = inp.block_table[0].long()
+    pool = syn.raw_numpy(inp.k_pool[layer][pages])
+    scale = None if inp.k_scale[layer] is None else syn.raw_numpy(inp.k_scale[layer][pages])
+    bt = np.arange(pages.numel(), dtype=np.int32)[None, :]
+    return pool, scale, bt
+
+
+def run_reference(args):
+    """The CPU oracle arm: each step a bounded sample of the workload on host cores."""
+    wl = syn.CONFIGS[args.config]
+    rho = wl.rho_bp if args.rho is None else args.rho
+    wl = wl.replace(rho_bp=rho)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = syn.SyntheticInputs(wl.replace(n_req=1), dev, layers=1)
+    pool, scale, bt = host_inputs_for_oracle(inp, wl)
+    q_list, w_list = [], []
+    for _ in range(4):
+        q, w, _ = inp.step_inputs()
+        q_list.append(syn.raw_numpy(q))
+        w_list.append(syn.raw_numpy(w))
+    from oracle import oracle as o
+    ocfg = o.make_cfg(**{**wl.config_fields(), "n_req": 1})
+    V, D, warm = o.new_state(ocfg)
+    ns = syn.raw_numpy(inp.n_slots).copy()
+    qp = (ns - 1).astype(np.int32)
+    bps = 64
+    # warm-up: one dense initialising step on a cheap sample, then the W warm-up steps
+    oracle_sample(wl, (pool, scale, bt, q_list, w_list, ns, qp), (V, D, warm), 1 + args.warmup, bps)
+    rate, secs, slots = oracle_sample(wl, (pool, scale, bt, q_list, w_list, ns, qp), (V, D, warm),
+                                      args.steps, bps, 1 + args.warmup)
+    line = {
+        "impl": "reference", "metric": "scored slots/s (SPIN indexer step)", "value": rate,
+        "unit": "slots/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "sample": "request 0, layer 0, %d selected blocks per step" % bps},
+        "cpu_baseline": {"kind": "oracle", "value": rate, "unit": "slots/s", "cores": 1,
+                         "sample": "per step: selection over the full context of request 0 (layer 0), "
+                                   "then score/top-K/EMA over its first %d selected blocks" % bps},
+        "e2e": {"value": rate, "unit": "slots/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------------- main
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from sparse_attention_indexer_spin_gb300 import spin
+    spin.lib()
+
+    base = syn.CONFIGS[args.config]
+    rho = base.rho_bp if args.rho is None else args.rho
+    W, K = max(args.warmup, 3), args.steps
+    wk = Workload(base, W + K, rho)
+    wl = wk.wl
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------------------------------------------------------- device-resident
+    wk.reset()
+    time_steps(wk, range(W))
+    barrier()
+    clocks = ClockSampler()
+    clocks.start()
+    ms, score_ms = time_steps(wk, range(W, W + K), with_score_events=True)
+    clk = clocks.stop()
+    barrier()
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    slots_per_launch = wk.scored_slots(range(W, W + K))
+    slots_total = sum(slots_per_launch)
+    value = slots_total * world / (ms_max / 1000.0)
+    ms_per_step = ms_max / K
+
+    # dominant kernel: the indexer score
+    avg_score_ms = float(np.mean(score_ms))
+    kbytes = wk.key_bytes_per_slot()
+    alg_bytes = float(np.mean(slots_per_launch)) * (kbytes + 4)   # keys (+scale) + score write
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (avg_score_ms / 1000.0) / 1e9
+    kernel_file = "spin_score_stream.cu" if wl.kv_heads > 1 else "spin_score_tc.cu"
+    traffic = ncu_traffic(wl.name, kernel_file)
+
+    # ---------------------------------------------------------------- dense comparison
+    dense = None
+    if not args.no_dense and rho != 0:
+        wd = Workload(base, W + K, 0, share=wk)
+        time_steps(wd, range(W))
+        msd, _ = time_steps(wd, range(W, W + K))
+        dense = {"rho": 0.0, "ms_per_step": msd / K, "latency_ratio": (ms / K) / (msd / K)}
+        del wd
+        torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- end to end
+    wk.reset()
+    time_steps(wk, range(W))
+    ms_e2e, h2d, d2h = time_e2e(wk, range(W, W + K))
+    e2e_value = slots_total * world / (ms_e2e / 1000.0)
+
+    # ---------------------------------------------------------------- CPU baseline
+    cpu = None
+    if rank == 0:
+        pool, scale, bt = host_inputs_for_oracle(wk.inp, wl)
+        q_list = [syn.raw_numpy(wk.q[i][0][:1]) for i in range(min(4, len(wk.q)))]
+        w_list = [syn.raw_numpy(wk.w[i][0][:1]) for i in range(min(4, len(wk.w)))]
+        st = wk.states[0]
+        state = (syn.raw_numpy(st.V[:1]).copy(), syn.raw_numpy(st.D[:1]).copy(),
+                 syn.raw_numpy(st.warm[:1]).copy())
+        ns = syn.raw_numpy(wk.n_slots[W + K - 1][:1]).copy()
+        qp = (ns - 1).astype(np.int32)
+        bps = 256
+        rate, secs, _ = oracle_sample(wl, (pool, scale, bt, q_list, w_list, ns, qp), state,
+                                      args.cpu_steps, bps, W + K)
+        cpu = {"kind": "oracle", "value": rate, "unit": "slots/s", "cores": 1,
+               "sample": "%d steps of request 0, layer 0: selection over the full context, then "
+                         "score/top-K/EMA over the first %d selected blocks (%.1f s)" % (args.cpu_steps, bps, secs)}
+
+    status = int(wk.buf.status.item())
+    if rank == 0:
+        line = {
+            "metric": "scored slots/s (SPIN indexer step)",
+            "value": value,
+            "unit": "slots/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": W,
+            "ms_per_step": ms_per_step,
+            "latency_us_per_layer_step": 1000.0 * ms_per_step / wk.L,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": wl.k_dtype if wl.k_dtype != "e4m3" else "e4m3/bf16",
+            "data": "synthetic",
+            "config": {"workload": "%s: %d req x %d layers, %d slots, %d heads x %d, kv_heads %d, %s keys, "
+                                   "K=%d, rho=%.0f%%, gamma=%.0f%%, rows=%d"
+                                   % (wl.name, wl.n_req, wk.L, base.n0, wl.n_heads, wl.head_dim, wl.kv_heads,
+                                      wl.k_dtype, wl.top_k, rho / 100, wl.gamma_bp / 100, wl.rows),
+                       "l2": "inputs larger than L2 (%.2f GB of keys per layer)"
+                             % (wk.inp.k_pool[0].numel() * wk.inp.k_pool[0].element_size() / 1e9),
+                       "parallelism": "replicas" if world > 1 else "1 GPU"},
+            "roofline": {"kernel": "indexer score (%s)" % kernel_file[:-3], "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": traffic,
+                         "alg_bytes_per_launch": alg_bytes, "avg_launch_us": 1000.0 * avg_score_ms},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "slots/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": wk.launches_per_step() * K,
+            "clocks": clk,
+            "dense": dense,
+            "status": status,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,193 @@
+/*
+ * spin.h -- C ABI of the SPIN (Shadow Predictive Indexer) decode-time indexer step
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Paper: "SPIN: Shadow Predictive Indexer for Sparse Attention" (arXiv 2610.09025).
+ * Per request, per layer and per decode step the library
+ *   1. predicts each 64-slot KV block's importance from two EMAs of past indexer scores
+ *      (Eq. 1, Eq. 2) and selects the layer's block budget: forced sink and newest
+ *      blocks, the top-ranked blocks and a random exploration share (Algorithm 1 lines
+ *      1-5, §3.2 practical details, §3.2.1)               -> spin_select_blocks
+ *   2. runs the indexer z[i] = sum_h w_h ReLU(q_h . k_{i,h}) over the slots of the
+ *      selected blocks only, read through a paged block table (§2, Alg. 1 line 6)
+ *                                                          -> spin_indexer_score
+ *   3. takes the post-indexer top-K of the fresh scores (Alg. 1 line 7) -> spin_topk
+ *   4. updates the vertical EMA V[i] and the diagonal EMA D[q-i] (Alg. 1 lines 8-10)
+ *                                                          -> spin_update_ema
+ *   and, for speculative decoding (§3.2.2), unions the masks of several verifier rows
+ *   (spin_select_blocks with rows > 1) and replays the EMA updates of the accepted
+ *   prefix of rows once verification is known (spin_commit_mtp).
+ *
+ * Conventions (every entry point):
+ *   - All pointers except `cfg` and `bytes` are DEVICE pointers owned by the caller; the
+ *     library allocates nothing and keeps no state between calls.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream): the host validates the configuration and sizes, then enqueues kernels.
+ *   - Host-side validation failures return an error code and enqueue nothing; the
+ *     message is available from spin_last_error_string() (thread-local).
+ *   - Values the host cannot see (N, q, block ids, page ids, accepted counts) are
+ *     checked by the kernels: a bad value sets a bit in the caller's `*status`
+ *     (atomicOr; may be NULL) and the affected request or block is skipped -- no
+ *     out-of-range access, no trap, no wait.
+ *
+ * Layouts (R = n_req, MB = ceil(max_slots / 64), DL = max_slots + max_rows, rows <= max_rows):
+ *   V        float  [R][max_slots]       vertical EMA per absolute slot i
+ *   D        float  [R][DL]              diagonal EMA per relative offset q - i
+ *   Vmax     float  [R][MB]              max of V over each block's 64 slots (kept exact)
+ *   warm     int32  [R]                  0 after a reset: the next selection is dense
+ *   n_slots  int32  [R]                  N, context length in KV slots (N <= max_slots)
+ *   q_pos    int32  [R]                  query position of row 0 (row r sits at q + r)
+ *   blocks   int32  [R][rows][MB]        per-row selection, ascending block ids
+ *   n_blocks int32  [R][rows]
+ *   list     int32  [R][MB], n_list [R]  a block list: a row-0 selection (rows == 1) or
+ *                                        the union of the rows' selections
+ *   q        [R][rows][n_heads][head_dim] in q_dtype (F32 or BF16)
+ *   w        float  [R][rows][n_heads]
+ *   k_pool   [n_pages][64][kv_heads][head_dim] in k_dtype (F32, BF16 or E4M3)
+ *   k_scale  float  [n_pages][64]        per-slot dequantisation scale (E4M3 only)
+ *   block_table int32 [R][bt_stride]     logical block j of request r -> page id
+ *   scores   float  [R][rows][MB*64]     slot s of list entry k at k*64 + s; slots
+ *                                        i >= N hold 0
+ *   topk_idx int32  [R][rows][top_k]     ascending slot ids, -1 padded
+ */
+#ifndef SPIN_H
+#define SPIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* spin_stream_t; /* a cudaStream_t */
+
+typedef enum spin_status {
+    SPIN_OK = 0,
+    SPIN_ERR_INVALID_ARG = 1,      /* NULL pointer, value out of range */
+    SPIN_ERR_SHAPE = 2,            /* inconsistent sizes (rows > max_rows, kv_heads, ...) */
+    SPIN_ERR_CAPACITY = 3,         /* a size beyond what the kernels support */
+    SPIN_ERR_UNSUPPORTED = 4,      /* dtype or score path not available for this shape */
+    SPIN_ERR_CUDA = 5              /* a CUDA runtime call or a launch failed */
+} spin_status_t;
+
+/* Bits of the device status word. */
+#define SPIN_STATUS_BAD_N        0x01u /* N < 0 or N > max_slots */
+#define SPIN_STATUS_BAD_QPOS     0x02u /* q < N - 1 or q + rows - 1 >= max_slots + max_rows */
+#define SPIN_STATUS_BAD_LIST     0x04u /* list count > MB or a listed block outside [0, ceil(N/64)) */
+#define SPIN_STATUS_BAD_PAGE     0x08u /* block-table entry outside [0, n_pages) */
+#define SPIN_STATUS_BAD_ACCEPTED 0x10u /* accepted outside [0, rows - 1] */
+#define SPIN_STATUS_TIMEOUT      0x20u /* a bounded wait inside a kernel gave up */
+#define SPIN_STATUS_BAD_RHO      0x40u /* budget override outside [0, 10000] */
+
+typedef enum spin_dtype { SPIN_DTYPE_F32 = 0, SPIN_DTYPE_BF16 = 1, SPIN_DTYPE_E4M3 = 2 } spin_dtype_t;
+
+/* Predicted slot score: Eq. 1's max(V[i], D[q-i]) (default) or the additive reading
+ * V[i] + D[q-i]. */
+typedef enum spin_combine { SPIN_COMBINE_MAX = 0, SPIN_COMBINE_SUM = 1 } spin_combine_t;
+
+/* Indexer-score kernel choice.  AUTO takes the tensor-core kernel when the key is shared
+ * by all heads (kv_heads == 1) and the shape is supported, the streaming CUDA-core
+ * kernel for per-head keys, and the generic kernel otherwise. */
+typedef enum spin_score_path {
+    SPIN_SCORE_AUTO = 0,
+    SPIN_SCORE_GENERIC = 1,   /* any shape; slow; a cross-check */
+    SPIN_SCORE_STREAM = 2,    /* per-head keys on CUDA cores, bulk-copy staged pages */
+    SPIN_SCORE_TCGEN05 = 3    /* shared key on tcgen05 tensor cores (TMA + TMEM) */
+} spin_score_path_t;
+
+typedef struct spin_config {
+    int32_t n_req;       /* R >= 1 */
+    int32_t max_slots;   /* capacity of V per request, 1 .. 2^24 */
+    int32_t max_rows;    /* verifier rows D leaves room for, 1 .. 8 */
+    int32_t block;       /* b: must be 64 (one KV page of compressed slots) */
+    int32_t n_heads;     /* n_h, 1 .. 128 */
+    int32_t head_dim;    /* d, 1 .. 256 */
+    int32_t kv_heads;    /* 1 (one key shared by all heads) or n_heads (a key per head) */
+    int32_t q_dtype;     /* SPIN_DTYPE_F32 or SPIN_DTYPE_BF16 */
+    int32_t k_dtype;     /* SPIN_DTYPE_F32, SPIN_DTYPE_BF16 or SPIN_DTYPE_E4M3 */
+    int32_t top_k;       /* K, 1 .. 16384 */
+    int32_t rho_bp;      /* target block sparsity rho in basis points, 0 .. 10000 */
+    int32_t gamma_bp;    /* exploration share gamma in basis points, 0 .. 10000 */
+    float alpha;         /* EMA decay, 0 .. 1 */
+    int32_t combine;     /* spin_combine_t */
+    uint64_t seed;       /* exploration key */
+    int32_t score_path;  /* spin_score_path_t */
+    int32_t reserved;    /* must be 0 */
+} spin_config;
+
+/* Zero V, D and Vmax and mark the request cold: the reset after prefill and at every
+ * turn start (§3.2 practical details).  req < 0 resets every request. */
+spin_status_t spin_init_state(const spin_config* cfg, float* V, float* D, float* Vmax,
+                              int32_t* warm, int32_t req, spin_stream_t stream);
+
+/* Block prediction and selection (Eq. 1, Eq. 2, Algorithm 1 lines 1-5; §3.2 forced blocks;
+ * §3.2.1 exploration; §3.2.2 union), for `rows` verifier rows of every request.
+ *   B = ceil(N/64); m = min(B, max(ceil(K/64), ceil((10000 - rho) B / 10000)));
+ *   forced F = {0, B-1}; e = min(floor(gamma m / 10000), m - |F|) (0 if m <= |F|);
+ *   the m - |F| - e non-forced blocks with the largest S (S desc, j asc), then the e
+ *   not-yet-selected blocks with the smallest exploration key, where the key of block j
+ *   is the high 32 bits of word 0 of Philox4x64-10(key = {seed, layer},
+ *   counter = {step, row, req, j}) (ties: lower j).  A cold request selects every block.
+ * rho_override: NULL, or a device int32 read by the kernel in place of cfg->rho_bp (a
+ *   per-layer budget table entry that CUDA graphs can replay).
+ * union_blocks/n_union: required when rows > 1 (ascending union of the rows), else may
+ *   be NULL.  workspace: at least spin_workspace_size(cfg, rows) bytes, 256-byte aligned. */
+spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const float* D,
+                                 const float* Vmax, const int32_t* warm,
+                                 const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
+                                 const int32_t* rho_override, uint64_t step, int32_t layer,
+                                 int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks,
+                                 int32_t* n_union, void* workspace, size_t workspace_bytes,
+                                 uint32_t* status, spin_stream_t stream);
+
+/* Indexer score (§2; Algorithm 1 line 6) of every slot of every listed block for `rows`
+ * query rows: z_r[i] = sum_h w[r][h] * ReLU(s_i * (q[r][h] . k[i][h'])), h' = h for
+ * per-head keys and 0 for a shared key, s_i = k_scale (E4M3) or 1.  fp32 accumulation.
+ * n_pages bounds the page ids of block_table (checked on the device). */
+spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const float* w,
+                                 const void* k_pool, const float* k_scale, int64_t n_pages,
+                                 const int32_t* block_table, int64_t bt_stride,
+                                 const int32_t* list, const int32_t* n_list,
+                                 const int32_t* n_slots, int32_t rows, float* scores,
+                                 uint32_t* status, spin_stream_t stream);
+
+/* Post-indexer top-K (Algorithm 1 line 7) of every row over the scored slots i < N of
+ * the list: the K largest z, equal z ordered by the lower slot id (-0 == +0); written
+ * as ascending slot ids and padded with -1 when fewer than K slots were scored. */
+spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32_t* list,
+                        const int32_t* n_list, const int32_t* n_slots, int32_t rows,
+                        int32_t* topk_idx, uint32_t* status, spin_stream_t stream);
+
+/* EMA update (Algorithm 1 lines 8-10) from the row-0 scores of the list:
+ *   t = fl((1 - alpha) z[i]);  V[i] = fma(alpha, V[i], t);  D[q-i] = fma(alpha, D[q-i], t)
+ * for every listed slot i < N; Vmax of the listed blocks is refreshed and the request
+ * is marked warm.  `scores` has the layout of a rows == 1 spin_indexer_score call. */
+spin_status_t spin_update_ema(const spin_config* cfg, float* V, float* D, float* Vmax,
+                              int32_t* warm, const float* scores, const int32_t* list,
+                              const int32_t* n_list, const int32_t* n_slots,
+                              const int32_t* q_pos, uint32_t* status, spin_stream_t stream);
+
+/* Deferred MTP commit (§3.2.2): with a = accepted[req] drafts accepted, replay the
+ * observations of rows 0..a in order (row r at query position q + r) with the update of
+ * spin_update_ema; rows a+1.. are discarded.  `scores` is the rows-row output of
+ * spin_indexer_score over the union list. */
+spin_status_t spin_commit_mtp(const spin_config* cfg, float* V, float* D, float* Vmax,
+                              int32_t* warm, const float* scores, int32_t rows,
+                              const int32_t* union_blocks, const int32_t* n_union,
+                              const int32_t* n_slots, const int32_t* q_pos,
+                              const int32_t* accepted, uint32_t* status, spin_stream_t stream);
+
+/* Bytes of device workspace spin_select_blocks needs for `rows` rows. */
+spin_status_t spin_workspace_size(const spin_config* cfg, int32_t rows, size_t* bytes);
+
+/* Version string of the library ("spin-gb300 <major>.<minor>.<patch> sm_103a"). */
+const char* spin_version(void);
+
+/* Message of the last host-side error of the calling thread ("" if none). */
+const char* spin_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPIN_H */

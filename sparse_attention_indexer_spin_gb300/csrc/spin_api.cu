@@ -1,0 +1,208 @@
+// spin_api.cu -- the C ABI (include/spin.h): host-side validation and kernel dispatch.
+//
+// Every entry point validates what the host can see (configuration, sizes, pointers),
+// records a message for spin_last_error_string() on failure, and otherwise enqueues the
+// kernels on the caller's stream.  Nothing is allocated, nothing is synchronised.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "spin_common.cuh"
+#include "spin_internal.h"
+
+namespace spin {
+
+static thread_local char g_err[512];
+
+static spin_status_t fail(spin_status_t code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static spin_status_t cuda_fail(cudaError_t e, const char* what) {
+    return fail(SPIN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+static spin_status_t check_cfg(const spin_config* c) {
+    g_err[0] = 0;
+    if (!c) return fail(SPIN_ERR_INVALID_ARG, "cfg is NULL");
+    if (c->block != kBlock) return fail(SPIN_ERR_INVALID_ARG, "block must be %d (got %d)", kBlock, c->block);
+    if (c->n_req < 1 || c->n_req > 65535) return fail(SPIN_ERR_INVALID_ARG, "n_req %d outside [1, 65535]", c->n_req);
+    if (c->max_slots < 1 || c->max_slots > (1 << 24))
+        return fail(SPIN_ERR_CAPACITY, "max_slots %d outside [1, 2^24]", c->max_slots);
+    if (c->max_rows < 1 || c->max_rows > kMaxRows)
+        return fail(SPIN_ERR_INVALID_ARG, "max_rows %d outside [1, %d]", c->max_rows, kMaxRows);
+    if (c->n_heads < 1 || c->n_heads > 128) return fail(SPIN_ERR_INVALID_ARG, "n_heads %d outside [1, 128]", c->n_heads);
+    if (c->head_dim < 1 || c->head_dim > 256)
+        return fail(SPIN_ERR_INVALID_ARG, "head_dim %d outside [1, 256]", c->head_dim);
+    if (c->kv_heads != 1 && c->kv_heads != c->n_heads)
+        return fail(SPIN_ERR_SHAPE, "kv_heads must be 1 or n_heads (got %d, n_heads %d)", c->kv_heads, c->n_heads);
+    if (c->q_dtype != SPIN_DTYPE_F32 && c->q_dtype != SPIN_DTYPE_BF16)
+        return fail(SPIN_ERR_UNSUPPORTED, "q_dtype %d: F32 or BF16 only", c->q_dtype);
+    if (c->k_dtype != SPIN_DTYPE_F32 && c->k_dtype != SPIN_DTYPE_BF16 && c->k_dtype != SPIN_DTYPE_E4M3)
+        return fail(SPIN_ERR_UNSUPPORTED, "k_dtype %d: F32, BF16 or E4M3 only", c->k_dtype);
+    if (c->top_k < 1 || c->top_k > 16384) return fail(SPIN_ERR_INVALID_ARG, "top_k %d outside [1, 16384]", c->top_k);
+    if (c->rho_bp < 0 || c->rho_bp > 10000) return fail(SPIN_ERR_INVALID_ARG, "rho_bp %d outside [0, 10000]", c->rho_bp);
+    if (c->gamma_bp < 0 || c->gamma_bp > 10000)
+        return fail(SPIN_ERR_INVALID_ARG, "gamma_bp %d outside [0, 10000]", c->gamma_bp);
+    if (!(c->alpha >= 0.0f && c->alpha <= 1.0f)) return fail(SPIN_ERR_INVALID_ARG, "alpha outside [0, 1]");
+    if (c->combine != SPIN_COMBINE_MAX && c->combine != SPIN_COMBINE_SUM)
+        return fail(SPIN_ERR_INVALID_ARG, "combine %d unknown", c->combine);
+    if (c->score_path < SPIN_SCORE_AUTO || c->score_path > SPIN_SCORE_TCGEN05)
+        return fail(SPIN_ERR_INVALID_ARG, "score_path %d unknown", c->score_path);
+    if (c->reserved != 0) return fail(SPIN_ERR_INVALID_ARG, "reserved must be 0");
+    return SPIN_OK;
+}
+
+static spin_status_t check_rows(const spin_config* c, int rows) {
+    if (rows < 1 || rows > c->max_rows) return fail(SPIN_ERR_SHAPE, "rows %d outside [1, max_rows=%d]", rows, c->max_rows);
+    if ((int64_t)c->n_req * rows > 65535) return fail(SPIN_ERR_CAPACITY, "n_req * rows above 65535");
+    return SPIN_OK;
+}
+
+static spin_status_t launched(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return SPIN_OK;
+    return cuda_fail(e, what);
+}
+
+}  // namespace spin
+
+using namespace spin;
+
+extern "C" {
+
+spin_status_t spin_init_state(const spin_config* cfg, float* V, float* D, float* Vmax, int32_t* warm, int32_t req,
+                              spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if (!V || !D || !Vmax || !warm) return fail(SPIN_ERR_INVALID_ARG, "V, D, Vmax and warm must be non-NULL");
+    if (req >= cfg->n_req) return fail(SPIN_ERR_INVALID_ARG, "req %d >= n_req %d", req, cfg->n_req);
+    return launched(launch_init_state(*cfg, V, D, Vmax, warm, req, (cudaStream_t)stream), "spin_init_state");
+}
+
+spin_status_t spin_workspace_size(const spin_config* cfg, int32_t rows, size_t* bytes) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    if (!bytes) return fail(SPIN_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = select_workspace_bytes(*cfg, rows);
+    return SPIN_OK;
+}
+
+spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
+                                 const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
+                                 const int32_t* rho_override, uint64_t step, int32_t layer, int32_t* blocks,
+                                 int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union, void* workspace,
+                                 size_t workspace_bytes, uint32_t* status, spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    const Dims dm = dims_of(*cfg);
+    if (dm.MB > kSelectMaxBlocks)
+        return fail(SPIN_ERR_CAPACITY, "max_slots %d needs %d blocks; selection supports %d", cfg->max_slots, dm.MB,
+                    kSelectMaxBlocks);
+    if (!V || !D || !Vmax || !warm || !n_slots || !q_pos || !blocks || !n_blocks)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (rows > 1 && (!union_blocks || !n_union))
+        return fail(SPIN_ERR_INVALID_ARG, "rows > 1 needs union_blocks and n_union");
+    if ((union_blocks == nullptr) != (n_union == nullptr))
+        return fail(SPIN_ERR_INVALID_ARG, "union_blocks and n_union go together");
+    const size_t need = select_workspace_bytes(*cfg, rows);
+    if (!workspace || workspace_bytes < need)
+        return fail(SPIN_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
+    if (((uintptr_t)workspace & 255) != 0) return fail(SPIN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer, blocks, n_blocks,
+                 union_blocks, n_union, reinterpret_cast<float*>(workspace), status};
+    return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks");
+}
+
+spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const float* w, const void* k_pool,
+                                 const float* k_scale, int64_t n_pages, const int32_t* block_table, int64_t bt_stride,
+                                 const int32_t* list, const int32_t* n_list, const int32_t* n_slots, int32_t rows,
+                                 float* scores, uint32_t* status, spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    const Dims dm = dims_of(*cfg);
+    if (!q || !w || !k_pool || !block_table || !list || !n_list || !n_slots || !scores)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (cfg->k_dtype == SPIN_DTYPE_E4M3 && !k_scale) return fail(SPIN_ERR_INVALID_ARG, "E4M3 keys need k_scale");
+    if (n_pages < 0) return fail(SPIN_ERR_INVALID_ARG, "n_pages < 0");
+    if (bt_stride < dm.MB) return fail(SPIN_ERR_SHAPE, "bt_stride %lld < max blocks %d", (long long)bt_stride, dm.MB);
+    if (((uintptr_t)k_pool & 15) != 0 || (k_scale && ((uintptr_t)k_scale & 15) != 0))
+        return fail(SPIN_ERR_INVALID_ARG, "k_pool and k_scale must be 16-byte aligned");
+    ScoreArgs a{q, w, k_pool, cfg->k_dtype == SPIN_DTYPE_E4M3 ? k_scale : nullptr, n_pages, block_table, bt_stride,
+                list, n_list, n_slots, rows, scores, status};
+    int path = cfg->score_path;
+    if (path == SPIN_SCORE_AUTO) {
+        if (score_tc_supported(*cfg, rows)) path = SPIN_SCORE_TCGEN05;
+        else if (score_stream_supported(*cfg, rows)) path = SPIN_SCORE_STREAM;
+        else path = SPIN_SCORE_GENERIC;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    switch (path) {
+        case SPIN_SCORE_GENERIC:
+            return launched(launch_score_generic(*cfg, a, s), "spin_indexer_score (generic)");
+        case SPIN_SCORE_STREAM:
+            if (!score_stream_supported(*cfg, rows))
+                return fail(SPIN_ERR_UNSUPPORTED, "no streaming kernel for this shape (needs per-head keys)");
+            return launched(launch_score_stream(*cfg, a, s), "spin_indexer_score (stream)");
+        case SPIN_SCORE_TCGEN05:
+            if (!score_tc_supported(*cfg, rows))
+                return fail(SPIN_ERR_UNSUPPORTED, "no tcgen05 kernel for this shape (needs a shared key)");
+            return launched(launch_score_tc(*cfg, a, s), "spin_indexer_score (tcgen05)");
+    }
+    return fail(SPIN_ERR_INVALID_ARG, "score_path");
+}
+
+spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32_t* list, const int32_t* n_list,
+                        const int32_t* n_slots, int32_t rows, int32_t* topk_idx, uint32_t* status,
+                        spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    if (!scores || !list || !n_list || !n_slots || !topk_idx) return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    return launched(launch_topk(*cfg, scores, list, n_list, n_slots, rows, topk_idx, status, (cudaStream_t)stream),
+                    "spin_topk");
+}
+
+spin_status_t spin_update_ema(const spin_config* cfg, float* V, float* D, float* Vmax, int32_t* warm,
+                              const float* scores, const int32_t* list, const int32_t* n_list, const int32_t* n_slots,
+                              const int32_t* q_pos, uint32_t* status, spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if (!V || !D || !Vmax || !warm || !scores || !list || !n_list || !n_slots || !q_pos)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    EmaArgs a{V, D, Vmax, warm, scores, 1, list, n_list, n_slots, q_pos, nullptr, status};
+    return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_update_ema");
+}
+
+spin_status_t spin_commit_mtp(const spin_config* cfg, float* V, float* D, float* Vmax, int32_t* warm,
+                              const float* scores, int32_t rows, const int32_t* union_blocks, const int32_t* n_union,
+                              const int32_t* n_slots, const int32_t* q_pos, const int32_t* accepted, uint32_t* status,
+                              spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    if (!V || !D || !Vmax || !warm || !scores || !union_blocks || !n_union || !n_slots || !q_pos || !accepted)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    EmaArgs a{V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots, q_pos, accepted, status};
+    return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_commit_mtp");
+}
+
+const char* spin_version(void) { return "spin-gb300 0.1.0 sm_103a"; }
+
+const char* spin_last_error_string(void) { return g_err; }
+
+}  // extern "C"

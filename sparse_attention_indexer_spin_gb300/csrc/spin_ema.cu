@@ -1,0 +1,167 @@
+// spin_ema.cu -- EMA update and the deferred MTP replay.
+//
+// "SPIN: Shadow Predictive Indexer for Sparse Attention":
+//   Algorithm 1 lines 8-10: for every scored slot i,
+//       V[i]   <- alpha V[i]   + (1 - alpha) z[i]
+//       D[q-i] <- alpha D[q-i] + (1 - alpha) z[i]
+//   §3.2.2: with a drafts accepted, the observations of verifier rows 0..a are replayed in
+//   order (row r at position q + r); rows above a are discarded.
+//
+// Both are one kernel: a CTA owns 1024 consecutive slots of one request.  V[i] is a chain
+// over the rows r = 0..a at slot i; D[o] is a chain over r at offset o, the slot being
+// i = q + r - o.  The CTA owning slot i0 owns offset q - i0 (and the CTA of slot 0 also the
+// offsets q+1..q+a), so every location is written by one thread that applies its updates
+// in row order: the result is bit-identical to a sequential replay.  The arithmetic is
+// t = fl((1 - alpha) z), v = fma(alpha, v, t), with (1 - alpha) rounded to fp32 once.
+// Afterwards Vmax (the per-block max of V that block prediction reads) is refreshed for
+// the CTA's listed blocks.
+#include <float.h>
+
+#include "spin_common.cuh"
+#include "spin_internal.h"
+
+namespace spin {
+
+constexpr int kEmaSpan = 1024;
+constexpr int kEmaThreads = 256;
+constexpr int kEmaMapBlocks = kEmaSpan / kBlock + 2;
+
+__global__ void __launch_bounds__(kEmaThreads) ema_replay_kernel(spin_config cfg, EmaArgs a) {
+    extern __shared__ float zs[];  // [(a+1)][span]
+    __shared__ int pos[kEmaMapBlocks];
+    const Dims dm = dims_of(cfg);
+    const int req = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+    const int rows = a.rows;
+    const int64_t n = a.n_slots[req], q = a.q_pos[req], cnt = a.n_list[req];
+    const int A = a.accepted ? a.accepted[req] : 0;
+    uint32_t bad = request_check(n, q, rows, dm);
+    if (cnt < 0 || cnt > dm.MB) bad |= SPIN_STATUS_BAD_LIST;
+    if (A < 0 || A >= rows) bad |= SPIN_STATUS_BAD_ACCEPTED;
+    if (bad) {
+        if (c == 0 && tid == 0) set_status(a.status, bad);
+        return;
+    }
+    if (c == 0 && tid == 0) a.warm[req] = 1;
+    const int64_t lo = (int64_t)c * kEmaSpan;
+    if (lo >= n && c > 0) return;
+    const int64_t hi = (lo + kEmaSpan < n) ? lo + kEmaSpan : n;  // may be <= lo when n == 0
+    const int64_t nb = (n + kBlock - 1) / kBlock;
+    const int64_t blk_lo = lo / kBlock;
+    const int64_t span = (hi > lo ? hi - lo : 0) + A;  // staged slots [lo, lo + span)
+    const int32_t* lst = a.list + (int64_t)req * dm.MB;
+
+    // union position of each block touching [lo, lo + span), or -1
+    if (tid == 0) {
+        for (int b = 0; b < kEmaMapBlocks; ++b) pos[b] = -1;
+        int64_t l = 0, h = cnt;  // first entry >= blk_lo
+        while (l < h) {
+            const int64_t m = (l + h) >> 1;
+            if (lst[m] < blk_lo) l = m + 1; else h = m;
+        }
+        bool bad_list = false;
+        for (int64_t k = l; k < cnt; ++k) {
+            const int64_t blk = lst[k];
+            if (blk < 0 || blk >= nb) { bad_list = true; break; }
+            const int64_t b = blk - blk_lo;
+            if (b >= kEmaMapBlocks) break;
+            pos[b] = (int)k;
+        }
+        if (bad_list) set_status(a.status, SPIN_STATUS_BAD_LIST);
+    }
+    __syncthreads();
+    auto scored = [&](int64_t i) -> int {  // union position of slot i's block, or -1
+        if (i < 0 || i >= n || i < lo) return -1;
+        const int64_t b = i / kBlock - blk_lo;
+        return (b < kEmaMapBlocks) ? pos[b] : -1;
+    };
+
+    // stage the observations z_r[i], r <= A, i in [lo, lo + span)
+    for (int64_t idx = tid; idx < (int64_t)(A + 1) * span; idx += kEmaThreads) {
+        const int r = (int)(idx / span);
+        const int64_t i = lo + (idx - (int64_t)r * span);
+        const int p = scored(i);
+        zs[idx] = p >= 0 ? a.scores[(((int64_t)req * rows + r) * dm.MB + p) * kBlock + (i & 63)] : 0.0f;
+    }
+    __syncthreads();
+
+    const float alpha = cfg.alpha;
+    const float oma = 1.0f - cfg.alpha;
+    float* Vq = a.V + (int64_t)req * dm.max_slots;
+    float* Dq = a.D + (int64_t)req * dm.DL;
+
+    // V chains
+    for (int64_t i = lo + tid; i < hi; i += kEmaThreads) {
+        if (scored(i) < 0) continue;
+        float v = Vq[i];
+        for (int r = 0; r <= A; ++r) v = __fmaf_rn(alpha, v, __fmul_rn(oma, zs[(int64_t)r * span + (i - lo)]));
+        Vq[i] = v;
+    }
+    // D chains: offsets o = q - i0 for i0 in [lo_d, hi)
+    const int64_t lo_d = (c == 0) ? -(int64_t)A : lo;
+    for (int64_t i0 = lo_d + tid; i0 < hi; i0 += kEmaThreads) {
+        const int64_t o = q - i0;
+        float d = 0.0f;
+        bool any = false;
+        for (int r = 0; r <= A; ++r) {
+            const int64_t i = i0 + r;
+            if (scored(i) < 0) continue;
+            if (!any) { d = Dq[o]; any = true; }
+            d = __fmaf_rn(alpha, d, __fmul_rn(oma, zs[(int64_t)r * span + (i - lo)]));
+        }
+        if (any) Dq[o] = d;
+    }
+    __syncthreads();
+
+    // Vmax of the listed blocks that start inside [lo, hi): one warp per block
+    const int lane = tid & 31, wid = tid >> 5;
+    for (int b = wid; b < kEmaSpan / kBlock; b += kEmaThreads / 32) {
+        const int64_t blk = blk_lo + b;
+        if (blk * kBlock >= hi || pos[b] < 0) continue;
+        const int64_t i0 = blk * kBlock + lane, i1 = i0 + 32;
+        float m = -FLT_MAX;
+        if (i0 < dm.max_slots) m = Vq[i0];
+        if (i1 < dm.max_slots) m = fmaxf(m, Vq[i1]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) a.Vmax[(int64_t)req * dm.MB + blk] = m;
+    }
+}
+
+cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s) {
+    const Dims dm = dims_of(cfg);
+    const int gx = (dm.max_slots + kEmaSpan - 1) / kEmaSpan;
+    dim3 grid(gx > 0 ? gx : 1, dm.R);
+    const size_t smem = sizeof(float) * (size_t)a.rows * (kEmaSpan + a.rows);
+    ema_replay_kernel<<<grid, kEmaThreads, smem, s>>>(cfg, a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------
+// Reset after prefill / at a turn start (§3.2 practical details).
+// ---------------------------------------------------------------------------------------
+__global__ void init_state_kernel(spin_config cfg, float* V, float* D, float* Vmax, int32_t* warm, int req0,
+                                  int nreq) {
+    const Dims dm = dims_of(cfg);
+    const int64_t nv = (int64_t)nreq * dm.max_slots, nd = (int64_t)nreq * dm.DL, nm = (int64_t)nreq * dm.MB;
+    float* V0 = V + (int64_t)req0 * dm.max_slots;
+    float* D0 = D + (int64_t)req0 * dm.DL;
+    float* M0 = Vmax + (int64_t)req0 * dm.MB;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv + nd + nm + nreq; i += stride) {
+        if (i < nv) V0[i] = 0.0f;
+        else if (i < nv + nd) D0[i - nv] = 0.0f;
+        else if (i < nv + nd + nm) M0[i - nv - nd] = 0.0f;
+        else warm[req0 + (i - nv - nd - nm)] = 0;
+    }
+}
+
+cudaError_t launch_init_state(const spin_config& cfg, float* V, float* D, float* Vmax, int32_t* warm, int req,
+                              cudaStream_t s) {
+    const int req0 = req < 0 ? 0 : req;
+    const int nreq = req < 0 ? cfg.n_req : 1;
+    const int grid = device_sm_count() * 4;
+    init_state_kernel<<<grid, 256, 0, s>>>(cfg, V, D, Vmax, warm, req0, nreq);
+    return cudaGetLastError();
+}
+
+}  // namespace spin

@@ -1,0 +1,80 @@
+// spin_internal.h -- host-side launchers of the SPIN kernels (called by spin_api.cu only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/spin.h"
+
+namespace spin {
+
+struct SelectArgs {
+    const float* V;
+    const float* D;
+    const float* Vmax;
+    const int32_t* warm;
+    const int32_t* n_slots;
+    const int32_t* q_pos;
+    int rows;
+    const int32_t* rho_override;
+    uint64_t step;
+    int layer;
+    int32_t* blocks;
+    int32_t* n_blocks;
+    int32_t* union_blocks;
+    int32_t* n_union;
+    float* block_scores;  // workspace [R][rows][MB]
+    uint32_t* status;
+};
+
+struct ScoreArgs {
+    const void* q;
+    const float* w;
+    const void* k_pool;
+    const float* k_scale;
+    int64_t n_pages;
+    const int32_t* block_table;
+    int64_t bt_stride;
+    const int32_t* list;
+    const int32_t* n_list;
+    const int32_t* n_slots;
+    int rows;
+    float* scores;
+    uint32_t* status;
+};
+
+struct EmaArgs {
+    float* V;
+    float* D;
+    float* Vmax;
+    int32_t* warm;
+    const float* scores;
+    int rows;
+    const int32_t* list;
+    const int32_t* n_list;
+    const int32_t* n_slots;
+    const int32_t* q_pos;
+    const int32_t* accepted;  // NULL: a = 0
+    uint32_t* status;
+};
+
+size_t select_workspace_bytes(const spin_config& cfg, int rows);
+
+cudaError_t launch_init_state(const spin_config& cfg, float* V, float* D, float* Vmax,
+                              int32_t* warm, int req, cudaStream_t s);
+cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_score_generic(const spin_config& cfg, const ScoreArgs& a, cudaStream_t s);
+// Returns cudaErrorNotSupported when the shape has no streaming kernel instance.
+cudaError_t launch_score_stream(const spin_config& cfg, const ScoreArgs& a, cudaStream_t s);
+bool score_stream_supported(const spin_config& cfg, int rows);
+cudaError_t launch_score_tc(const spin_config& cfg, const ScoreArgs& a, cudaStream_t s);
+bool score_tc_supported(const spin_config& cfg, int rows);
+cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32_t* list,
+                        const int32_t* n_list, const int32_t* n_slots, int rows,
+                        int32_t* topk_idx, uint32_t* status, cudaStream_t s);
+cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace spin
