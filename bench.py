@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--rho", type=int, default=None, help="target sparsity in basis points")
     p.add_argument("--cpu-steps", type=int, default=8, help="oracle steps of the CPU baseline")
     p.add_argument("--no-dense", action="store_true")
+    p.add_argument("--layers", type=int, default=None, help="fewer layers (small profiling case)")
+    p.add_argument("--n0", type=int, default=None, help="fewer slots per request (small profiling case)")
     return p.parse_args()
 
 
@@ -389,6 +391,10 @@ def main():
     spin.lib()
 
     base = syn.CONFIGS[args.config]
+    if args.layers is not None:
+        base = base.replace(n_layers=args.layers)
+    if args.n0 is not None:
+        base = base.replace(n0=args.n0)
     rho = base.rho_bp if args.rho is None else args.rho
     W, K = max(args.warmup, 3), args.steps
     wk = Workload(base, W + K, rho)

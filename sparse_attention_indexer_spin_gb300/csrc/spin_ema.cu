@@ -50,23 +50,43 @@ __global__ void __launch_bounds__(kEmaThreads) ema_replay_kernel(spin_config cfg
     const int64_t span = (hi > lo ? hi - lo : 0) + A;  // staged slots [lo, lo + span)
     const int32_t* lst = a.list + (int64_t)req * dm.MB;
 
-    // union position of each block touching [lo, lo + span), or -1
-    if (tid == 0) {
-        for (int b = 0; b < kEmaMapBlocks; ++b) pos[b] = -1;
-        int64_t l = 0, h = cnt;  // first entry >= blk_lo
-        while (l < h) {
-            const int64_t m = (l + h) >> 1;
-            if (lst[m] < blk_lo) l = m + 1; else h = m;
+    // union position of each block touching [lo, lo + span), or -1: warp 0 finds the first
+    // list entry >= blk_lo with a 32-way search (a few dependent loads), then maps the
+    // next entries
+    if (tid < 32) {
+        const int lane = tid;
+        int64_t l = 0, h = cnt;  // the answer lies in [l, h]
+        while (h - l > 32) {
+            const int64_t step = (h - l + 31) / 32;
+            const int64_t p = l + (int64_t)lane * step;
+            const bool ge = p >= h || lst[p] >= blk_lo;
+            const unsigned b = __ballot_sync(0xffffffffu, ge);
+            if (b == 0u) {
+                l = l + 31 * step + 1;
+            } else {
+                const int f = __ffs(b) - 1;
+                if (f == 0) { h = l; }
+                else {
+                    const int64_t hf = l + (int64_t)f * step;
+                    h = hf < h ? hf : h;
+                    l = l + (int64_t)(f - 1) * step + 1;
+                }
+            }
         }
+        const int64_t p = l + lane;
+        const bool ge = p >= h || lst[p] >= blk_lo;
+        const unsigned b = __ballot_sync(0xffffffffu, ge);
+        const int64_t first = b ? l + (__ffs(b) - 1) : h;
+        if (lane < kEmaMapBlocks) pos[lane] = -1;
+        __syncwarp();
         bool bad_list = false;
-        for (int64_t k = l; k < cnt; ++k) {
+        const int64_t k = first + lane;
+        if (lane < kEmaMapBlocks && k < cnt) {
             const int64_t blk = lst[k];
-            if (blk < 0 || blk >= nb) { bad_list = true; break; }
-            const int64_t b = blk - blk_lo;
-            if (b >= kEmaMapBlocks) break;
-            pos[b] = (int)k;
+            if (blk < 0 || blk >= nb) bad_list = true;
+            else if (blk - blk_lo < kEmaMapBlocks) pos[blk - blk_lo] = (int)k;
         }
-        if (bad_list) set_status(a.status, SPIN_STATUS_BAD_LIST);
+        if (__any_sync(0xffffffffu, bad_list) && lane == 0) set_status(a.status, SPIN_STATUS_BAD_LIST);
     }
     __syncthreads();
     auto scored = [&](int64_t i) -> int {  // union position of slot i's block, or -1

@@ -101,9 +101,17 @@ __device__ void top_select(const uint32_t* keys, uint8_t* flag, int n, int k, ui
         const int shift = 24 - 8 * pass;
         for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0;
         __syncthreads();
-        for (int j = tid; j < n; j += kSelThreads) {
-            const uint32_t key = keys[j];
-            if (flag[j] == 0 && (key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1);
+        // warp-aggregated shared atomics: block scores share their high bits, so many
+        // lanes hit the same bin
+        const int n_pad = (n + 31) & ~31;
+        for (int j = tid; j < n_pad; j += kSelThreads) {
+            int bin = -1;
+            if (j < n) {
+                const uint32_t key = keys[j];
+                if (flag[j] == 0 && (key & mask) == prefix) bin = (int)((key >> shift) & 255u);
+            }
+            const unsigned same = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&sh.hist[bin], __popc(same));
         }
         __syncthreads();
         if (wid == 0) {
