@@ -20,7 +20,8 @@
  *
  * Conventions (every entry point):
  *   - All pointers except `cfg` and `bytes` are DEVICE pointers owned by the caller; the
- *     library allocates nothing and keeps no state between calls.
+ *     library allocates nothing and keeps no state between calls (except the built-in
+ *     scratch array of spin_select_blocks_noalloc, see there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream): the host validates the configuration and sizes, then enqueues kernels.
  *   - Host-side validation failures return an error code and enqueue nothing; the
@@ -140,6 +141,31 @@ spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const f
                                  int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks,
                                  int32_t* n_union, void* workspace, size_t workspace_bytes,
                                  uint32_t* status, spin_stream_t stream);
+
+/* Allocation-free variant of spin_select_blocks (the paper has no counterpart: this is a
+ * deployment convenience).  Some callers cannot allocate device memory for the workspace:
+ * serving engines that reserve all device memory up front in their own pool and forbid
+ * other allocations, plugin hosts that give the library no allocator, and latency-critical
+ * loops that must not pay for an allocation.  This entry point takes the same arguments
+ * minus the workspace and uses instead a scratch array that lives in the library itself
+ * (a static device array of 4 MiB, held on every GPU that loads the library until the
+ * process exits).  It calls no cudaMalloc/cudaFree and no allocating library routine.
+ *   - Capacity: n_req * rows * ceil(max_slots/64) <= 1048576 (one float per block and
+ *     row); larger configurations are rejected with SPIN_ERR_CAPACITY.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents: calls that
+ *     may overlap on the GPU (different streams, or different host threads, on one
+ *     device) race on it and must be serialised by the caller.
+ * Outputs are identical to spin_select_blocks. */
+spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V, const float* D,
+                                         const float* Vmax, const int32_t* warm,
+                                         const int32_t* n_slots, const int32_t* q_pos,
+                                         int32_t rows, const int32_t* rho_override,
+                                         uint64_t step, int32_t layer, int32_t* blocks,
+                                         int32_t* n_blocks, int32_t* union_blocks,
+                                         int32_t* n_union, uint32_t* status,
+                                         spin_stream_t stream);
 
 /* Indexer score (§2; Algorithm 1 line 6) of every slot of every listed block for `rows`
  * query rows: z_r[i] = sum_h w[r][h] * ReLU(s_i * (q[r][h] . k[i][h'])), h' = h for

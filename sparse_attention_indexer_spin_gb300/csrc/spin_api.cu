@@ -127,6 +127,76 @@ spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const f
     return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks");
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free selection: the block-score scratch lives in this static device array
+// instead of a caller workspace, for callers that cannot allocate device memory.  The
+// array's device address is looked up once per device (with that device current) on the
+// first call and cached; calls that overlap on one device race on the array.
+// ---------------------------------------------------------------------------------------
+namespace spin {
+
+constexpr size_t kNoAllocScratchFloats = (size_t)1 << 20;  // 4 MiB
+static __device__ __align__(256) float g_select_scratch[kNoAllocScratchFloats];
+
+constexpr int kMaxDevices = 128;
+static std::mutex g_scratch_mu;
+static float* g_scratch_addr[kMaxDevices];
+
+static spin_status_t scratch_of_current_device(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "spin_select_blocks_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(SPIN_ERR_CAPACITY, "device ordinal %d above %d", dev, kMaxDevices);
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_select_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                             "spin_select_blocks_noalloc: cudaGetSymbolAddress of the scratch array");
+        g_scratch_addr[dev] = reinterpret_cast<float*>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return SPIN_OK;
+}
+
+}  // namespace spin
+
+extern "C" {
+
+spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
+                                         const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos,
+                                         int32_t rows, const int32_t* rho_override, uint64_t step, int32_t layer,
+                                         int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks,
+                                         int32_t* n_union, uint32_t* status, spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    const Dims dm = dims_of(*cfg);
+    if (dm.MB > kSelectMaxBlocks)
+        return fail(SPIN_ERR_CAPACITY, "max_slots %d needs %d blocks; selection supports %d", cfg->max_slots, dm.MB,
+                    kSelectMaxBlocks);
+    const size_t need = (size_t)dm.R * (size_t)rows * (size_t)dm.MB;
+    if (need > kNoAllocScratchFloats)
+        return fail(SPIN_ERR_CAPACITY,
+                    "spin_select_blocks_noalloc: n_req * rows * max_blocks = %zu exceeds its built-in scratch of %zu "
+                    "entries; use spin_select_blocks with a workspace",
+                    need, kNoAllocScratchFloats);
+    if (!V || !D || !Vmax || !warm || !n_slots || !q_pos || !blocks || !n_blocks)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (rows > 1 && (!union_blocks || !n_union))
+        return fail(SPIN_ERR_INVALID_ARG, "rows > 1 needs union_blocks and n_union");
+    if ((union_blocks == nullptr) != (n_union == nullptr))
+        return fail(SPIN_ERR_INVALID_ARG, "union_blocks and n_union go together");
+    float* scratch = nullptr;
+    if ((st = scratch_of_current_device(&scratch))) return st;
+    SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer, blocks, n_blocks,
+                 union_blocks, n_union, scratch, status};
+    return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks_noalloc");
+}
+
 spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const float* w, const void* k_pool,
                                  const float* k_scale, int64_t n_pages, const int32_t* block_table, int64_t bt_stride,
                                  const int32_t* list, const int32_t* n_list, const int32_t* n_slots, int32_t rows,

@@ -86,6 +86,7 @@ def lib():
             "spin_init_state": [C, P, P, P, P, i32, P],
             "spin_select_blocks": [C, P, P, P, P, P, P, i32, P, u64, i32, P, P, P, P, P,
                                    ctypes.c_size_t, P, P],
+            "spin_select_blocks_noalloc": [C, P, P, P, P, P, P, i32, P, u64, i32, P, P, P, P, P, P],
             "spin_indexer_score": [C, P, P, P, P, i64, P, i64, P, P, P, i32, P, P, P],
             "spin_topk": [C, P, P, P, P, i32, P, P, P],
             "spin_update_ema": [C, P, P, P, P, P, P, P, P, P, P, P],
@@ -150,6 +151,16 @@ def select_blocks(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, ste
         _ptr(union_blocks), _ptr(n_union), _ptr(workspace),
         0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
         _stream(stream)))
+
+
+def select_blocks_noalloc(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer,
+                          blocks, n_blocks, union_blocks, n_union, status, stream=None):
+    """spin_select_blocks without a workspace: for callers that cannot allocate device
+    memory, the library's own static scratch array is used instead."""
+    _check(lib().spin_select_blocks_noalloc(
+        ctypes.byref(cfg), _ptr(V), _ptr(D), _ptr(Vmax), _ptr(warm), _ptr(n_slots), _ptr(q_pos),
+        rows, _ptr(rho_override), int(step), int(layer), _ptr(blocks), _ptr(n_blocks),
+        _ptr(union_blocks), _ptr(n_union), _ptr(status), _stream(stream)))
 
 
 def indexer_score(cfg, q, w, k_pool, k_scale, n_pages, block_table, list_, n_list, n_slots, rows,
