@@ -114,6 +114,45 @@ def test_rho_override_device_table():
     run_steps(h, 4, rho=rho)
 
 
+# --------------------------------------------------------------- tensor-core kernel
+
+def _tc_workload(k_dtype, rows, n_req=3, n0=2000, seed=21):
+    return syn.Workload("tc", n_req=n_req, n_layers=1, n0=n0, n_heads=64, head_dim=128,
+                        kv_heads=1, q_dtype="bf16", k_dtype=k_dtype, top_k=256, rho_bp=4000,
+                        gamma_bp=500, alpha=0.9, steps=4, rows=rows, heavy=8, rope_dims=64,
+                        shuffle=True, mean_accept=2.0 if rows > 1 else 0.0, seed=seed)
+
+
+@pytest.mark.parametrize("k_dtype,rows", [("bf16", 1), ("e4m3", 1), ("bf16", 4), ("e4m3", 2),
+                                          ("bf16", 3)])
+def test_tcgen05_small_ragged(k_dtype, rows):
+    """Shared key, 64 heads x 128 dims: requests of 2000, 130 and 64 slots (odd block lists
+    leave half-empty 128-slot tiles), through the tcgen05 kernel."""
+    h = Harness(_tc_workload(k_dtype, rows), score_path="tcgen05")
+    h.inp.n_slots.copy_(torch.tensor([2000, 130, 64], dtype=torch.int32))
+    run_steps(h, 4)
+
+
+@pytest.mark.parametrize("k_dtype", ["bf16", "e4m3"])
+def test_tcgen05_matches_generic_kernel(k_dtype):
+    """Independent GPU cross-check: the tensor-core and the generic CUDA-core kernel on
+    the same selection."""
+    wl = _tc_workload(k_dtype, 1, n_req=4, n0=5000, seed=3)
+    h = Harness(wl, score_path="tcgen05")
+    q, w, qp = h.inp.step_inputs()
+    h.step(0, 0, q, w, qp)
+    cfg_g = spin.make_config(**wl.config_fields(), score_path="generic")
+    out = torch.zeros_like(h.buf.scores)
+    spin.indexer_score(cfg_g, q, w, h.inp.k_pool[0], h.inp.k_scale[0], h.inp.n_pages,
+                       h.inp.block_table, h.buf.blocks, h.buf.n_blocks, h.inp.n_slots, 1, out,
+                       h.buf.status)
+    torch.cuda.synchronize()
+    nb = h.buf.n_blocks[:, 0].tolist()
+    for r in range(wl.n_req):
+        a, b = out[r, 0, : nb[r] * 64], h.buf.scores[r, 0, : nb[r] * 64]
+        assert torch.allclose(a, b, rtol=1e-4, atol=1e-3), (r, (a - b).abs().max())
+
+
 # ------------------------------------------------------------------------------- MTP
 
 def test_mtp_small_union_and_replay():
