@@ -224,8 +224,9 @@ class Workload:
                 spin.commit_mtp(cfg, st.V, st.D, st.Vmax, st.warm, buf.scores, rows, lst, nl, ns, qp,
                                 self.accepted[s], buf.status)
 
-    def scored_slots(self, steps):
-        """Slots scored per (step, layer) launch, times rows, from the recorded lists."""
+    def scored_slots(self, steps, unique=False):
+        """Slots scored per (step, layer) launch, from the recorded lists: times the query
+        rows (the metric's count), or each slot once (unique=True, the key bytes read)."""
         out = []
         ns_all = self.n_slots.cpu().numpy()
         lists = (self.blocks[:, :, :, 0] if self.rows == 1 else self.unions).cpu().numpy()
@@ -236,7 +237,7 @@ class Workload:
                 for r in range(self.wl.n_req):
                     blks = lists[s, layer, r, : counts[s, layer, r]].astype(np.int64)
                     tot += int(np.minimum(64, ns_all[s, r] - 64 * blks).clip(min=0).sum())
-                out.append(tot * self.rows)
+                out.append(tot if unique else tot * self.rows)
         return out
 
     def key_bytes_per_slot(self):
@@ -427,7 +428,9 @@ def main():
     # dominant kernel: the indexer score
     avg_score_ms = float(np.mean(score_ms))
     kbytes = wk.key_bytes_per_slot()
-    alg_bytes = float(np.mean(slots_per_launch)) * (kbytes + 4)   # keys (+scale) + score write
+    unique_per_launch = wk.scored_slots(range(W, W + K), unique=True)
+    # keys (+ FP8 scale) of every scored slot once, plus one fp32 score per slot and row
+    alg_bytes = float(np.mean(unique_per_launch)) * (kbytes + 4 * wk.rows)
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (avg_score_ms / 1000.0) / 1e9
     kernel_file = "spin_score_stream.cu" if wl.kv_heads > 1 else "spin_score_tc.cu"

@@ -147,8 +147,79 @@ __global__ void __launch_bounds__(kEmaThreads) ema_replay_kernel(spin_config cfg
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// One-row update (a = 0): each listed slot i is updated once and its offset q - i is
+// distinct, so the work splits by list entry with no ordering between threads.  A warp
+// owns two list entries (128 slots), issues all their loads together, and refreshes the
+// two blocks' Vmax with a warp max.
+// ---------------------------------------------------------------------------------------
+constexpr int kEmaListEntries = 16;  // per CTA of 8 warps
+
+__global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs a) {
+    const Dims dm = dims_of(cfg);
+    const int req = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int64_t n = a.n_slots[req], q = a.q_pos[req], cnt = a.n_list[req];
+    uint32_t bad = request_check(n, q, 1, dm);
+    if (cnt < 0 || cnt > dm.MB) bad |= SPIN_STATUS_BAD_LIST;
+    if (bad) {
+        if (blockIdx.x == 0 && tid == 0) set_status(a.status, bad);
+        return;
+    }
+    if (blockIdx.x == 0 && tid == 0) a.warm[req] = 1;
+    const int64_t nb = (n + kBlock - 1) / kBlock;
+    const float alpha = cfg.alpha;
+    const float oma = 1.0f - cfg.alpha;
+    float* Vq = a.V + (int64_t)req * dm.max_slots;
+    float* Dq = a.D + (int64_t)req * dm.DL;
+    const int32_t* lst = a.list + (int64_t)req * dm.MB;
+    const float* zq = a.scores + (int64_t)req * dm.MB * kBlock;
+    const int64_t k0 = (int64_t)blockIdx.x * kEmaListEntries + 2 * wid;
+    int64_t blk[2];
+    bool ok[2];
+    float z[2][2], v[2][2], d[2][2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int64_t k = k0 + e;
+        blk[e] = k < cnt ? lst[k] : -1;
+        ok[e] = blk[e] >= 0 && blk[e] < nb;
+        if (k < cnt && !ok[e] && lane == 0) set_status(a.status, SPIN_STATUS_BAD_LIST);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int64_t i = blk[e] * kBlock + lane + 32 * hh;
+            const bool live = ok[e] && i < n;
+            z[e][hh] = live ? zq[k * kBlock + lane + 32 * hh] : 0.0f;
+            v[e][hh] = (ok[e] && i < dm.max_slots) ? Vq[i] : 0.0f;
+            d[e][hh] = live ? Dq[q - i] : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        if (!ok[e]) continue;  // warp-uniform
+        float m = -FLT_MAX;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int64_t i = blk[e] * kBlock + lane + 32 * hh;
+            if (i < n) {
+                const float t = __fmul_rn(oma, z[e][hh]);
+                v[e][hh] = __fmaf_rn(alpha, v[e][hh], t);
+                Vq[i] = v[e][hh];
+                Dq[q - i] = __fmaf_rn(alpha, d[e][hh], t);
+            }
+            if (i < dm.max_slots) m = fmaxf(m, v[e][hh]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) a.Vmax[(int64_t)req * dm.MB + blk[e]] = m;
+    }
+}
+
 cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
+    if (a.accepted == nullptr && a.rows == 1) {
+        dim3 grid((dm.MB + kEmaListEntries - 1) / kEmaListEntries, dm.R);
+        ema_list_kernel<<<grid, 256, 0, s>>>(cfg, a);
+        return cudaGetLastError();
+    }
     const int gx = (dm.max_slots + kEmaSpan - 1) / kEmaSpan;
     dim3 grid(gx > 0 ? gx : 1, dm.R);
     const size_t smem = sizeof(float) * (size_t)a.rows * (kEmaSpan + a.rows);

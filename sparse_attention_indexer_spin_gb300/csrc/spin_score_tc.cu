@@ -9,19 +9,28 @@
 // of a 128-slot tile (two selected pages) with the 64*rows query vectors, so it runs on
 // the tensor cores: M = 128 slots, N = 64*rows, K = d = 128, fp32 accumulation in TMEM.
 //
+// bf16 keys: kind::f16 (bf16 x bf16, exact products).  The keys and q reach shared memory
+//   by 2D TMA in the 128-byte-swizzled K-major layout the MMA reads.
+// FP8 (e4m3) keys: kind::f8f6f4 straight from the TMA-loaded pages, no conversion.  q is
+//   carried as two e4m3 terms: for every (row, head) a power-of-two scale g puts
+//   max|q|/g in (224, 448]; hi = e4m3(q/g), lo = e4m3(q/g - hi), and the MMA runs over
+//   K = 2 x 128 with the keys repeated against [hi | lo], so the accumulator holds
+//   k . (hi + lo) with |q/g - hi - lo| <= 2^-8 |q/g| per element (plus the e4m3
+//   subnormal floor); the epilogue multiplies by g.  The per-slot dequantisation scale is
+//   applied before the ReLU.
+//
 // Warp roles of a persistent CTA (tiles = pairs of selected blocks of one request):
-//   warp 0      producer: bf16 keys -> two 2D TMA loads per page straight into the
-//               128-byte-swizzled K-major operand layout; FP8 keys -> one bulk copy per
-//               page into a raw staging ring
-//   warp 1      TMEM owner and MMA issuer (one thread): 8 tcgen05.mma of K = 16 per
-//               tile, commits to the operand-release and accumulator-full barriers;
-//               stages q (and converts it to f16 for FP8 keys) when the request changes
-//   warps 2-5   epilogue: tcgen05.ld of the tile's accumulators (one slot per thread),
-//               z = s_i * sum_h w_h max(acc_h, 0) per row, masked to i < N, stored
-//   warps 6-9   (FP8 keys only) converters: e4m3 -> f16 (exact) from the raw ring into
-//               the swizzled operand layout
-// Accumulators are double-buffered in TMEM so the epilogue of tile t overlaps the MMAs
-// of tile t+1; every barrier wait is bounded and a timeout unwinds all roles.
+//   warp 0      producer: one (FP8) or two (bf16) 2D TMA loads per page into a ring
+//   warp 1      TMEM owner and MMA issuer (one thread): 8 tcgen05.mma per tile into
+//               double-buffered accumulators; stages q when the request changes
+//   warps 2-9   epilogue, two warps per TMEM lane quarter taking alternate tiles:
+//               tcgen05.ld of a tile's accumulators (one slot per thread),
+//               z = sum_h w_h g_h max(s_i acc_h, 0) per row, masked to i < N, stored
+// Accumulators are 2-4 deep in TMEM (N <= 128: 4), the per-slot FP8 scales travel with
+// the pages by bulk copy into a ring of their own.
+// Every warp resolves its tiles' pages 32 at a time (one tile per lane), so the dependent
+// list and block-table loads are paid once per 32 tiles.  Every barrier wait is bounded
+// and a timeout unwinds all roles.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -38,12 +47,11 @@ constexpr int kTcNH = 64;      // heads
 constexpr int kTcM = 128;      // slots per tile (two pages)
 constexpr int kTcMaxRows = 4;  // N = 64 * rows <= 256
 constexpr int kTcMaxReq = 2048;
-constexpr int kTcRegionBytes = kTcM * 128;          // one 64-element K half of a 128-slot tile
-constexpr int kTcABytes = 2 * kTcRegionBytes;       // 32 KB operand tile (16-bit elements)
-constexpr int kTcRawBytes = 2 * kBlock * kTcD;      // 16 KB: two FP8 pages
-constexpr int kTcStagesBf16 = 3;
-constexpr int kTcRawStages = 4;
-constexpr int kTcAStagesFp8 = 2;
+constexpr int kTcEpiWarps = 8;                      // two per TMEM lane quarter
+constexpr int kTcThreads = (2 + kTcEpiWarps) * 32;  // producer, MMA, epilogue
+constexpr int kTcMaxAcc = 4;                        // accumulator buffers in TMEM
+constexpr int kTcStagesMax = 8;  // operand ring depth (tiles in flight per CTA): 128 KB either way
+__host__ __device__ constexpr int tc_stages(bool fp8) { return fp8 ? 8 : 4; }
 
 // ------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -58,17 +66,26 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, A and B both f16 (fmt 0) or both
-// bf16 (fmt 1), both K-major, N >> 3 and M >> 4.
-__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt, uint32_t n, uint32_t m) {
+// Instruction descriptor (kind::f16 and kind::f8f6f4): fp32 accumulator, A and B of the same
+// format (kind::f16: 0 = f16, 1 = bf16; kind::f8f6f4: 0 = e4m3), both K-major, N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t idesc_mma(uint32_t ab_fmt, uint32_t n, uint32_t m) {
     return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -78,19 +95,27 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
-    uint32_t r[32];
+// 64 consecutive fp32 columns of this thread's TMEM lane, waited for in the same statement.
+__device__ __forceinline__ void tc_ld64(uint32_t taddr, float* v) {
+    uint32_t r[64];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, "
+        "%36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, "
+        "%57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -101,50 +126,75 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-// Byte offset of element c (0..127) of operand row m inside a [rows][128 x 16-bit] K-major
-// tile stored as two 128-byte-swizzled regions of region_bytes each.
-__device__ __forceinline__ uint32_t sw128_offset(int m, int c, int region_bytes) {
-    const int kh = c >> 6, ch = (c & 63) >> 3;
-    return (uint32_t)(kh * region_bytes + (m >> 3) * 1024 + (m & 7) * 128 + ((ch ^ (m & 7)) << 4) + (c & 7) * 2);
+
+// Scale g of one q row (128 values): the power of two with max|q|/g in (224, 448].
+__device__ __forceinline__ float q_row_scale(const __nv_bfloat16* qrow) {
+    float amax = 0.0f;
+    const uint4* p = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll
+    for (int c = 0; c < kTcD / 8; ++c) {
+        const uint4 u = p[c];
+        const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(wds[e] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(wds[e] & 0xffff0000u)));
+        }
+    }
+    if (!(amax > 0.0f)) return 1.0f;
+    const float t = fmaxf(amax * (1.0f / 448.0f), 1e-30f);
+    const uint32_t bits = __float_as_uint(t);
+    float g = (bits & 0x7fffffu) ? __uint_as_float((bits & 0x7f800000u) + 0x00800000u) : t;
+    if (amax > 448.0f * g) g *= 2.0f;
+    return g;
 }
 
+struct TileInfo {
+    int req, k0, blk0, blk1, page0, page1, n;
+};
+
 struct TcHdr {
-    uint64_t full[kTcRawStages];     // producer -> consumer of a loaded stage
-    uint64_t empty[kTcRawStages];    // stage released back to the producer
-    uint64_t afull[kTcAStagesFp8];   // FP8: converted operand ready
-    uint64_t aempty[kTcAStagesFp8];  // FP8: converted operand consumed by the MMAs
-    uint64_t tfull[2];               // accumulator ready
-    uint64_t tempty[2];              // accumulator drained by the epilogue
-    uint64_t qdone;                  // every issued MMA finished (before q is restaged)
+    uint64_t full[kTcStagesMax];   // tile landed in shared memory
+    uint64_t empty[kTcStagesMax];  // tile consumed by the MMAs
+    uint64_t sfull[kTcStagesMax + kTcMaxAcc];  // FP8: the tile's slot scales landed
+    uint64_t tfull[kTcMaxAcc];  // accumulator ready
+    uint64_t tempty[kTcMaxAcc]; // accumulator drained by the epilogue
+    uint64_t qfull;             // q staged by TMA (bf16 keys)
+    uint64_t qdone;             // every issued MMA finished (before q is restaged)
     uint32_t tmem_base;
     int abort_flag;
     int total_tiles;
 };
 
 struct TcLayout {
-    uint32_t prefix, stage_a, raw, qbuf, wbuf, total;
+    uint32_t prefix, stage_a, scales, qbuf, wbuf, tile_bytes, total;
 };
+
+// accumulator buffers that fit in TMEM's 512 columns
+__host__ __device__ constexpr int tc_nacc(int n) { return n <= 128 ? 4 : 2; }
 
 __host__ __device__ inline TcLayout tc_layout(int R, int rows, bool fp8) {
     TcLayout L;
-    uint32_t off = 1024;  // header
+    L.tile_bytes = fp8 ? kTcM * kTcD : kTcM * kTcD * 2;  // 16 KB or 32 KB
+    uint32_t off = 1024;                                 // header
     L.prefix = off;
     off += ((uint32_t)(R + 1) * 4 + 1023) & ~1023u;
     L.stage_a = off;
-    off += (fp8 ? kTcAStagesFp8 : kTcStagesBf16) * kTcABytes;
-    L.raw = off;
-    if (fp8) off += kTcRawStages * kTcRawBytes;
+    off += tc_stages(fp8) * L.tile_bytes;
+    L.scales = off;                                      // [stages + acc][128] fp32 (FP8 only)
+    off += fp8 ? (kTcStagesMax + kTcMaxAcc) * kTcM * 4 : 0;
     L.qbuf = off;
-    off += (uint32_t)(64 * rows) * 256;  // two 128-byte regions of N rows
+    off += (uint32_t)(64 * rows) * 256;                  // two regions of N rows x 128 B
     L.wbuf = off;
-    off += 4u * 64 * rows * 4;           // a copy of w per epilogue warp
-    L.total = off + 1024;                // slack for 1024-byte alignment of the base
+    off += (uint32_t)kTcEpiWarps * 64 * rows * 4;        // w (times g) per epilogue warp
+    L.total = off + 1024;                                // slack for 1024-byte alignment
     return L;
 }
 
 template <bool FP8>
-__global__ void __launch_bounds__(FP8 ? 320 : 192, 1)
-score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMap kmap) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap qmap) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Dims dm = dims_of(cfg);
@@ -154,13 +204,15 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     TcHdr* hdr = reinterpret_cast<TcHdr*>(smem);
     int* prefix = reinterpret_cast<int*>(smem + L.prefix);
     unsigned char* sA = smem + L.stage_a;
-    unsigned char* sRaw = smem + L.raw;
     unsigned char* sQ = smem + L.qbuf;
     float* sW = reinterpret_cast<float*>(smem + L.wbuf);
+    float* sScale = reinterpret_cast<float*>(smem + L.scales);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    constexpr int NSA = FP8 ? kTcAStagesFp8 : kTcStagesBf16;  // operand stages
-    constexpr int NSL = FP8 ? kTcRawStages : kTcStagesBf16;   // load stages
-    const uint32_t tmem_cols = N <= 64 ? 128u : (N <= 128 ? 256u : 512u);
+    const int NACC = tc_nacc(N);
+    const uint32_t tmem_cols = (uint32_t)(NACC * N) <= 256u ? 256u : 512u;
+    const uint32_t qregion = (uint32_t)N * 128;  // bytes of one B region
+    constexpr int kTcStages = tc_stages(FP8);
+    const int NSR = kTcStages + NACC;  // scale ring: the producer leads the epilogue by < NSR tiles
 
     // ------------------------------------------------------------------ set-up
     if (wid == 0) {
@@ -183,18 +235,16 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             prefix[dm.R] = carry;
             hdr->total_tiles = carry;
             hdr->abort_flag = 0;
-            for (int s = 0; s < NSL; ++s) {
+            for (int s = 0; s < kTcStages; ++s) {
                 mbar_init(&hdr->full[s], 1);
-                mbar_init(&hdr->empty[s], FP8 ? 128 : 1);
+                mbar_init(&hdr->empty[s], 1);
             }
-            for (int s = 0; s < kTcAStagesFp8; ++s) {
-                mbar_init(&hdr->afull[s], 128);
-                mbar_init(&hdr->aempty[s], 1);
-            }
-            for (int s = 0; s < 2; ++s) {
+            for (int s = 0; s < kTcStagesMax + kTcMaxAcc; ++s) mbar_init(&hdr->sfull[s], 1);
+            for (int s = 0; s < kTcMaxAcc; ++s) {
                 mbar_init(&hdr->tfull[s], 1);
                 mbar_init(&hdr->tempty[s], 128);
             }
+            mbar_init(&hdr->qfull, 1);
             mbar_init(&hdr->qdone, 1);
             fence_barrier_init();
         }
@@ -213,31 +263,55 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     const int t0 = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
     const int t1 = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
 
-    // tile -> request, first list entry, and the two pages (or -1)
-    auto decode = [&](int t, int& req, int& k0, int64_t* page, int64_t* blk) {
+    // tile -> request, first list entry, its two blocks and their pages (-1: none / invalid)
+    auto decode = [&](int t, TileInfo& ti) {
         int lo = 0, hi = dm.R - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
         }
-        req = lo;
-        k0 = 2 * (t - prefix[req]);
-        const int64_t n = a.n_slots[req], cnt = a.n_list[req];
+        ti.req = lo;
+        ti.k0 = 2 * (t - prefix[lo]);
+        const int64_t n = a.n_slots[lo], cnt = a.n_list[lo];
         const int64_t nb = (n + kBlock - 1) / kBlock;
+        int bl[2], pg[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            page[h] = -1;
-            blk[h] = -1;
-            const int64_t k = k0 + h;
+            bl[h] = -1;
+            pg[h] = -1;
+            const int64_t k = ti.k0 + h;
             if (k < cnt) {
-                const int64_t b = a.list[(int64_t)req * dm.MB + k];
-                blk[h] = b;
+                const int64_t b = a.list[(int64_t)lo * dm.MB + k];
+                bl[h] = (int)b;
                 if (b >= 0 && b < nb) {
-                    const int64_t p = a.block_table[(int64_t)req * a.bt_stride + b];
-                    if (p >= 0 && p < a.n_pages) page[h] = p;
+                    const int64_t p = a.block_table[(int64_t)lo * a.bt_stride + b];
+                    if (p >= 0 && p < a.n_pages) pg[h] = (int)p;
+                } else {
+                    bl[h] = -2;  // a listed block outside the context
                 }
             }
         }
+        ti.blk0 = bl[0]; ti.blk1 = bl[1]; ti.page0 = pg[0]; ti.page1 = pg[1];
+        ti.n = (int)n;
+    };
+    // warp-cooperative: lane j resolves tile base + j; tile() broadcasts one tile's info
+    TileInfo mine;
+    int batch_base = -1;
+    auto tile = [&](int t) -> TileInfo {
+        if (batch_base < 0 || t >= batch_base + 32) {
+            batch_base = t;
+            if (t + lane < t1) decode(t + lane, mine);
+        }
+        const int j = t - batch_base;
+        TileInfo r;
+        r.req = __shfl_sync(0xffffffffu, mine.req, j);
+        r.k0 = __shfl_sync(0xffffffffu, mine.k0, j);
+        r.blk0 = __shfl_sync(0xffffffffu, mine.blk0, j);
+        r.blk1 = __shfl_sync(0xffffffffu, mine.blk1, j);
+        r.page0 = __shfl_sync(0xffffffffu, mine.page0, j);
+        r.page1 = __shfl_sync(0xffffffffu, mine.page1, j);
+        r.n = __shfl_sync(0xffffffffu, mine.n, j);
+        return r;
     };
     auto fail_wait = [&]() {
         hdr->abort_flag = 1;
@@ -246,54 +320,78 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
 
     if (wid == 0) {
         // -------------------------------------------------------------- producer
-        if (lane == 0) {
-            int last_phase[NSL];
-            for (int s = 0; s < NSL; ++s) last_phase[s] = -1;
-            for (int t = t0, it = 0; t < t1; ++t, ++it) {
-                const int s = it % NSL;
-                const uint32_t ph = (uint32_t)(it / NSL) & 1u;
-                if (!mbar_wait(&hdr->empty[s], ph ^ 1u, &hdr->abort_flag)) { fail_wait(); break; }
-                int req, k0;
-                int64_t page[2], blk[2];
-                decode(t, req, k0, page, blk);
+        uint32_t issued = 0, phases = 0;  // per stage: ever filled, parity of its last fill
+        for (int t = t0, it = 0; t < t1; ++t, ++it) {
+            const TileInfo ti = tile(t);
+            const int s = it % kTcStages;
+            const uint32_t ph = (uint32_t)(it / kTcStages) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&hdr->empty[s], ph ^ 1u, &hdr->abort_flag);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                if (lane == 0) fail_wait();
+                break;
+            }
+            if (lane == 0) {
+                const int page[2] = {ti.page0, ti.page1};  // indexed by unrolled constants only
+                const uint32_t page_bytes = FP8 ? (uint32_t)(kBlock * kTcD) : (uint32_t)(kBlock * kTcD * 2);
                 uint32_t bytes = 0;
+#pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    if (page[h] >= 0) bytes += FP8 ? (uint32_t)(kBlock * kTcD) : (uint32_t)(2 * 8192);
+                    if (page[h] >= 0) bytes += page_bytes;
+                if (FP8) {
+                    // the tile's 2 x 64 slot scales, into the scale ring (epilogue side)
+                    const int sr = it % NSR;
+                    uint32_t sb = 0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (page[h] >= 0) sb += kBlock * 4;
+                    if (sb == 0) {
+                        mbar_arrive(&hdr->sfull[sr]);
+                    } else {
+                        mbar_arrive_expect_tx(&hdr->sfull[sr], sb);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (page[h] >= 0)
+                                bulk_g2s(sScale + sr * kTcM + h * kBlock, a.k_scale + (int64_t)page[h] * kBlock,
+                                         kBlock * 4, &hdr->sfull[sr]);
+                    }
+                }
                 if (bytes == 0) {
                     mbar_arrive(&hdr->full[s]);
                 } else {
                     mbar_arrive_expect_tx(&hdr->full[s], bytes);
+                    unsigned char* stage = sA + (size_t)s * L.tile_bytes;
+#pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         if (page[h] < 0) continue;
+                        const int y = page[h] * kBlock;
                         if (FP8) {
-                            const unsigned char* src =
-                                reinterpret_cast<const unsigned char*>(a.k_pool) + (size_t)page[h] * kBlock * kTcD;
-                            bulk_g2s(sRaw + (size_t)s * kTcRawBytes + h * kBlock * kTcD, src, kBlock * kTcD,
-                                     &hdr->full[s]);
+                            // one 64-row x 128-byte box: the page's keys, 128B-swizzled
+                            tma_load_2d(stage + h * 8192, &kmap, 0, y, &hdr->full[s]);
                         } else {
-                            unsigned char* dst = sA + (size_t)s * kTcABytes + h * 8192;
-                            const int y = (int)(page[h] * kBlock);
-                            tma_load_2d(dst, &kmap, 0, y, &hdr->full[s]);
-                            tma_load_2d(dst + kTcRegionBytes, &kmap, 64, y, &hdr->full[s]);
+                            // two 64-row x 64-element boxes: the two K halves of the page
+                            tma_load_2d(stage + h * 8192, &kmap, 0, y, &hdr->full[s]);
+                            tma_load_2d(stage + kTcM * 128 + h * 8192, &kmap, 64, y, &hdr->full[s]);
                         }
                     }
                 }
-                last_phase[s] = (int)ph;
             }
-            for (int s = 0; s < NSL; ++s)
-                if (last_phase[s] >= 0 && !mbar_wait(&hdr->full[s], (uint32_t)last_phase[s], nullptr))
-                    set_status(a.status, SPIN_STATUS_TIMEOUT);
+            issued |= 1u << s;
+            phases = (phases & ~(1u << s)) | (ph << s);
+            __syncwarp();
         }
+        if (lane == 0)
+            for (int s = 0; s < kTcStages; ++s)
+                if (((issued >> s) & 1u) && !mbar_wait(&hdr->full[s], (phases >> s) & 1u, nullptr))
+                    set_status(a.status, SPIN_STATUS_TIMEOUT);
     } else if (wid == 1) {
         // ------------------------------------------------------------ MMA issuer
-        const uint32_t idesc = idesc_f16(FP8 ? 0u : 1u, (uint32_t)N, (uint32_t)kTcM);
+        const uint32_t idesc = idesc_mma(FP8 ? 0u : 1u, (uint32_t)N, (uint32_t)kTcM);
         int cur_req = -1;
-        uint32_t qphase = 0;
+        uint32_t qphase = 0, qload_phase = 0;
         bool issued_any = false;
         for (int t = t0, it = 0; t < t1; ++t, ++it) {
-            int req, k0;
-            int64_t page[2], blk[2];
-            decode(t, req, k0, page, blk);
+            const int req = tile(t).req;
             if (req != cur_req) {
                 if (issued_any) {  // the MMAs of the previous request still read sQ
                     if (lane == 0) tc_commit(&hdr->qdone);
@@ -301,61 +399,89 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                     if (!mbar_wait(&hdr->qdone, qphase, &hdr->abort_flag)) { fail_wait(); break; }
                     qphase ^= 1u;
                 }
-                // stage q[req] (rows x 64 heads x 128 dims) as the K-major B operand
-                const int nchunks = N * (kTcD / 8);
-                for (int ci = lane; ci < nchunks; ci += 32) {
-                    const int nrow = ci / (kTcD / 8), c0 = (ci % (kTcD / 8)) * 8;
-                    const int r = nrow / kTcNH, h = nrow % kTcNH;
-                    const int64_t qoff = (((int64_t)req * rows + r) * kTcNH + h) * kTcD + c0;
-                    uint32_t wv[4];
+                if (FP8) {
+                    // B = [hi | lo]: lane handles q rows n = lane, lane + 32, ...
+                    for (int n = lane; n < N; n += 32) {
+                        const int r = n / kTcNH, h = n % kTcNH;
+                        const __nv_bfloat16* qrow =
+                            reinterpret_cast<const __nv_bfloat16*>(a.q) + (((int64_t)req * rows + r) * kTcNH + h) * kTcD;
+                        const float inv_g = 1.0f / q_row_scale(qrow);   // exact: a power of two
+                        const uint4* src = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll 2
+                        for (int ch = 0; ch < kTcD / 16; ++ch) {         // 16 elements -> 16 B of e4m3
+                            const uint4 u0 = src[2 * ch], u1 = src[2 * ch + 1];
+                            const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                            uint32_t hw[4], lw[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float f0, f1;
-                        if (cfg.q_dtype == SPIN_DTYPE_BF16) {
-                            const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q) + qoff;
-                            f0 = __bfloat162float(qb[2 * e]);
-                            f1 = __bfloat162float(qb[2 * e + 1]);
-                        } else {
-                            const float* qf = reinterpret_cast<const float*>(a.q) + qoff;
-                            f0 = qf[2 * e];
-                            f1 = qf[2 * e + 1];
-                        }
-                        if (FP8) {
-                            __half2 hv = __floats2half2_rn(f0, f1);
-                            wv[e] = *reinterpret_cast<uint32_t*>(&hv);
-                        } else {
-                            __nv_bfloat162 bv = __floats2bfloat162_rn(f0, f1);
-                            wv[e] = *reinterpret_cast<uint32_t*>(&bv);
+                            for (int e = 0; e < 4; ++e) {
+                                uint32_t hv = 0, lv = 0;
+#pragma unroll
+                                for (int pr = 0; pr < 2; ++pr) {
+                                    const uint32_t wd = wds[2 * e + pr];
+                                    const float2 x = make_float2(__uint_as_float(wd << 16) * inv_g,
+                                                                 __uint_as_float(wd & 0xffff0000u) * inv_g);
+                                    const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+                                    const __half2 hf = *reinterpret_cast<const __half2*>(
+                                        &static_cast<const __half2_raw&>(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+                                    const float2 hx = __half22float2(hf);
+                                    const float2 rx = make_float2(x.x - hx.x, x.y - hx.y);
+                                    const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(rx, __NV_SATFINITE, __NV_E4M3);
+                                    hv |= (uint32_t)h2 << (16 * pr);
+                                    lv |= (uint32_t)l2 << (16 * pr);
+                                }
+                                hw[e] = hv;
+                                lw[e] = lv;
+                            }
+                            const uint32_t off = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((ch ^ (n & 7)) << 4));
+                            *reinterpret_cast<uint4*>(sQ + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            *reinterpret_cast<uint4*>(sQ + qregion + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                         }
                     }
-                    *reinterpret_cast<uint4*>(sQ + sw128_offset(nrow, c0, N * 128)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    fence_async_smem();
+                    __syncwarp();
+                } else {
+                    // q rows of this request by TMA, straight into the swizzled B layout
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&hdr->qfull, (uint32_t)N * kTcD * 2);
+                        const int y = req * rows * kTcNH;
+                        tma_load_2d(sQ, &qmap, 0, y, &hdr->qfull);
+                        tma_load_2d(sQ + qregion, &qmap, 64, y, &hdr->qfull);
+                    }
+                    __syncwarp();
+                    if (!mbar_wait(&hdr->qfull, qload_phase, &hdr->abort_flag)) { fail_wait(); break; }
+                    qload_phase ^= 1u;
                 }
-                fence_async_smem();
-                __syncwarp();
                 cur_req = req;
             }
-            const int sa = it % NSA;
-            const uint32_t pha = (uint32_t)(it / NSA) & 1u;
-            bool ok = FP8 ? mbar_wait(&hdr->afull[sa], pha, &hdr->abort_flag)
-                          : mbar_wait(&hdr->full[sa], pha, &hdr->abort_flag);
-            const int acc = it & 1;
-            const uint32_t phc = (uint32_t)(it >> 1) & 1u;
+            const int sa = it % kTcStages;
+            const uint32_t pha = (uint32_t)(it / kTcStages) & 1u;
+            bool ok = mbar_wait(&hdr->full[sa], pha, &hdr->abort_flag);
+            const int acc = it % NACC;
+            const uint32_t phc = (uint32_t)(it / NACC) & 1u;
             if (ok) ok = mbar_wait(&hdr->tempty[acc], phc ^ 1u, &hdr->abort_flag);
             if (!ok) { fail_wait(); break; }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t a_base = smem_u32(sA + (size_t)sa * kTcABytes);
+                const uint32_t a_base = smem_u32(sA + (size_t)sa * L.tile_bytes);
                 const uint32_t b_base = smem_u32(sQ);
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * N);
+                if (FP8) {
+                    // K = 2 x 128: the keys against hi, then the same keys against lo
 #pragma unroll
-                for (int kh = 0; kh < 2; ++kh)
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t adesc = smem_desc_sw128(a_base + kh * kTcRegionBytes + kk * 32);
-                        const uint64_t bdesc = smem_desc_sw128(b_base + kh * (N * 128) + kk * 32);
-                        tc_mma(d_tmem, adesc, bdesc, idesc, (kh | kk) ? 1u : 0u);
-                    }
-                tc_commit(FP8 ? &hdr->aempty[sa] : &hdr->empty[sa]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_f8(d_tmem, smem_desc_sw128(a_base + kk * 32),
+                                      smem_desc_sw128(b_base + part * qregion + kk * 32), idesc, (part | kk) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma_f16(d_tmem, smem_desc_sw128(a_base + kh * (kTcM * 128) + kk * 32),
+                                       smem_desc_sw128(b_base + kh * qregion + kk * 32), idesc, (kh | kk) ? 1u : 0u);
+                }
+                tc_commit(&hdr->empty[sa]);
                 tc_commit(&hdr->tfull[acc]);
             }
             issued_any = true;
@@ -367,90 +493,71 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             __syncwarp();
             if (!mbar_wait(&hdr->qdone, qphase, nullptr)) set_status(a.status, SPIN_STATUS_TIMEOUT);
         }
-    } else if (wid < 6) {
+    } else {
         // ------------------------------------------------------------- epilogue
         const int quarter = wid & 3;
+        const int parity = (wid - 2) / 4;       // this warp takes the tiles it with it % 2 == parity
         const int m = quarter * 32 + lane;      // slot row of the tile = TMEM lane
         const int h = m >> 6, s = m & 63;
         float* wloc = sW + (size_t)(wid - 2) * N;
         int cur_req = -1;
-        for (int t = t0, it = 0; t < t1; ++t, ++it) {
-            int req, k0;
-            int64_t page[2], blk[2];
-            decode(t, req, k0, page, blk);
+        for (int t = t0 + parity, it = parity; t < t1; t += 2, it += 2) {
+            const TileInfo ti = tile(t);
+            const int req = ti.req;
             if (req != cur_req) {
                 __syncwarp();
-                for (int i = lane; i < N; i += 32) wloc[i] = a.w[(int64_t)req * rows * kTcNH + i];
+                for (int n = lane; n < N; n += 32) {
+                    float g = 1.0f;
+                    if (FP8) {
+                        const int r = n / kTcNH, hh = n % kTcNH;
+                        g = q_row_scale(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                        (((int64_t)req * rows + r) * kTcNH + hh) * kTcD);
+                    }
+                    wloc[n] = a.w[(int64_t)req * rows * kTcNH + n] * g;
+                }
                 __syncwarp();
                 cur_req = req;
             }
-            const int acc = it & 1;
-            const uint32_t phc = (uint32_t)(it >> 1) & 1u;
+            const int page = h ? ti.page1 : ti.page0;
+            const int blk = h ? ti.blk1 : ti.blk0;
+            const int64_t k = ti.k0 + h;
+            const bool listed = blk != -1;                                    // a real list entry
+            const bool live = page >= 0 && (int64_t)blk * kBlock + s < ti.n;  // a slot of the context
+            if (listed && page < 0 && s == 0)
+                set_status(a.status, blk == -2 ? SPIN_STATUS_BAD_LIST : SPIN_STATUS_BAD_PAGE);
+            const int acc = it % NACC;
+            const uint32_t phc = (uint32_t)(it / NACC) & 1u;
+            float scale = 1.0f;
+            if (FP8) {
+                const int sr = it % NSR;
+                if (!mbar_wait(&hdr->sfull[sr], (uint32_t)(it / NSR) & 1u, &hdr->abort_flag)) { fail_wait(); break; }
+                scale = sScale[sr * kTcM + m];
+            }
             if (!mbar_wait(&hdr->tfull[acc], phc, &hdr->abort_flag)) { fail_wait(); break; }
             tc_fence_after();
-            const int64_t k = k0 + h;
-            const int64_t n = a.n_slots[req];
-            const bool listed = k < a.n_list[req];                      // a real list entry
-            const bool live = page[h] >= 0 && blk[h] * kBlock + s < n;  // a slot of the context
-            const float scale = (FP8 && page[h] >= 0) ? a.k_scale[page[h] * kBlock + s] : 1.0f;
-            if (page[h] < 0 && blk[h] >= 0 && s == 0) {
-                const int64_t nb = (n + kBlock - 1) / kBlock;
-                set_status(a.status, (blk[h] < nb) ? SPIN_STATUS_BAD_PAGE : SPIN_STATUS_BAD_LIST);
-            }
             for (int r = 0; r < rows; ++r) {
-                float z = 0.0f;
+                float v[64];
+                tc_ld64(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N + r * kTcNH), v);
+                const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH);
+                float z4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {
-                    float v[32];
-                    const uint32_t taddr =
-                        tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N + r * kTcNH + cb * 32);
-                    tc_ld32(taddr, v);
-                    const float* wr = wloc + r * kTcNH + cb * 32;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) z = fmaf(wr[j], fmaxf(scale * v[j], 0.0f), z);
+                for (int j = 0; j < 16; ++j) {
+                    const float4 wv = wr[j];
+                    const float x0 = FP8 ? scale * v[4 * j + 0] : v[4 * j + 0];
+                    const float x1 = FP8 ? scale * v[4 * j + 1] : v[4 * j + 1];
+                    const float x2 = FP8 ? scale * v[4 * j + 2] : v[4 * j + 2];
+                    const float x3 = FP8 ? scale * v[4 * j + 3] : v[4 * j + 3];
+                    z4[0] = fmaf(wv.x, fmaxf(x0, 0.0f), z4[0]);
+                    z4[1] = fmaf(wv.y, fmaxf(x1, 0.0f), z4[1]);
+                    z4[2] = fmaf(wv.z, fmaxf(x2, 0.0f), z4[2]);
+                    z4[3] = fmaf(wv.w, fmaxf(x3, 0.0f), z4[3]);
                 }
+                float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
                 if (!live || z == 0.0f) z = 0.0f;
                 if (listed) a.scores[(((int64_t)req * rows + r) * dm.MB + k) * kBlock + s] = z;
             }
             tc_fence_before();
             mbar_arrive(&hdr->tempty[acc]);
-        }
-    } else {
-        // ------------------------------------------------------- FP8 converters
-        if (FP8) {
-            const int ct = tid - 192;  // 0..127
-            for (int t = t0, it = 0; t < t1; ++t, ++it) {
-                const int rs = it % kTcRawStages;
-                const uint32_t phr = (uint32_t)(it / kTcRawStages) & 1u;
-                const int sa = it % kTcAStagesFp8;
-                const uint32_t pha = (uint32_t)(it / kTcAStagesFp8) & 1u;
-                if (!mbar_wait(&hdr->full[rs], phr, &hdr->abort_flag)) { fail_wait(); break; }
-                if (!mbar_wait(&hdr->aempty[sa], pha ^ 1u, &hdr->abort_flag)) { fail_wait(); break; }
-                int req, k0;
-                int64_t page[2], blk[2];
-                decode(t, req, k0, page, blk);
-                const unsigned char* raw = sRaw + (size_t)rs * kTcRawBytes;
-                unsigned char* dstA = sA + (size_t)sa * kTcABytes;
-                for (int idx = ct; idx < kTcM * (kTcD / 8); idx += 128) {
-                    const int mm = idx >> 4, cc = idx & 15;
-                    if (page[mm >> 6] < 0) continue;
-                    const uint2 codes = *reinterpret_cast<const uint2*>(raw + mm * kTcD + cc * 8);
-                    uint32_t hv[4];
-                    const uint32_t cw[2] = {codes.x, codes.y};
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(cw[e] & 0xffffu), __NV_E4M3);
-                        __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(cw[e] >> 16), __NV_E4M3);
-                        hv[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                        hv[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-                    }
-                    *reinterpret_cast<uint4*>(dstA + sw128_offset(mm, cc * 8, kTcRegionBytes)) =
-                        make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                }
-                fence_async_smem();
-                mbar_arrive(&hdr->afull[sa]);
-                mbar_arrive(&hdr->empty[rs]);
-            }
         }
     }
 
@@ -483,6 +590,20 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// 2D tiled map over rows of 128 elements, 128-byte swizzle, box = {inner, box_rows}.
+static bool encode_rows(CUtensorMap* map, CUtensorMapDataType dt, int elt, const void* base, int64_t n_rows,
+                        uint32_t inner, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || n_rows < 1) return false;
+    const cuuint64_t gdim[2] = {(cuuint64_t)kTcD, (cuuint64_t)n_rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)kTcD * elt};
+    const cuuint32_t box[2] = {inner, box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void*>(base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool score_tc_supported(const spin_config& cfg, int rows) {
     return cfg.kv_heads == 1 && cfg.n_heads == kTcNH && cfg.head_dim == kTcD && rows >= 1 && rows <= kTcMaxRows &&
            cfg.n_req <= kTcMaxReq && cfg.q_dtype == SPIN_DTYPE_BF16 &&
@@ -491,23 +612,22 @@ bool score_tc_supported(const spin_config& cfg, int rows) {
 
 cudaError_t launch_score_tc(const spin_config& cfg, const ScoreArgs& a, cudaStream_t s) {
     if (!score_tc_supported(cfg, a.rows)) return cudaErrorNotSupported;
+    if (((uintptr_t)a.q & 15) != 0 || a.n_pages < 1) return cudaErrorInvalidValue;
     const Dims dm = dims_of(cfg);
     const bool fp8 = cfg.k_dtype == SPIN_DTYPE_E4M3;
     const TcLayout L = tc_layout(dm.R, a.rows, fp8);
-    CUtensorMap map;
-    memset(&map, 0, sizeof map);
-    if (!fp8) {
-        EncodeTiledFn enc = encode_fn();
-        if (!enc) return cudaErrorNotSupported;
-        const cuuint64_t gdim[2] = {(cuuint64_t)kTcD, (cuuint64_t)a.n_pages * kBlock};
-        const cuuint64_t gstride[1] = {(cuuint64_t)kTcD * 2};
-        const cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
-        const cuuint32_t estride[2] = {1, 1};
-        if (a.n_pages < 1) return cudaErrorInvalidValue;
-        CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.k_pool), gdim, gstride, box,
-                         estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    CUtensorMap kmap, qmap;
+    memset(&kmap, 0, sizeof kmap);
+    memset(&qmap, 0, sizeof qmap);
+    const int64_t pool_rows = a.n_pages * kBlock;
+    if (fp8) {
+        if (!encode_rows(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.k_pool, pool_rows, 128, kBlock))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!encode_rows(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.k_pool, pool_rows, 64, kBlock) ||
+            !encode_rows(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, (int64_t)dm.R * a.rows * kTcNH, 64,
+                         (uint32_t)(kTcNH * a.rows)))
+            return cudaErrorInvalidValue;
     }
     const int64_t max_tiles = (int64_t)dm.R * ((dm.MB + 1) / 2);
     int64_t grid = device_sm_count();
@@ -517,11 +637,11 @@ cudaError_t launch_score_tc(const spin_config& cfg, const ScoreArgs& a, cudaStre
     if (fp8) {
         e = cudaFuncSetAttribute(score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
         if (e != cudaSuccess) return e;
-        score_tc_kernel<true><<<(unsigned)grid, 320, L.total, s>>>(cfg, a, map);
+        score_tc_kernel<true><<<(unsigned)grid, kTcThreads, L.total, s>>>(cfg, a, kmap, qmap);
     } else {
         e = cudaFuncSetAttribute(score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
         if (e != cudaSuccess) return e;
-        score_tc_kernel<false><<<(unsigned)grid, 192, L.total, s>>>(cfg, a, map);
+        score_tc_kernel<false><<<(unsigned)grid, kTcThreads, L.total, s>>>(cfg, a, kmap, qmap);
     }
     return cudaGetLastError();
 }

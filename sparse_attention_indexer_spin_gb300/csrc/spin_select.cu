@@ -25,6 +25,8 @@ namespace spin {
 // block equals max(Vmax[j], max_i D[q-i]), so V is read only through its per-block max.
 // The additive reading needs V[i] + D[q-i] slot by slot.
 // ---------------------------------------------------------------------------------------
+constexpr int kBsBlocksPerWarp = 8;
+
 __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const float* __restrict__ V,
                                                           const float* __restrict__ D,
                                                           const float* __restrict__ Vmax,
@@ -44,24 +46,27 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
     const float* Vq = V + (int64_t)req * dm.max_slots;
     const float* Vm = Vmax + (int64_t)req * dm.MB;
     float* Sq = S + (int64_t)rr * dm.MB;
-    for (int64_t j = (int64_t)blockIdx.x * nw + wid; j < nb; j += (int64_t)gridDim.x * nw) {
-        const int64_t i0 = j * kBlock + lane, i1 = i0 + 32;
-        float best = -FLT_MAX;
-        bool any = false;
-        if (cfg.combine == SPIN_COMBINE_SUM) {
-            if (i0 < n) { best = __fadd_rn(Vq[i0], Dq[qr - i0]); any = true; }
-            if (i1 < n) { float v = __fadd_rn(Vq[i1], Dq[qr - i1]); best = any ? fmaxf(best, v) : v; any = true; }
-        } else {
-            if (i0 < n) { best = Dq[qr - i0]; any = true; }
-            if (i1 < n) { float v = Dq[qr - i1]; best = any ? fmaxf(best, v) : v; any = true; }
-        }
+    const bool sum = cfg.combine == SPIN_COMBINE_SUM;
+    // each warp owns kBsBlocksPerWarp consecutive blocks and issues all their loads first
+    for (int64_t j0 = ((int64_t)blockIdx.x * nw + wid) * kBsBlocksPerWarp; j0 < nb;
+         j0 += (int64_t)gridDim.x * nw * kBsBlocksPerWarp) {
+        float lo[kBsBlocksPerWarp], hi[kBsBlocksPerWarp];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            int oa = __shfl_xor_sync(0xffffffffu, (int)any, o);
-            if (oa) { best = any ? fmaxf(best, ob) : ob; any = true; }
+        for (int b = 0; b < kBsBlocksPerWarp; ++b) {
+            const int64_t i0 = (j0 + b) * kBlock + lane, i1 = i0 + 32;
+            lo[b] = i0 < n ? (sum ? __fadd_rn(Vq[i0], Dq[qr - i0]) : Dq[qr - i0]) : -FLT_MAX;
+            hi[b] = i1 < n ? (sum ? __fadd_rn(Vq[i1], Dq[qr - i1]) : Dq[qr - i1]) : -FLT_MAX;
         }
-        if (lane == 0) Sq[j] = (cfg.combine == SPIN_COMBINE_SUM) ? best : fmaxf(Vm[j], best);
+        const float vm = (!sum && lane < kBsBlocksPerWarp && j0 + lane < nb) ? Vm[j0 + lane] : -FLT_MAX;
+#pragma unroll
+        for (int b = 0; b < kBsBlocksPerWarp; ++b) {
+            // every block of the loop has at least one slot < N, so the max is a real value
+            float m = fmaxf(lo[b], hi[b]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const float vmb = __shfl_sync(0xffffffffu, vm, b);
+            if (lane == 0 && j0 + b < nb) Sq[j0 + b] = sum ? m : fmaxf(vmb, m);
+        }
     }
 }
 
@@ -261,8 +266,8 @@ size_t select_workspace_bytes(const spin_config& cfg, int rows) {
 
 cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
-    const int nw = 256 / 32;
-    int gx = (dm.MB + nw - 1) / nw;
+    const int per_cta = (256 / 32) * kBsBlocksPerWarp;
+    int gx = (dm.MB + per_cta - 1) / per_cta;
     if (gx > 512) gx = 512;
     dim3 g1(gx, dm.R * a.rows);
     block_score_kernel<<<g1, 256, 0, s>>>(cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,

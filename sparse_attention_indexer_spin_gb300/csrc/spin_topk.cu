@@ -186,6 +186,13 @@ topk_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __
 // ---------------------------------------------------------------------------------------
 constexpr int kTkCluster = 8;
 
+// keys of a slice, then (at this offset, in 4-byte words) the slice's list entries
+__host__ __device__ inline int64_t kTkListOffset(const spin_config& cfg) {
+    const Dims dm = dims_of(cfg);
+    const int64_t per = ((int64_t)dm.MB * kBlock + kTkCluster - 1) / kTkCluster;
+    return (per + 3) & ~(int64_t)3;
+}
+
 struct TkClusterShared {
     int hist[2][kTopkBins];   // double-buffered local histogram (peers read it)
     int merged[kTopkBins];
@@ -225,21 +232,36 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
     const int nloc = (int)(c1 - c0);
     const int nloc_pad = (nloc + 31) & ~31;
 
-    // 1. keys of this slice (0 = not a live candidate; live keys are never 0)
+    // 1. keys of this slice (0 = not a live candidate; live keys are never 0).  The slice
+    // [c0, c1) is a multiple of 8 candidates long and starts 32-byte aligned: its list
+    // entries are staged first, then the scores are read as float4 with every load of a
+    // thread in flight together.
+    int* slist = reinterpret_cast<int*>(keys + kTkListOffset(cfg));
+    const int64_t e0 = c0 >> 6;
+    const int ne = (int)(nloc > 0 ? ((c1 - 1) >> 6) - e0 + 1 : 0);
+    for (int i = tid; i < ne; i += kTopkThreads) slist[i] = lst[e0 + i];
+    __syncthreads();
     int v = 0;
     bool bad_list = false;
-    for (int i = tid; i < nloc; i += kTopkThreads) {
-        const int64_t c = c0 + i;
-        const int64_t blk = lst[c >> 6];
-        const int64_t slot = blk * kBlock + (c & 63);
-        uint32_t key = 0;
+    const float4* sc4 = reinterpret_cast<const float4*>(sc + c0);
+    uint4* keys4 = reinterpret_cast<uint4*>(keys);
+#pragma unroll 4
+    for (int i4 = tid; i4 < nloc / 4; i4 += kTopkThreads) {
+        const int64_t c = c0 + 4 * (int64_t)i4;
+        const int blk = slist[(c >> 6) - e0];
+        const float4 z = sc4[i4];
+        const int64_t slot = (int64_t)blk * kBlock + (c & 63);
+        uint4 kv = make_uint4(0u, 0u, 0u, 0u);
         if (blk >= 0 && blk < nb) {
-            if (slot < n) key = order_key(sc[c]);
+            kv.x = slot + 0 < n ? order_key(z.x) : 0u;
+            kv.y = slot + 1 < n ? order_key(z.y) : 0u;
+            kv.z = slot + 2 < n ? order_key(z.z) : 0u;
+            kv.w = slot + 3 < n ? order_key(z.w) : 0u;
         } else {
             bad_list = true;
         }
-        keys[i] = key;
-        v += key != 0u;
+        keys4[i4] = kv;
+        v += (kv.x != 0u) + (kv.y != 0u) + (kv.z != 0u) + (kv.w != 0u);
     }
     if (bad_list && rr % rows == 0) set_status(status, SPIN_STATUS_BAD_LIST);
     int nvalid_loc;
@@ -364,7 +386,7 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
         for (int it = 0; it < kItems; ++it) {
             if (keep[it] && pos < K) {
                 const int64_t c = c0 + base + tid * kItems + it;
-                out[pos++] = (int32_t)((int64_t)lst[c >> 6] * kBlock + (c & 63));
+                out[pos++] = (int32_t)((int64_t)slist[(c >> 6) - e0] * kBlock + (c & 63));
             }
         }
         written += keep_total;
@@ -375,15 +397,252 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
     cluster.sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
+// ---------------------------------------------------------------------------------------
+// Row kernel: one 1024-thread CTA per (request, row), for launches with enough rows to fill
+// the GPU.  Pass A reads every candidate once (float4) and builds a 4096-bin histogram of
+// the top 12 bits of its key; the bin holding the K-th key is found.  Pass B collects the
+// low 20 bits and the candidate index of the keys in that bin (usually a few thousand)
+// into shared memory, where two 10-bit radix passes finish the exact threshold.  Pass C
+// writes the kept slot ids in candidate (= ascending slot) order.  If the boundary bin
+// overflows the collection buffer, the threshold is refined over global memory instead.
+// ---------------------------------------------------------------------------------------
+constexpr int kTrThreads = 1024;
+constexpr int kTrBins = 4096;
+constexpr int kTrCollect = 8192;
+
+struct TrShared {
+    int hist[kTrBins];
+    uint32_t ckey[kTrCollect];  // low 20 bits of the boundary-bin keys
+    int ncol;
+    int scan[33];
+    uint32_t prefix;
+    int kk;
+};
+
+// block-wide digit search: the digit d with (#keys with digit > d) < kk <= (#keys >= d);
+// returns d and the count above it.  nb bins, each warp owning a contiguous descending range.
+__device__ __forceinline__ void tr_find_digit(const int* hist, int nbins, int kk, TrShared& sh, int& digit_out,
+                                              int& above_out) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = kTrThreads / 32;
+    const int per_warp = nbins / nw, per_lane = per_warp / 32;
+    // bins of warp w: top = nbins-1 - w*per_warp, descending; lane l owns per_lane of them
+    const int top = nbins - 1 - wid * per_warp - lane * per_lane;
+    int cnt = 0;
+    for (int b = 0; b < per_lane; ++b) cnt += hist[top - b];
+    const int inc = warp_incl_scan(cnt);
+    __shared__ int wsum[32];
+    if (lane == 31) wsum[wid] = inc;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < wid; ++w) before += wsum[w];
+    const int excl = before + inc - cnt;
+    if (excl < kk && excl + cnt >= kk) {
+        int above = excl, digit = top;
+        for (int b = 0; b < per_lane; ++b) {
+            const int h = hist[top - b];
+            if (above + h >= kk) { digit = top - b; break; }
+            above += h;
+        }
+        sh.prefix = (uint32_t)digit;
+        sh.kk = above;
+    }
+    __syncthreads();
+    digit_out = (int)sh.prefix;
+    above_out = sh.kk;
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kTrThreads, 1)
+topk_row_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __restrict__ list,
+                const int32_t* __restrict__ n_list, const int32_t* __restrict__ n_slots, int rows,
+                int32_t* __restrict__ topk_idx, uint32_t* status) {
+    extern __shared__ __align__(16) unsigned char tr_smem[];
+    TrShared& sh = *reinterpret_cast<TrShared*>(tr_smem);
+    int* slist = reinterpret_cast<int*>(tr_smem + sizeof(TrShared));  // the row's list entries
+    const Dims dm = dims_of(cfg);
+    const int rr = blockIdx.x, req = rr / rows;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int K = cfg.top_k;
+    int32_t* out = topk_idx + (int64_t)rr * K;
+    const int64_t n = n_slots[req];
+    const int64_t cnt = n_list[req];
+    if (n < 0 || n > dm.max_slots || cnt < 0 || cnt > dm.MB) {
+        if (tid == 0) set_status(status, (n < 0 || n > dm.max_slots) ? SPIN_STATUS_BAD_N : SPIN_STATUS_BAD_LIST);
+        for (int k = tid; k < K; k += kTrThreads) out[k] = -1;
+        return;
+    }
+    const int64_t nb = (n + kBlock - 1) / kBlock;
+    const int32_t* lst = list + (int64_t)req * dm.MB;
+    const float4* sc4 = reinterpret_cast<const float4*>(scores + (int64_t)rr * dm.MB * kBlock);
+    const int C4 = (int)cnt * (kBlock / 4);
+    bool bad_list = false;
+    for (int i = tid; i < cnt; i += kTrThreads) {
+        const int b = lst[i];
+        if (b < 0 || b >= nb) bad_list = true;
+        slist[i] = b;
+    }
+    for (int b = tid; b < kTrBins; b += kTrThreads) sh.hist[b] = 0;
+    if (tid == 0) sh.ncol = 0;
+    if (bad_list && rr % rows == 0) set_status(status, SPIN_STATUS_BAD_LIST);
+    __syncthreads();
+    // 4 keys of float4 i4 (0 = not a live candidate)
+    auto keys4 = [&](int i4, const float4& z, uint32_t* k4) {
+        const int c = 4 * i4;
+        const int blk = slist[c >> 6];
+        const int64_t slot = (int64_t)blk * kBlock + (c & 63);
+        const bool okb = blk >= 0 && blk < nb;
+        k4[0] = okb && slot + 0 < n ? order_key(z.x) : 0u;
+        k4[1] = okb && slot + 1 < n ? order_key(z.y) : 0u;
+        k4[2] = okb && slot + 2 < n ? order_key(z.z) : 0u;
+        k4[3] = okb && slot + 3 < n ? order_key(z.w) : 0u;
+    };
+
+    // pass A: histogram of the top 12 bits
+    int v = 0;
+    const int C4pad = (C4 + 31) & ~31;
+#pragma unroll 8
+    for (int i4 = tid; i4 < C4pad; i4 += kTrThreads) {
+        uint32_t k4[4] = {0u, 0u, 0u, 0u};
+        if (i4 < C4) keys4(i4, sc4[i4], k4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int bin = k4[e] ? (int)(k4[e] >> 20) : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&sh.hist[bin], __popc(same));
+            v += k4[e] != 0u;
+        }
+    }
+    int nvalid;
+    block_excl_scan(v, sh.scan, &nvalid);
+
+    uint32_t T = 0;   // full threshold key
+    int kk = 0;       // keys == T to keep (lowest candidate index first)
+    if (nvalid > K) {
+        int d1, above1;
+        tr_find_digit(sh.hist, kTrBins, K, sh, d1, above1);
+        const int need = K - above1;  // still needed from bin d1
+        // pass B: collect the low 20 bits of bin d1's keys
+#pragma unroll 8
+        for (int i4 = tid; i4 < C4; i4 += kTrThreads) {
+            uint32_t k4[4];
+            keys4(i4, sc4[i4], k4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (k4[e] && (int)(k4[e] >> 20) == d1) {
+                    const int slot = atomicAdd(&sh.ncol, 1);
+                    if (slot < kTrCollect) sh.ckey[slot] = k4[e] & 0xFFFFFu;
+                }
+        }
+        __syncthreads();
+        const int ncol = sh.ncol;
+        uint32_t prefix = (uint32_t)d1 << 20, mask = 0xFFF00000u;
+        int kk2 = need;
+        const int shifts[2] = {10, 0};
+        for (int pass = 0; pass < 2; ++pass) {
+            const int shift = shifts[pass];
+            for (int b = tid; b < 1024; b += kTrThreads) sh.hist[b] = 0;
+            __syncthreads();
+            if (ncol <= kTrCollect) {
+                const uint32_t high = (uint32_t)d1 << 20;  // the bin's common top 12 bits
+                for (int i = tid; i < ncol; i += kTrThreads) {
+                    const uint32_t key = high | sh.ckey[i];
+                    if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 1023u], 1);
+                }
+            } else {  // the boundary bin overflowed the buffer: refine over global memory
+#pragma unroll 4
+                for (int i4 = tid; i4 < C4; i4 += kTrThreads) {
+                    uint32_t k4[4];
+                    keys4(i4, sc4[i4], k4);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (k4[e] && (k4[e] & mask) == prefix) atomicAdd(&sh.hist[(k4[e] >> shift) & 1023u], 1);
+                }
+            }
+            __syncthreads();
+            int d, above;
+            tr_find_digit(sh.hist, 1024, kk2, sh, d, above);
+            prefix |= (uint32_t)d << shift;
+            mask |= 1023u << shift;
+            kk2 -= above;
+        }
+        T = prefix;
+        kk = kk2;
+    }
+
+    // pass C: ordered write (keys > T, then the first kk keys == T in candidate order).
+    // A thread takes kV consecutive float4 (16 candidates) per round; the next round's
+    // loads are issued before this round's scans.
+    constexpr int kV = 4, kItems = 4 * kV;
+    int written = 0, eq_seen = 0;
+    const bool take_all = nvalid <= K;
+    float4 zn[kV];
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+        const int i4 = tid * kV + j;
+        zn[j] = i4 < C4 ? sc4[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int base4 = 0; base4 < C4; base4 += kTrThreads * kV) {
+        float4 zc[kV];
+#pragma unroll
+        for (int j = 0; j < kV; ++j) zc[j] = zn[j];
+        const int nbase = base4 + kTrThreads * kV;
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+            const int i4 = nbase + tid * kV + j;
+            if (i4 < C4) zn[j] = sc4[i4];
+        }
+        uint32_t kx[kItems];
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+            const int i4 = base4 + tid * kV + j;
+            uint32_t k4[4] = {0u, 0u, 0u, 0u};
+            if (i4 < C4) keys4(i4, zc[j], k4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) kx[4 * j + e] = k4[e];
+        }
+        int n_eq = 0;
+#pragma unroll
+        for (int e = 0; e < kItems; ++e) n_eq += !take_all && kx[e] != 0u && kx[e] == T;
+        int eq_total;
+        int eq_rank = eq_seen + block_excl_scan(n_eq, sh.scan, &eq_total);
+        uint32_t keep = 0;  // bit e: candidate e of this thread is kept
+#pragma unroll
+        for (int e = 0; e < kItems; ++e) {
+            bool kp = take_all ? (kx[e] != 0u) : (kx[e] > T);
+            if (!take_all && kx[e] != 0u && kx[e] == T) { kp = eq_rank < kk; ++eq_rank; }
+            keep |= (uint32_t)kp << e;
+        }
+        int keep_total;
+        int pos = written + block_excl_scan(__popc(keep), sh.scan, &keep_total);
+#pragma unroll
+        for (int e = 0; e < kItems; ++e)
+            if (((keep >> e) & 1u) && pos < K) {
+                const int c = 4 * (base4 + tid * kV) + e;
+                out[pos++] = (int32_t)((int64_t)slist[c >> 6] * kBlock + (c & 63));
+            }
+        written += keep_total;
+        eq_seen += eq_total;
+    }
+    for (int k = written + tid; k < K; k += kTrThreads) out[k] = -1;
+}
+
 static size_t topk_cluster_smem(const spin_config& cfg) {
     const Dims dm = dims_of(cfg);
-    const int64_t per = ((int64_t)dm.MB * kBlock + kTkCluster - 1) / kTkCluster;
-    return (size_t)per * 4;
+    return (size_t)kTkListOffset(cfg) * 4 + (size_t)(dm.MB / kTkCluster + 2) * 4;
 }
 
 cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32_t* list,
                         const int32_t* n_list, const int32_t* n_slots, int rows, int32_t* topk_idx,
                         uint32_t* status, cudaStream_t s) {
+    const Dims dm = dims_of(cfg);
+    const size_t row_smem = sizeof(TrShared) + (size_t)dm.MB * 4;
+    if ((int64_t)cfg.n_req * rows >= 32 && row_smem <= 200 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)row_smem);
+        if (e != cudaSuccess) return e;
+        topk_row_kernel<<<cfg.n_req * rows, kTrThreads, row_smem, s>>>(cfg, scores, list, n_list, n_slots, rows,
+                                                                       topk_idx, status);
+        return cudaGetLastError();
+    }
     const size_t smem = topk_cluster_smem(cfg);
     if (smem + sizeof(TkClusterShared) <= 200 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

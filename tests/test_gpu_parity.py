@@ -153,6 +153,34 @@ def test_tcgen05_matches_generic_kernel(k_dtype):
         assert torch.allclose(a, b, rtol=1e-4, atol=1e-3), (r, (a - b).abs().max())
 
 
+# ------------------------------------------------------------------------- top-K paths
+
+def test_topk_many_rows_ragged():
+    """40 requests (enough rows for the one-CTA-per-row top-K) of ragged lengths."""
+    wl = syn.CONFIGS["pr1"].replace(n_req=40, n0=6000, steps=3, gamma_bp=1000, shuffle=True)
+    h = Harness(wl)
+    ns = torch.randint(1, 6000, (40,), generator=torch.Generator().manual_seed(4)).to(torch.int32)
+    h.inp.n_slots.copy_(ns)
+    run_steps(h, 3)
+
+
+def test_topk_all_equal_scores():
+    """Degenerate case: w = 0 makes every score 0, so the top-K is the K lowest slot ids
+    (and the boundary bin overflows the collection buffer of the per-row kernel)."""
+    wl = syn.CONFIGS["v4flash"].replace(n_req=36, n0=20000, steps=2, n_heads=8, head_dim=64,
+                                        kv_heads=8, q_dtype="f32", k_dtype="f32", top_k=512)
+    h = Harness(wl)
+    for step in range(2):
+        q, w, qp = h.inp.step_inputs()
+        out = h.step(step, 0, q, torch.zeros_like(w), qp)
+        h.inp.advance(step)
+    for r in range(wl.n_req):
+        blks = out["blist"][r, : out["nlist"][r]]
+        ids = (blks[:, None] * 64 + np.arange(64)[None, :]).ravel()
+        ids = ids[ids < np_(h.inp.n_slots)[r]]
+        np.testing.assert_array_equal(out["topk"][r, 0], np.sort(ids)[: wl.top_k])
+
+
 # ------------------------------------------------------------------------------- MTP
 
 def test_mtp_small_union_and_replay():
