@@ -13,21 +13,26 @@
 //   by 2D TMA in the 128-byte-swizzled K-major layout the MMA reads.
 // FP8 (e4m3) keys: kind::f8f6f4 straight from the TMA-loaded pages, no conversion.  q is
 //   carried as two e4m3 terms: for every (row, head) a power-of-two scale g puts
-//   max|q|/g in (224, 448]; hi = e4m3(q/g), lo = e4m3(q/g - hi), and the MMA runs over
-//   K = 2 x 128 with the keys repeated against [hi | lo], so the accumulator holds
-//   k . (hi + lo) with |q/g - hi - lo| <= 2^-8 |q/g| per element (plus the e4m3
-//   subnormal floor); the epilogue multiplies by g.  The per-slot dequantisation scale is
-//   applied before the ReLU.
+//   max|q|/g in (224, 448]; hi = e4m3(q/g), lo = e4m3(q/g - hi).  Both terms are rows of
+//   the B operand (N = 2 x 64 per query row), so one MMA of K = 32 covers both and a tile
+//   needs 4 MMAs; the epilogue adds the hi and lo columns of a head, k.(hi + lo), where
+//   |q/g - hi - lo| <= 2^-8 |q/g| per element (plus the e4m3 subnormal floor), and
+//   multiplies by g.  The per-slot dequantisation scale is applied before the ReLU.
+// A tcgen05.mma costs a near-constant issue time whatever its N, so the kernel keeps
+// the instruction count per tile low and interleaves two tiles (two accumulator chains)
+// when TMEM holds four accumulators.
 //
 // Warp roles of a persistent CTA (tiles = pairs of selected blocks of one request):
-//   warp 0      producer: one (FP8) or two (bf16) 2D TMA loads per page into a ring
-//   warp 1      TMEM owner and MMA issuer (one thread): 8 tcgen05.mma per tile into
-//               double-buffered accumulators; stages q when the request changes
-//   warps 2-9   epilogue, two warps per TMEM lane quarter taking alternate tiles:
+//   warps 0, 2  producers (even and odd tiles): one (FP8) or two (bf16) 2D TMA loads per
+//               page into a ring
+//   warp 1      TMEM owner and MMA issuer (one thread): 4 (FP8) or 8 (bf16) tcgen05.mma
+//               per tile, two tiles interleaved when possible; stages q when the request
+//               changes
+//   warps 3-10  epilogue, two warps per TMEM lane quarter taking alternate tiles:
 //               tcgen05.ld of a tile's accumulators (one slot per thread),
 //               z = sum_h w_h g_h max(s_i acc_h, 0) per row, masked to i < N, stored
-// Accumulators are 2-4 deep in TMEM (N <= 128: 4), the per-slot FP8 scales travel with
-// the pages by bulk copy into a ring of their own.
+// Accumulators are 2-4 deep in TMEM (N <= 128: 4); the epilogue fetches the per-slot FP8
+// scales of its next tile while it works on the current one.
 // Every warp resolves its tiles' pages 32 at a time (one tile per lane), so the dependent
 // list and block-table loads are paid once per 32 tiles.  Every barrier wait is bounded
 // and a timeout unwinds all roles.
@@ -48,7 +53,8 @@ constexpr int kTcM = 128;      // slots per tile (two pages)
 constexpr int kTcMaxRows = 4;  // N = 64 * rows <= 256
 constexpr int kTcMaxReq = 2048;
 constexpr int kTcEpiWarps = 8;                      // two per TMEM lane quarter
-constexpr int kTcThreads = (2 + kTcEpiWarps) * 32;  // producer, MMA, epilogue
+constexpr int kTcEpiWarp0 = 3;                      // warps 0, 2: producers; 1: MMA; 3-10: epilogue
+constexpr int kTcThreads = (kTcEpiWarp0 + kTcEpiWarps) * 32;
 constexpr int kTcMaxAcc = 4;                        // accumulator buffers in TMEM
 constexpr int kTcStagesMax = 8;  // operand ring depth (tiles in flight per CTA): 128 KB either way
 __host__ __device__ constexpr int tc_stages(bool fp8) { return fp8 ? 8 : 4; }
@@ -93,6 +99,23 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, waited for in the same statement.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 64 consecutive fp32 columns of this thread's TMEM lane, waited for in the same statement.
@@ -156,7 +179,6 @@ struct TileInfo {
 struct TcHdr {
     uint64_t full[kTcStagesMax];   // tile landed in shared memory
     uint64_t empty[kTcStagesMax];  // tile consumed by the MMAs
-    uint64_t sfull[kTcStagesMax + kTcMaxAcc];  // FP8: the tile's slot scales landed
     uint64_t tfull[kTcMaxAcc];  // accumulator ready
     uint64_t tempty[kTcMaxAcc]; // accumulator drained by the epilogue
     uint64_t qfull;             // q staged by TMA (bf16 keys)
@@ -167,7 +189,7 @@ struct TcHdr {
 };
 
 struct TcLayout {
-    uint32_t prefix, stage_a, scales, qbuf, wbuf, tile_bytes, total;
+    uint32_t prefix, stage_a, qbuf, wbuf, tile_bytes, total;
 };
 
 // accumulator buffers that fit in TMEM's 512 columns
@@ -181,8 +203,6 @@ __host__ __device__ inline TcLayout tc_layout(int R, int rows, bool fp8) {
     off += ((uint32_t)(R + 1) * 4 + 1023) & ~1023u;
     L.stage_a = off;
     off += tc_stages(fp8) * L.tile_bytes;
-    L.scales = off;                                      // [stages + acc][128] fp32 (FP8 only)
-    off += fp8 ? (kTcStagesMax + kTcMaxAcc) * kTcM * 4 : 0;
     L.qbuf = off;
     off += (uint32_t)(64 * rows) * 256;                  // two regions of N rows x 128 B
     L.wbuf = off;
@@ -199,20 +219,19 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Dims dm = dims_of(cfg);
     const int rows = a.rows;
-    const int N = kTcNH * rows;
+    const int NQ = kTcNH * rows;          // query vectors (rows x heads)
+    const int N = FP8 ? 2 * NQ : NQ;      // MMA N = accumulator columns per tile
     const TcLayout L = tc_layout(dm.R, rows, FP8);
     TcHdr* hdr = reinterpret_cast<TcHdr*>(smem);
     int* prefix = reinterpret_cast<int*>(smem + L.prefix);
     unsigned char* sA = smem + L.stage_a;
     unsigned char* sQ = smem + L.qbuf;
     float* sW = reinterpret_cast<float*>(smem + L.wbuf);
-    float* sScale = reinterpret_cast<float*>(smem + L.scales);
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int NACC = tc_nacc(N);
     const uint32_t tmem_cols = (uint32_t)(NACC * N) <= 256u ? 256u : 512u;
-    const uint32_t qregion = (uint32_t)N * 128;  // bytes of one B region
+    const uint32_t qregion = (uint32_t)NQ * 128;  // bf16: bytes of one K half of B
     constexpr int kTcStages = tc_stages(FP8);
-    const int NSR = kTcStages + NACC;  // scale ring: the producer leads the epilogue by < NSR tiles
 
     // ------------------------------------------------------------------ set-up
     if (wid == 0) {
@@ -239,7 +258,6 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 mbar_init(&hdr->full[s], 1);
                 mbar_init(&hdr->empty[s], 1);
             }
-            for (int s = 0; s < kTcStagesMax + kTcMaxAcc; ++s) mbar_init(&hdr->sfull[s], 1);
             for (int s = 0; s < kTcMaxAcc; ++s) {
                 mbar_init(&hdr->tfull[s], 1);
                 mbar_init(&hdr->tempty[s], 128);
@@ -297,11 +315,15 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     // warp-cooperative: lane j resolves tile base + j; tile() broadcasts one tile's info
     TileInfo mine;
     int batch_base = -1;
-    auto tile = [&](int t) -> TileInfo {
+    auto refresh = [&](int t) {  // make the batch hold tile t (t non-decreasing per warp)
         if (batch_base < 0 || t >= batch_base + 32) {
             batch_base = t;
             if (t + lane < t1) decode(t + lane, mine);
         }
+    };
+    auto bc = [&](int v, int t) { return __shfl_sync(0xffffffffu, v, t - batch_base); };
+    auto tile = [&](int t) -> TileInfo {
+        refresh(t);
         const int j = t - batch_base;
         TileInfo r;
         r.req = __shfl_sync(0xffffffffu, mine.req, j);
@@ -318,11 +340,14 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         set_status(a.status, SPIN_STATUS_TIMEOUT);
     };
 
-    if (wid == 0) {
-        // -------------------------------------------------------------- producer
+    if (wid == 0 || wid == 2) {
+        // -------------------------------------------------------------- producers
+        // warp 0 loads the even tiles, warp 2 the odd ones (stages alternate with them)
+        const int par = wid >> 1;
         uint32_t issued = 0, phases = 0;  // per stage: ever filled, parity of its last fill
-        for (int t = t0, it = 0; t < t1; ++t, ++it) {
-            const TileInfo ti = tile(t);
+        for (int t = t0 + par, it = par; t < t1; t += 2, it += 2) {
+            refresh(t);
+            const int page0 = bc(mine.page0, t), page1 = bc(mine.page1, t);
             const int s = it % kTcStages;
             const uint32_t ph = (uint32_t)(it / kTcStages) & 1u;
             int ok = 1;
@@ -332,30 +357,8 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 break;
             }
             if (lane == 0) {
-                const int page[2] = {ti.page0, ti.page1};  // indexed by unrolled constants only
                 const uint32_t page_bytes = FP8 ? (uint32_t)(kBlock * kTcD) : (uint32_t)(kBlock * kTcD * 2);
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    if (page[h] >= 0) bytes += page_bytes;
-                if (FP8) {
-                    // the tile's 2 x 64 slot scales, into the scale ring (epilogue side)
-                    const int sr = it % NSR;
-                    uint32_t sb = 0;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        if (page[h] >= 0) sb += kBlock * 4;
-                    if (sb == 0) {
-                        mbar_arrive(&hdr->sfull[sr]);
-                    } else {
-                        mbar_arrive_expect_tx(&hdr->sfull[sr], sb);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            if (page[h] >= 0)
-                                bulk_g2s(sScale + sr * kTcM + h * kBlock, a.k_scale + (int64_t)page[h] * kBlock,
-                                         kBlock * 4, &hdr->sfull[sr]);
-                    }
-                }
+                const uint32_t bytes = (page0 >= 0 ? page_bytes : 0u) + (page1 >= 0 ? page_bytes : 0u);
                 if (bytes == 0) {
                     mbar_arrive(&hdr->full[s]);
                 } else {
@@ -363,16 +366,12 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                     unsigned char* stage = sA + (size_t)s * L.tile_bytes;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        if (page[h] < 0) continue;
-                        const int y = page[h] * kBlock;
-                        if (FP8) {
-                            // one 64-row x 128-byte box: the page's keys, 128B-swizzled
-                            tma_load_2d(stage + h * 8192, &kmap, 0, y, &hdr->full[s]);
-                        } else {
-                            // two 64-row x 64-element boxes: the two K halves of the page
-                            tma_load_2d(stage + h * 8192, &kmap, 0, y, &hdr->full[s]);
-                            tma_load_2d(stage + kTcM * 128 + h * 8192, &kmap, 64, y, &hdr->full[s]);
-                        }
+                        const int page = h ? page1 : page0;
+                        if (page < 0) continue;
+                        const int y = page * kBlock;
+                        // FP8: one 64-row x 128-byte box; bf16: the two 64-element K halves
+                        tma_load_2d(stage + h * 8192, &kmap, 0, y, &hdr->full[s]);
+                        if (!FP8) tma_load_2d(stage + kTcM * 128 + h * 8192, &kmap, 64, y, &hdr->full[s]);
                     }
                 }
             }
@@ -387,11 +386,16 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     } else if (wid == 1) {
         // ------------------------------------------------------------ MMA issuer
         const uint32_t idesc = idesc_mma(FP8 ? 0u : 1u, (uint32_t)N, (uint32_t)kTcM);
+        const int G = NACC >= 4 ? 2 : 1;  // tiles whose MMAs are interleaved
         int cur_req = -1;
         uint32_t qphase = 0, qload_phase = 0;
         bool issued_any = false;
-        for (int t = t0, it = 0; t < t1; ++t, ++it) {
-            const int req = tile(t).req;
+        // ring positions of tile `it` (advanced incrementally: no division on this path)
+        int sa = 0, ac = 0;
+        uint32_t pha = 0, phc = 0;
+        for (int t = t0, it = 0; t < t1;) {
+            refresh(t);
+            const int req = bc(mine.req, t);
             if (req != cur_req) {
                 if (issued_any) {  // the MMAs of the previous request still read sQ
                     if (lane == 0) tc_commit(&hdr->qdone);
@@ -400,13 +404,15 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                     qphase ^= 1u;
                 }
                 if (FP8) {
-                    // B = [hi | lo]: lane handles q rows n = lane, lane + 32, ...
-                    for (int n = lane; n < N; n += 32) {
+                    // B rows r*128 + h (hi) and r*128 + 64 + h (lo), 128 e4m3 each; lane
+                    // handles the query vectors n = lane, lane + 32, ...
+                    for (int n = lane; n < NQ; n += 32) {
                         const int r = n / kTcNH, h = n % kTcNH;
                         const __nv_bfloat16* qrow =
                             reinterpret_cast<const __nv_bfloat16*>(a.q) + (((int64_t)req * rows + r) * kTcNH + h) * kTcD;
                         const float inv_g = 1.0f / q_row_scale(qrow);   // exact: a power of two
                         const uint4* src = reinterpret_cast<const uint4*>(qrow);
+                        const int nh = r * 2 * kTcNH + h, nl = nh + kTcNH;
 #pragma unroll 2
                         for (int ch = 0; ch < kTcD / 16; ++ch) {         // 16 elements -> 16 B of e4m3
                             const uint4 u0 = src[2 * ch], u1 = src[2 * ch + 1];
@@ -432,9 +438,10 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                                 hw[e] = hv;
                                 lw[e] = lv;
                             }
-                            const uint32_t off = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((ch ^ (n & 7)) << 4));
-                            *reinterpret_cast<uint4*>(sQ + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                            *reinterpret_cast<uint4*>(sQ + qregion + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                            const uint32_t oh = (uint32_t)((nh >> 3) * 1024 + (nh & 7) * 128 + ((ch ^ (nh & 7)) << 4));
+                            const uint32_t ol = (uint32_t)((nl >> 3) * 1024 + (nl & 7) * 128 + ((ch ^ (nl & 7)) << 4));
+                            *reinterpret_cast<uint4*>(sQ + oh) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            *reinterpret_cast<uint4*>(sQ + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                         }
                     }
                     fence_async_smem();
@@ -442,7 +449,7 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 } else {
                     // q rows of this request by TMA, straight into the swizzled B layout
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&hdr->qfull, (uint32_t)N * kTcD * 2);
+                        mbar_arrive_expect_tx(&hdr->qfull, (uint32_t)NQ * kTcD * 2);
                         const int y = req * rows * kTcNH;
                         tma_load_2d(sQ, &qmap, 0, y, &hdr->qfull);
                         tma_load_2d(sQ + qregion, &qmap, 64, y, &hdr->qfull);
@@ -453,39 +460,61 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 }
                 cur_req = req;
             }
-            const int sa = it % kTcStages;
-            const uint32_t pha = (uint32_t)(it / kTcStages) & 1u;
-            bool ok = mbar_wait(&hdr->full[sa], pha, &hdr->abort_flag);
-            const int acc = it % NACC;
-            const uint32_t phc = (uint32_t)(it / NACC) & 1u;
-            if (ok) ok = mbar_wait(&hdr->tempty[acc], phc ^ 1u, &hdr->abort_flag);
-            if (!ok) { fail_wait(); break; }
+            // a pair of tiles of this request when accumulators allow, else one
+            int g = 1;
+            if (G == 2 && t + 1 < t1) {
+                refresh(t + 1);
+                if (bc(mine.req, t + 1) == req) g = 2;
+            }
+            int sa1 = sa + 1, ac1 = ac + 1;
+            uint32_t pha1 = pha, phc1 = phc;
+            if (sa1 == kTcStages) { sa1 = 0; pha1 ^= 1u; }
+            if (ac1 == NACC) { ac1 = 0; phc1 ^= 1u; }
+            bool ok = mbar_wait(&hdr->full[sa], pha, &hdr->abort_flag) &&
+                      mbar_wait(&hdr->tempty[ac], phc ^ 1u, &hdr->abort_flag);
+            if (g == 2)
+                ok = ok && mbar_wait(&hdr->full[sa1], pha1, &hdr->abort_flag) &&
+                     mbar_wait(&hdr->tempty[ac1], phc1 ^ 1u, &hdr->abort_flag);
+            if (!__all_sync(0xffffffffu, ok)) { fail_wait(); break; }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t a_base = smem_u32(sA + (size_t)sa * L.tile_bytes);
-                const uint32_t b_base = smem_u32(sQ);
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * N);
+                // descriptors of the k-step 0 operands; a k-step of 32 bytes adds 2 to the
+                // encoded start address, a K half of a bf16 tile adds 16 KB >> 4
+                const uint64_t a0 = smem_desc_sw128(smem_u32(sA + (size_t)sa * L.tile_bytes));
+                const uint64_t a1 = smem_desc_sw128(smem_u32(sA + (size_t)sa1 * L.tile_bytes));
+                const uint64_t b0 = smem_desc_sw128(smem_u32(sQ));
+                const uint32_t d0 = tmem_base + (uint32_t)(ac * N), d1 = tmem_base + (uint32_t)(ac1 * N);
                 if (FP8) {
-                    // K = 2 x 128: the keys against hi, then the same keys against lo
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma_f8(d_tmem, smem_desc_sw128(a_base + kk * 32),
-                                      smem_desc_sw128(b_base + part * qregion + kk * 32), idesc, (part | kk) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        tc_mma_f8(d0, a0 + 2 * kk, b0 + 2 * kk, idesc, kk ? 1u : 0u);
+                        if (g == 2) tc_mma_f8(d1, a1 + 2 * kk, b0 + 2 * kk, idesc, kk ? 1u : 0u);
+                    }
                 } else {
+                    const uint64_t bh = qregion >> 4;
 #pragma unroll
-                    for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma_f16(d_tmem, smem_desc_sw128(a_base + kh * (kTcM * 128) + kk * 32),
-                                       smem_desc_sw128(b_base + kh * qregion + kk * 32), idesc, (kh | kk) ? 1u : 0u);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ao = (uint64_t)((ks >> 2) * (kTcM * 128 >> 4) + 2 * (ks & 3));
+                        const uint64_t bo = (uint64_t)(ks >> 2) * bh + 2 * (ks & 3);
+                        tc_mma_f16(d0, a0 + ao, b0 + bo, idesc, ks ? 1u : 0u);
+                        if (g == 2) tc_mma_f16(d1, a1 + ao, b0 + bo, idesc, ks ? 1u : 0u);
+                    }
                 }
                 tc_commit(&hdr->empty[sa]);
-                tc_commit(&hdr->tfull[acc]);
+                tc_commit(&hdr->tfull[ac]);
+                if (g == 2) {
+                    tc_commit(&hdr->empty[sa1]);
+                    tc_commit(&hdr->tfull[ac1]);
+                }
             }
             issued_any = true;
             __syncwarp();
+            // advance by g tiles
+            if (g == 2) { sa = sa1; ac = ac1; pha = pha1; phc = phc1; }
+            if (++sa == kTcStages) { sa = 0; pha ^= 1u; }
+            if (++ac == NACC) { ac = 0; phc ^= 1u; }
+            t += g;
+            it += g;
         }
         // every issued MMA has finished before TMEM is released
         if (issued_any) {
@@ -496,17 +525,26 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     } else {
         // ------------------------------------------------------------- epilogue
         const int quarter = wid & 3;
-        const int parity = (wid - 2) / 4;       // this warp takes the tiles it with it % 2 == parity
+        const int parity = (wid - kTcEpiWarp0) / 4;  // this warp takes the tiles it with it % 2 == parity
         const int m = quarter * 32 + lane;      // slot row of the tile = TMEM lane
         const int h = m >> 6, s = m & 63;
-        float* wloc = sW + (size_t)(wid - 2) * N;
+        float* wloc = sW + (size_t)(wid - kTcEpiWarp0) * NQ;
         int cur_req = -1;
+        // FP8: the slot scale of this warp's next tile is loaded one tile ahead
+        auto scale_of = [&](int t) -> float {
+            if (!FP8 || t >= t1) return 1.0f;
+            refresh(t);
+            const int pg = bc(h ? mine.page1 : mine.page0, t);
+            return pg >= 0 ? __ldg(a.k_scale + (int64_t)pg * kBlock + s) : 1.0f;
+        };
+        float scale_next = scale_of(t0 + parity);
         for (int t = t0 + parity, it = parity; t < t1; t += 2, it += 2) {
+            const float scale = scale_next;
             const TileInfo ti = tile(t);
             const int req = ti.req;
             if (req != cur_req) {
                 __syncwarp();
-                for (int n = lane; n < N; n += 32) {
+                for (int n = lane; n < NQ; n += 32) {
                     float g = 1.0f;
                     if (FP8) {
                         const int r = n / kTcNH, hh = n % kTcNH;
@@ -527,30 +565,34 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 set_status(a.status, blk == -2 ? SPIN_STATUS_BAD_LIST : SPIN_STATUS_BAD_PAGE);
             const int acc = it % NACC;
             const uint32_t phc = (uint32_t)(it / NACC) & 1u;
-            float scale = 1.0f;
-            if (FP8) {
-                const int sr = it % NSR;
-                if (!mbar_wait(&hdr->sfull[sr], (uint32_t)(it / NSR) & 1u, &hdr->abort_flag)) { fail_wait(); break; }
-                scale = sScale[sr * kTcM + m];
-            }
+            scale_next = scale_of(t + 2);  // (ti holds everything tile t still needs)
             if (!mbar_wait(&hdr->tfull[acc], phc, &hdr->abort_flag)) { fail_wait(); break; }
             tc_fence_after();
+            const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
             for (int r = 0; r < rows; ++r) {
-                float v[64];
-                tc_ld64(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N + r * kTcNH), v);
-                const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH);
                 float z4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float4 wv = wr[j];
-                    const float x0 = FP8 ? scale * v[4 * j + 0] : v[4 * j + 0];
-                    const float x1 = FP8 ? scale * v[4 * j + 1] : v[4 * j + 1];
-                    const float x2 = FP8 ? scale * v[4 * j + 2] : v[4 * j + 2];
-                    const float x3 = FP8 ? scale * v[4 * j + 3] : v[4 * j + 3];
-                    z4[0] = fmaf(wv.x, fmaxf(x0, 0.0f), z4[0]);
-                    z4[1] = fmaf(wv.y, fmaxf(x1, 0.0f), z4[1]);
-                    z4[2] = fmaf(wv.z, fmaxf(x2, 0.0f), z4[2]);
-                    z4[3] = fmaf(wv.w, fmaxf(x3, 0.0f), z4[3]);
+                for (int half = 0; half < 2; ++half) {  // heads 32*half .. 32*half + 31
+                    float v[32];
+                    if (FP8) {
+                        // columns r*128 + h (k.hi) and r*128 + 64 + h (k.lo)
+                        float u[32];
+                        tc_ld32(trow + (uint32_t)(r * 2 * kTcNH + half * 32), v);
+                        tc_ld32(trow + (uint32_t)(r * 2 * kTcNH + kTcNH + half * 32), u);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = scale * (v[j] + u[j]);
+                    } else {
+                        tc_ld32(trow + (uint32_t)(r * kTcNH + half * 32), v);
+                    }
+                    const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH + half * 32);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 wv = wr[j];
+                        z4[0] = fmaf(wv.x, fmaxf(v[4 * j + 0], 0.0f), z4[0]);
+                        z4[1] = fmaf(wv.y, fmaxf(v[4 * j + 1], 0.0f), z4[1]);
+                        z4[2] = fmaf(wv.z, fmaxf(v[4 * j + 2], 0.0f), z4[2]);
+                        z4[3] = fmaf(wv.w, fmaxf(v[4 * j + 3], 0.0f), z4[3]);
+                    }
                 }
                 float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
                 if (!live || z == 0.0f) z = 0.0f;
@@ -605,6 +647,7 @@ static bool encode_rows(CUtensorMap* map, CUtensorMapDataType dt, int elt, const
 }
 
 bool score_tc_supported(const spin_config& cfg, int rows) {
+    if (cfg.k_dtype == SPIN_DTYPE_E4M3 && rows > 2) return false;  // N = 2 x 64 x rows <= 256
     return cfg.kv_heads == 1 && cfg.n_heads == kTcNH && cfg.head_dim == kTcD && rows >= 1 && rows <= kTcMaxRows &&
            cfg.n_req <= kTcMaxReq && cfg.q_dtype == SPIN_DTYPE_BF16 &&
            (cfg.k_dtype == SPIN_DTYPE_BF16 || cfg.k_dtype == SPIN_DTYPE_E4M3);
