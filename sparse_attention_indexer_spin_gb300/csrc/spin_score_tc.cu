@@ -53,7 +53,7 @@ constexpr int kTcM = 128;      // slots per tile (two pages)
 constexpr int kTcMaxRows = 4;  // N = 64 * rows <= 256
 constexpr int kTcMaxReq = 2048;
 constexpr int kTcEpiWarps = 8;                      // two per TMEM lane quarter
-constexpr int kTcEpiWarp0 = 3;                      // warps 0, 2: producers; 1: MMA; 3-10: epilogue
+constexpr int kTcEpiWarp0 = 4;  // warps 0, 2: producers; 1, 3: MMA issuers; 4-11: epilogue
 constexpr int kTcThreads = (kTcEpiWarp0 + kTcEpiWarps) * 32;
 constexpr int kTcMaxAcc = 4;                        // accumulator buffers in TMEM
 constexpr int kTcStagesMax = 8;  // operand ring depth (tiles in flight per CTA): 128 KB either way
@@ -182,7 +182,9 @@ struct TcHdr {
     uint64_t tfull[kTcMaxAcc];  // accumulator ready
     uint64_t tempty[kTcMaxAcc]; // accumulator drained by the epilogue
     uint64_t qfull;             // q staged by TMA (bf16 keys)
-    uint64_t qdone;             // every issued MMA finished (before q is restaged)
+    uint64_t qdone;             // both issuers' MMAs of the previous request finished (2 arrivals)
+    uint64_t qready;            // q of the next request staged (issuer 0 -> issuer 1)
+    uint64_t fin[2];            // an issuer's MMAs all finished (teardown)
     uint32_t tmem_base;
     int abort_flag;
     int total_tiles;
@@ -244,7 +246,7 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 const bool ok = n >= 0 && n <= dm.max_slots && cnt >= 0 && cnt <= dm.MB;
                 if (!ok && blockIdx.x == 0)
                     set_status(a.status, (n < 0 || n > dm.max_slots) ? SPIN_STATUS_BAD_N : SPIN_STATUS_BAD_LIST);
-                c = ok ? (int)((cnt + 1) / 2) : 0;
+                c = ok ? 2 * (int)((cnt + 3) / 4) : 0;  // tiles, padded to even: see the issuers
             }
             const int inc = warp_incl_scan(c);
             if (r < dm.R) prefix[r] = carry + inc - c;
@@ -263,7 +265,10 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 mbar_init(&hdr->tempty[s], 128);
             }
             mbar_init(&hdr->qfull, 1);
-            mbar_init(&hdr->qdone, 1);
+            mbar_init(&hdr->qdone, tc_nacc(FP8 ? 2 * kTcNH * rows : kTcNH * rows) >= 4 ? 2 : 1);
+            mbar_init(&hdr->qready, 1);
+            mbar_init(&hdr->fin[0], 1);
+            mbar_init(&hdr->fin[1], 1);
             fence_barrier_init();
         }
     } else if (wid == 1) {
@@ -278,8 +283,10 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     tc_fence_after();
     const uint32_t tmem_base = hdr->tmem_base;
     const int total = hdr->total_tiles;
-    const int t0 = (int)(((int64_t)total * blockIdx.x) / gridDim.x);
-    const int t1 = (int)(((int64_t)total * (blockIdx.x + 1)) / gridDim.x);
+    // ranges in whole tile pairs: every request contributes an even number of tiles to a
+    // range, so the even- and odd-tile pipelines see the same sequence of requests
+    const int t0 = 2 * (int)(((int64_t)(total / 2) * blockIdx.x) / gridDim.x);
+    const int t1 = 2 * (int)(((int64_t)(total / 2) * (blockIdx.x + 1)) / gridDim.x);
 
     // tile -> request, first list entry, its two blocks and their pages (-1: none / invalid)
     auto decode = [&](int t, TileInfo& ti) {
@@ -383,113 +390,107 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             for (int s = 0; s < kTcStages; ++s)
                 if (((issued >> s) & 1u) && !mbar_wait(&hdr->full[s], (phases >> s) & 1u, nullptr))
                     set_status(a.status, SPIN_STATUS_TIMEOUT);
-    } else if (wid == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (wid == 1 || wid == 3) {
+        // ------------------------------------------------------------ MMA issuers
+        // warp 1 issues the even tiles' MMAs, warp 3 the odd ones' (each issuing thread
+        // sustains only so many tcgen05.mma, so two double the rate).  Both read sQ: on a
+        // request change both commit to qdone, warp 1 waits for both, restages q and
+        // signals qready, warp 3 waits for qready.
+        // two issuers when each can own two accumulators (NACC = 4); with NACC = 2 one
+        // issuer alternates both, so its MMAs overlap the epilogue of the previous tile
+        const int nis = NACC >= 4 ? 2 : 1;
+        const int par = wid >> 1;
         const uint32_t idesc = idesc_mma(FP8 ? 0u : 1u, (uint32_t)N, (uint32_t)kTcM);
-        const int G = NACC >= 4 ? 2 : 1;  // tiles whose MMAs are interleaved
         int cur_req = -1;
-        uint32_t qphase = 0, qload_phase = 0;
+        uint32_t nchange = 0, qload_phase = 0;
         bool issued_any = false;
-        // ring positions of tile `it` (advanced incrementally: no division on this path)
-        int sa = 0, ac = 0;
+        int sa = par, ac = par;  // ring positions of tile `it` (stride nis; S and NACC are even)
         uint32_t pha = 0, phc = 0;
-        for (int t = t0, it = 0; t < t1;) {
+        for (int t = t0 + par, it = par; par < nis && t < t1; t += nis, it += nis) {
             refresh(t);
             const int req = bc(mine.req, t);
             if (req != cur_req) {
-                if (issued_any) {  // the MMAs of the previous request still read sQ
+                if (nchange > 0) {  // the previous request's MMAs must finish before sQ changes
                     if (lane == 0) tc_commit(&hdr->qdone);
                     __syncwarp();
-                    if (!mbar_wait(&hdr->qdone, qphase, &hdr->abort_flag)) { fail_wait(); break; }
-                    qphase ^= 1u;
                 }
-                if (FP8) {
-                    // B rows r*128 + h (hi) and r*128 + 64 + h (lo), 128 e4m3 each; lane
-                    // handles the query vectors n = lane, lane + 32, ...
-                    for (int n = lane; n < NQ; n += 32) {
-                        const int r = n / kTcNH, h = n % kTcNH;
-                        const __nv_bfloat16* qrow =
-                            reinterpret_cast<const __nv_bfloat16*>(a.q) + (((int64_t)req * rows + r) * kTcNH + h) * kTcD;
-                        const float inv_g = 1.0f / q_row_scale(qrow);   // exact: a power of two
-                        const uint4* src = reinterpret_cast<const uint4*>(qrow);
-                        const int nh = r * 2 * kTcNH + h, nl = nh + kTcNH;
-#pragma unroll 2
-                        for (int ch = 0; ch < kTcD / 16; ++ch) {         // 16 elements -> 16 B of e4m3
-                            const uint4 u0 = src[2 * ch], u1 = src[2 * ch + 1];
-                            const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                            uint32_t hw[4], lw[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                uint32_t hv = 0, lv = 0;
-#pragma unroll
-                                for (int pr = 0; pr < 2; ++pr) {
-                                    const uint32_t wd = wds[2 * e + pr];
-                                    const float2 x = make_float2(__uint_as_float(wd << 16) * inv_g,
-                                                                 __uint_as_float(wd & 0xffff0000u) * inv_g);
-                                    const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
-                                    const __half2 hf = *reinterpret_cast<const __half2*>(
-                                        &static_cast<const __half2_raw&>(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
-                                    const float2 hx = __half22float2(hf);
-                                    const float2 rx = make_float2(x.x - hx.x, x.y - hx.y);
-                                    const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(rx, __NV_SATFINITE, __NV_E4M3);
-                                    hv |= (uint32_t)h2 << (16 * pr);
-                                    lv |= (uint32_t)l2 << (16 * pr);
+                if (par == 0) {
+                    if (nchange > 0 && !mbar_wait(&hdr->qdone, (nchange - 1) & 1u, &hdr->abort_flag)) { fail_wait(); break; }
+                    if (FP8) {
+                        // B rows r*128 + h (hi) and r*128 + 64 + h (lo), 128 e4m3 each; lane
+                        // handles the query vectors n = lane, lane + 32, ...
+                        for (int n = lane; n < NQ; n += 32) {
+                            const int r = n / kTcNH, h = n % kTcNH;
+                            const __nv_bfloat16* qrow =
+                                reinterpret_cast<const __nv_bfloat16*>(a.q) + (((int64_t)req * rows + r) * kTcNH + h) * kTcD;
+                            const float inv_g = 1.0f / q_row_scale(qrow);   // exact: a power of two
+                            const uint4* src = reinterpret_cast<const uint4*>(qrow);
+                            const int nh = r * 2 * kTcNH + h, nl = nh + kTcNH;
+    #pragma unroll 2
+                            for (int ch = 0; ch < kTcD / 16; ++ch) {         // 16 elements -> 16 B of e4m3
+                                const uint4 u0 = src[2 * ch], u1 = src[2 * ch + 1];
+                                const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                                uint32_t hw[4], lw[4];
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    uint32_t hv = 0, lv = 0;
+    #pragma unroll
+                                    for (int pr = 0; pr < 2; ++pr) {
+                                        const uint32_t wd = wds[2 * e + pr];
+                                        const float2 x = make_float2(__uint_as_float(wd << 16) * inv_g,
+                                                                     __uint_as_float(wd & 0xffff0000u) * inv_g);
+                                        const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+                                        const __half2 hf = *reinterpret_cast<const __half2*>(
+                                            &static_cast<const __half2_raw&>(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+                                        const float2 hx = __half22float2(hf);
+                                        const float2 rx = make_float2(x.x - hx.x, x.y - hx.y);
+                                        const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(rx, __NV_SATFINITE, __NV_E4M3);
+                                        hv |= (uint32_t)h2 << (16 * pr);
+                                        lv |= (uint32_t)l2 << (16 * pr);
+                                    }
+                                    hw[e] = hv;
+                                    lw[e] = lv;
                                 }
-                                hw[e] = hv;
-                                lw[e] = lv;
+                                const uint32_t oh = (uint32_t)((nh >> 3) * 1024 + (nh & 7) * 128 + ((ch ^ (nh & 7)) << 4));
+                                const uint32_t ol = (uint32_t)((nl >> 3) * 1024 + (nl & 7) * 128 + ((ch ^ (nl & 7)) << 4));
+                                *reinterpret_cast<uint4*>(sQ + oh) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                                *reinterpret_cast<uint4*>(sQ + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                             }
-                            const uint32_t oh = (uint32_t)((nh >> 3) * 1024 + (nh & 7) * 128 + ((ch ^ (nh & 7)) << 4));
-                            const uint32_t ol = (uint32_t)((nl >> 3) * 1024 + (nl & 7) * 128 + ((ch ^ (nl & 7)) << 4));
-                            *reinterpret_cast<uint4*>(sQ + oh) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                            *reinterpret_cast<uint4*>(sQ + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                         }
+                        fence_async_smem();
+                        __syncwarp();
+                    } else {
+                        // q rows of this request by TMA, straight into the swizzled B layout
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&hdr->qfull, (uint32_t)NQ * kTcD * 2);
+                            const int y = req * rows * kTcNH;
+                            tma_load_2d(sQ, &qmap, 0, y, &hdr->qfull);
+                            tma_load_2d(sQ + qregion, &qmap, 64, y, &hdr->qfull);
+                        }
+                        __syncwarp();
+                        if (!mbar_wait(&hdr->qfull, qload_phase, &hdr->abort_flag)) { fail_wait(); break; }
+                        qload_phase ^= 1u;
                     }
-                    fence_async_smem();
-                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&hdr->qready);
                 } else {
-                    // q rows of this request by TMA, straight into the swizzled B layout
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&hdr->qfull, (uint32_t)NQ * kTcD * 2);
-                        const int y = req * rows * kTcNH;
-                        tma_load_2d(sQ, &qmap, 0, y, &hdr->qfull);
-                        tma_load_2d(sQ + qregion, &qmap, 64, y, &hdr->qfull);
-                    }
-                    __syncwarp();
-                    if (!mbar_wait(&hdr->qfull, qload_phase, &hdr->abort_flag)) { fail_wait(); break; }
-                    qload_phase ^= 1u;
+                    if (!mbar_wait(&hdr->qready, nchange & 1u, &hdr->abort_flag)) { fail_wait(); break; }
                 }
+                ++nchange;
                 cur_req = req;
             }
-            // a pair of tiles of this request when accumulators allow, else one
-            int g = 1;
-            if (G == 2 && t + 1 < t1) {
-                refresh(t + 1);
-                if (bc(mine.req, t + 1) == req) g = 2;
-            }
-            int sa1 = sa + 1, ac1 = ac + 1;
-            uint32_t pha1 = pha, phc1 = phc;
-            if (sa1 == kTcStages) { sa1 = 0; pha1 ^= 1u; }
-            if (ac1 == NACC) { ac1 = 0; phc1 ^= 1u; }
             bool ok = mbar_wait(&hdr->full[sa], pha, &hdr->abort_flag) &&
                       mbar_wait(&hdr->tempty[ac], phc ^ 1u, &hdr->abort_flag);
-            if (g == 2)
-                ok = ok && mbar_wait(&hdr->full[sa1], pha1, &hdr->abort_flag) &&
-                     mbar_wait(&hdr->tempty[ac1], phc1 ^ 1u, &hdr->abort_flag);
             if (!__all_sync(0xffffffffu, ok)) { fail_wait(); break; }
             tc_fence_after();
             if (lane == 0) {
-                // descriptors of the k-step 0 operands; a k-step of 32 bytes adds 2 to the
-                // encoded start address, a K half of a bf16 tile adds 16 KB >> 4
+                // k-step 0 descriptors; a k-step of 32 bytes adds 2 to the encoded start
+                // address, a K half of a bf16 tile adds 16 KB >> 4
                 const uint64_t a0 = smem_desc_sw128(smem_u32(sA + (size_t)sa * L.tile_bytes));
-                const uint64_t a1 = smem_desc_sw128(smem_u32(sA + (size_t)sa1 * L.tile_bytes));
                 const uint64_t b0 = smem_desc_sw128(smem_u32(sQ));
-                const uint32_t d0 = tmem_base + (uint32_t)(ac * N), d1 = tmem_base + (uint32_t)(ac1 * N);
+                const uint32_t d0 = tmem_base + (uint32_t)(ac * N);
                 if (FP8) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        tc_mma_f8(d0, a0 + 2 * kk, b0 + 2 * kk, idesc, kk ? 1u : 0u);
-                        if (g == 2) tc_mma_f8(d1, a1 + 2 * kk, b0 + 2 * kk, idesc, kk ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 4; ++kk) tc_mma_f8(d0, a0 + 2 * kk, b0 + 2 * kk, idesc, kk ? 1u : 0u);
                 } else {
                     const uint64_t bh = qregion >> 4;
 #pragma unroll
@@ -497,30 +498,23 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                         const uint64_t ao = (uint64_t)((ks >> 2) * (kTcM * 128 >> 4) + 2 * (ks & 3));
                         const uint64_t bo = (uint64_t)(ks >> 2) * bh + 2 * (ks & 3);
                         tc_mma_f16(d0, a0 + ao, b0 + bo, idesc, ks ? 1u : 0u);
-                        if (g == 2) tc_mma_f16(d1, a1 + ao, b0 + bo, idesc, ks ? 1u : 0u);
                     }
                 }
                 tc_commit(&hdr->empty[sa]);
                 tc_commit(&hdr->tfull[ac]);
-                if (g == 2) {
-                    tc_commit(&hdr->empty[sa1]);
-                    tc_commit(&hdr->tfull[ac1]);
-                }
             }
             issued_any = true;
             __syncwarp();
-            // advance by g tiles
-            if (g == 2) { sa = sa1; ac = ac1; pha = pha1; phc = phc1; }
-            if (++sa == kTcStages) { sa = 0; pha ^= 1u; }
-            if (++ac == NACC) { ac = 0; phc ^= 1u; }
-            t += g;
-            it += g;
+            sa += nis;
+            if (sa >= kTcStages) { sa -= kTcStages; pha ^= 1u; }
+            ac += nis;
+            if (ac >= NACC) { ac -= NACC; phc ^= 1u; }
         }
         // every issued MMA has finished before TMEM is released
         if (issued_any) {
-            if (lane == 0) tc_commit(&hdr->qdone);
+            if (lane == 0) tc_commit(&hdr->fin[par]);
             __syncwarp();
-            if (!mbar_wait(&hdr->qdone, qphase, nullptr)) set_status(a.status, SPIN_STATUS_TIMEOUT);
+            if (!mbar_wait(&hdr->fin[par], 0u, nullptr)) set_status(a.status, SPIN_STATUS_TIMEOUT);
         }
     } else {
         // ------------------------------------------------------------- epilogue
@@ -571,22 +565,29 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
             for (int r = 0; r < rows; ++r) {
                 float z4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                if (FP8) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {  // heads 32*half .. 32*half + 31
-                    float v[32];
-                    if (FP8) {
+                    for (int half = 0; half < 2; ++half) {  // heads 32*half .. 32*half + 31
                         // columns r*128 + h (k.hi) and r*128 + 64 + h (k.lo)
-                        float u[32];
+                        float v[32], u[32];
                         tc_ld32(trow + (uint32_t)(r * 2 * kTcNH + half * 32), v);
                         tc_ld32(trow + (uint32_t)(r * 2 * kTcNH + kTcNH + half * 32), u);
+                        const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH + half * 32);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = scale * (v[j] + u[j]);
-                    } else {
-                        tc_ld32(trow + (uint32_t)(r * kTcNH + half * 32), v);
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 wv = wr[j];
+                            z4[0] = fmaf(wv.x, fmaxf(scale * (v[4 * j + 0] + u[4 * j + 0]), 0.0f), z4[0]);
+                            z4[1] = fmaf(wv.y, fmaxf(scale * (v[4 * j + 1] + u[4 * j + 1]), 0.0f), z4[1]);
+                            z4[2] = fmaf(wv.z, fmaxf(scale * (v[4 * j + 2] + u[4 * j + 2]), 0.0f), z4[2]);
+                            z4[3] = fmaf(wv.w, fmaxf(scale * (v[4 * j + 3] + u[4 * j + 3]), 0.0f), z4[3]);
+                        }
                     }
-                    const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH + half * 32);
+                } else {
+                    float v[64];
+                    tc_ld64(trow + (uint32_t)(r * kTcNH), v);
+                    const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int j = 0; j < 16; ++j) {
                         const float4 wv = wr[j];
                         z4[0] = fmaf(wv.x, fmaxf(v[4 * j + 0], 0.0f), z4[0]);
                         z4[1] = fmaf(wv.y, fmaxf(v[4 * j + 1], 0.0f), z4[1]);
