@@ -122,9 +122,10 @@ def kernel_source_hash(names):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload, kernel_file):
-    """DRAM bytes per launch of the score kernel from the committed ncu summary, if it was
-    taken on the current source of that kernel."""
+def ncu_traffic(workload, kernel_file, alg_bytes):
+    """DRAM bytes (read + write) per launch of the score kernel: the ratio of DRAM traffic to
+    algorithmic bytes measured by ncu on a reduced case of the same workload, scaled to this
+    launch's algorithmic bytes; None unless the capture was taken on the current source."""
     path = os.path.join(ROOT, "profiles", "score_traffic.json")
     if not os.path.exists(path):
         return None
@@ -133,7 +134,8 @@ def ncu_traffic(workload, kernel_file):
     e = d.get(workload)
     if not e or e.get("source_hash") != kernel_source_hash([kernel_file, "spin_common.cuh"]):
         return None
-    return e.get("dram_bytes_per_launch")
+    r = e.get("traffic_per_alg_byte")
+    return None if r is None else float(r) * alg_bytes
 
 
 # ----------------------------------------------------------------------- CUDA workload
@@ -297,6 +299,18 @@ def time_e2e(wk, steps):
     return t0.elapsed_time(t1), h2d, d2h
 
 
+def reduce_over_ranks(ms, slots, dist, device):
+    """Whole-job figures of a replicas-only run: the slowest rank's time and the slots that
+    all ranks scored.  `dist` is torch.distributed (or None for one process)."""
+    if dist is None:
+        return float(ms), int(slots)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    n = torch.tensor([int(slots)], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 # --------------------------------------------------------------------- CPU (oracle)
 
 def oracle_sample(wl: syn.Workload, inp_host, state, n_steps, blocks_per_step, seed_step=0):
@@ -415,14 +429,10 @@ def main():
     ms, score_ms = time_steps(wk, range(W, W + K), with_score_events=True)
     clk = clocks.stop()
     barrier()
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
     slots_per_launch = wk.scored_slots(range(W, W + K))
     slots_total = sum(slots_per_launch)
-    value = slots_total * world / (ms_max / 1000.0)
+    ms_max, slots_all = reduce_over_ranks(ms, slots_total, dist, "cuda")
+    value = slots_all / (ms_max / 1000.0)
     ms_per_step = ms_max / K
 
     # dominant kernel: the indexer score
@@ -434,7 +444,7 @@ def main():
     peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (avg_score_ms / 1000.0) / 1e9
     kernel_file = "spin_score_stream.cu" if wl.kv_heads > 1 else "spin_score_tc.cu"
-    traffic = ncu_traffic(wl.name, kernel_file)
+    traffic = ncu_traffic(wl.name, kernel_file, alg_bytes)
 
     # ---------------------------------------------------------------- dense comparison
     dense = None
@@ -449,8 +459,11 @@ def main():
     # ---------------------------------------------------------------- end to end
     wk.reset()
     time_steps(wk, range(W))
+    barrier()
     ms_e2e, h2d, d2h = time_e2e(wk, range(W, W + K))
-    e2e_value = slots_total * world / (ms_e2e / 1000.0)
+    barrier()
+    ms_e2e_max, _ = reduce_over_ranks(ms_e2e, slots_total, dist, "cuda")
+    e2e_value = slots_all / (ms_e2e_max / 1000.0)
 
     # ---------------------------------------------------------------- CPU baseline
     cpu = None

@@ -9,10 +9,10 @@
  *      blocks, the top-ranked blocks and a random exploration share (Algorithm 1 lines
  *      1-5, §3.2 practical details, §3.2.1)               -> spin_select_blocks
  *   2. runs the indexer z[i] = sum_h w_h ReLU(q_h . k_{i,h}) over the slots of the
- *      selected blocks only, read through a paged block table (§2, Alg. 1 line 6)
+ *      selected blocks only, read through a paged block table (§2, Algorithm 1's scoring step)
  *                                                          -> spin_indexer_score
- *   3. takes the post-indexer top-K of the fresh scores (Alg. 1 line 7) -> spin_topk
- *   4. updates the vertical EMA V[i] and the diagonal EMA D[q-i] (Alg. 1 lines 8-10)
+ *   3. takes the post-indexer top-K of the fresh scores (Algorithm 1's top-K step) -> spin_topk
+ *   4. updates the vertical EMA V[i] and the diagonal EMA D[q-i] (Algorithm 1's EMA update)
  *                                                          -> spin_update_ema
  *   and, for speculative decoding (§3.2.2), unions the masks of several verifier rows
  *   (spin_select_blocks with rows > 1) and replays the EMA updates of the accepted
@@ -122,7 +122,7 @@ typedef struct spin_config {
 spin_status_t spin_init_state(const spin_config* cfg, float* V, float* D, float* Vmax,
                               int32_t* warm, int32_t req, spin_stream_t stream);
 
-/* Block prediction and selection (Eq. 1, Eq. 2, Algorithm 1 lines 1-5; §3.2 forced blocks;
+/* Block prediction and selection (Eq. 1, Eq. 2, Algorithm 1's prediction, budget and block top-m steps; §3.2 forced blocks;
  * §3.2.1 exploration; §3.2.2 union), for `rows` verifier rows of every request.
  *   B = ceil(N/64); m = min(B, max(ceil(K/64), ceil((10000 - rho) B / 10000)));
  *   forced F = {0, B-1}; e = min(floor(gamma m / 10000), m - |F|) (0 if m <= |F|);
@@ -167,7 +167,7 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
                                          int32_t* n_union, uint32_t* status,
                                          spin_stream_t stream);
 
-/* Indexer score (§2; Algorithm 1 line 6) of every slot of every listed block for `rows`
+/* Indexer score (§2; Algorithm 1's scoring step) of every slot of every listed block for `rows`
  * query rows: z_r[i] = sum_h w[r][h] * ReLU(s_i * (q[r][h] . k[i][h'])), h' = h for
  * per-head keys and 0 for a shared key, s_i = k_scale (E4M3) or 1.  fp32 accumulation.
  * n_pages bounds the page ids of block_table (checked on the device). */
@@ -178,14 +178,14 @@ spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const fl
                                  const int32_t* n_slots, int32_t rows, float* scores,
                                  uint32_t* status, spin_stream_t stream);
 
-/* Post-indexer top-K (Algorithm 1 line 7) of every row over the scored slots i < N of
+/* Post-indexer top-K (Algorithm 1's top-K step) of every row over the scored slots i < N of
  * the list: the K largest z, equal z ordered by the lower slot id (-0 == +0); written
  * as ascending slot ids and padded with -1 when fewer than K slots were scored. */
 spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32_t* list,
                         const int32_t* n_list, const int32_t* n_slots, int32_t rows,
                         int32_t* topk_idx, uint32_t* status, spin_stream_t stream);
 
-/* EMA update (Algorithm 1 lines 8-10) from the row-0 scores of the list:
+/* EMA update (Algorithm 1's EMA update) from the row-0 scores of the list:
  *   t = fl((1 - alpha) z[i]);  V[i] = fma(alpha, V[i], t);  D[q-i] = fma(alpha, D[q-i], t)
  * for every listed slot i < N; Vmax of the listed blocks is refreshed and the request
  * is marked warm.  `scores` has the layout of a rows == 1 spin_indexer_score call. */

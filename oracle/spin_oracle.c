@@ -17,7 +17,7 @@
  *   oracle_philox4x64_10 ...... numpy's Philox4x64-10 bit generator (library routine)
  *   oracle_decode_e4m3 ........ torch's float8_e4m3fn conversion, all 256 codes
  *   oracle_decode_bf16 ........ torch's bfloat16 conversion
- *   oracle_budget ............. hand-derived table of Algorithm 1 line 4 (golden file)
+ *   oracle_budget ............. hand-derived table of Algorithm 1's budget step (golden file)
  *   oracle_explore_count ...... hand-derived table (golden file) + invariants
  *   oracle_block_scores ....... numpy reductions in the degenerate cases D = -inf and
  *                               V = -inf, and brute force on tiny inputs
@@ -124,7 +124,7 @@ static int64_t elem_size(int32_t dtype) {
 }
 
 /* ------------------------------------------------------------------------------
- * Budget (Algorithm 1 line 4): m = min{B, max(ceil(K/b), ceil((1-rho) B))}, rho in
+ * Budget (Algorithm 1's budget step): m = min{B, max(ceil(K/b), ceil((1-rho) B))}, rho in
  * integer basis points so that the ceiling is exact.
  * ---------------------------------------------------------------------------- */
 int64_t oracle_budget(int64_t n_blocks, int64_t top_k, int64_t block, int32_t rho_bp) {
@@ -144,7 +144,7 @@ int64_t oracle_explore_count(int64_t m, int64_t n_forced, int32_t gamma_bp) {
 }
 
 /* ------------------------------------------------------------------------------
- * Eq. 1 and Eq. 2 (Algorithm 1 line 3): predicted slot score max(V[i], D[q-i])
+ * Eq. 1 and Eq. 2 (Algorithm 1's pooling step): predicted slot score max(V[i], D[q-i])
  * (or V[i] + D[q-i] in the additive mode), max-pooled over the slots i < N of each
  * block of b slots.
  * ---------------------------------------------------------------------------- */
@@ -213,7 +213,7 @@ static int request_ok(const oracle_cfg* cfg, int64_t n, int64_t q, int32_t rows)
     return 1;
 }
 
-/* One query row of one request: Algorithm 1 lines 1-5, the forced sink and newest
+/* One query row of one request: Algorithm 1's prediction, budget and block top-m steps, the forced sink and newest
  * blocks and the warm-up rule of §3.2, and random exploration of §3.2.1.  Writes a
  * 0/1 mask of B entries; returns the number of selected blocks. */
 static int64_t select_row(const oracle_cfg* cfg, const float* V_req, const float* D_req,
@@ -221,16 +221,16 @@ static int64_t select_row(const oracle_cfg* cfg, const float* V_req, const float
                           uint64_t step, int32_t layer, int32_t row, int32_t req,
                           unsigned char* mask) {
     int64_t b = cfg->block;
-    int64_t nb = (n_slots + b - 1) / b;                      /* line 1 */
+    int64_t nb = (n_slots + b - 1) / b;                      /* block count */
     memset(mask, 0, (size_t)(nb > 0 ? nb : 1));
     if (nb == 0) return 0;
     if (!warm) {                                             /* first step after a reset */
         memset(mask, 1, (size_t)nb);
         return nb;
     }
-    float* S = (float*)malloc(sizeof(float) * (size_t)nb);  /* lines 2-3 */
+    float* S = (float*)malloc(sizeof(float) * (size_t)nb);  /* predict and pool */
     oracle_block_scores(cfg, V_req, D_req, n_slots, q, S);
-    int64_t m = oracle_budget(nb, cfg->top_k, b, rho_bp);    /* line 4 */
+    int64_t m = oracle_budget(nb, cfg->top_k, b, rho_bp);    /* budget */
 
     mask[0] = 1;                                             /* sink block */
     mask[nb - 1] = 1;                                        /* newest active block */
@@ -238,7 +238,7 @@ static int64_t select_row(const oracle_cfg* cfg, const float* V_req, const float
     int64_t e = oracle_explore_count(m, f, cfg->gamma_bp);
     int64_t t = m > f ? m - f - e : 0;                       /* top-ranked share */
 
-    /* line 5 on the blocks that are not forced */
+    /* block top-m over the blocks that are not forced */
     score_idx* cand = (score_idx*)malloc(sizeof(score_idx) * (size_t)nb);
     int64_t nc = 0;
     for (int64_t j = 0; j < nb; ++j)
@@ -391,7 +391,7 @@ int oracle_indexer_score(const oracle_cfg* cfg, const void* q, const float* w,
 }
 
 /* ------------------------------------------------------------------------------
- * Post-indexer top-K (Algorithm 1 line 7) over the slots that were scored: the K
+ * Post-indexer top-K (Algorithm 1's top-K step) over the slots that were scored: the K
  * largest scores, equal scores ordered by the lower slot id; returned in ascending
  * slot order, padded with -1 when fewer than K slots were scored.
  * ---------------------------------------------------------------------------- */
@@ -433,7 +433,7 @@ int oracle_topk(const oracle_cfg* cfg, const float* scores, const int32_t* list,
 }
 
 /* ------------------------------------------------------------------------------
- * EMA update, Algorithm 1 lines 8-10: for every scored slot i,
+ * EMA update, Algorithm 1's EMA update: for every scored slot i,
  *   V[i] <- alpha V[i] + (1-alpha) z[i],   D[q-i] <- alpha D[q-i] + (1-alpha) z[i].
  * §3.2.2: with a accepted drafts the observations of rows 0..a are replayed in order
  * (row r at query position q + r); rows above a are discarded.

@@ -61,17 +61,17 @@ uint32_t oracle_explore_key(uint64_t seed, int32_t layer, uint64_t step, int32_t
 double oracle_decode_e4m3(uint8_t code);
 double oracle_decode_bf16(uint16_t bits);
 
-/* Algorithm 1 line 4, rho in basis points. */
+/* Algorithm 1's budget step, rho in basis points. */
 int64_t oracle_budget(int64_t n_blocks, int64_t top_k, int64_t block, int32_t rho_bp);
 /* Exploration share of §3.2.1: floor(gamma*m), capped by the capacity m - f left
  * after the forced blocks; 0 when m <= f. */
 int64_t oracle_explore_count(int64_t m, int64_t n_forced, int32_t gamma_bp);
 
-/* Eq. 2 (Algorithm 1 line 3) for one query row at position q: S[j], j < ceil(N/b). */
+/* Eq. 2 (Algorithm 1's pooling step) for one query row at position q: S[j], j < ceil(N/b). */
 void oracle_block_scores(const oracle_cfg* cfg, const float* V_req, const float* D_req,
                          int64_t n_slots, int64_t q, float* S_out);
 
-/* Block selection for every request and row (Algorithm 1 lines 1-5 plus forced
+/* Block selection for every request and row (Algorithm 1's prediction, budget and block top-m steps plus forced
  * blocks, exploration and the multi-row union).  rho_bp < 0 uses cfg->rho_bp.
  * union_blocks / n_union may be NULL. Returns 0, or -1 on invalid input. */
 int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
@@ -80,7 +80,7 @@ int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
                          int32_t* blocks, int32_t* n_blocks,
                          int32_t* union_blocks, int32_t* n_union);
 
-/* Indexer score (Algorithm 1 line 6) of every slot i < N of every listed block, for
+/* Indexer score (Algorithm 1's scoring step) of every slot i < N of every listed block, for
  * `rows` query rows.  q: [R][rows][n_heads][d] in q_dtype; w: [R][rows][n_heads];
  * k_pool: [pages][64][kv_heads][d] in k_dtype; k_scale: [pages][64] (E4M3 only, else
  * NULL); block_table: [R][bt_stride].  Slots i >= N get score 0.  mags (nullable,
@@ -97,12 +97,12 @@ void oracle_score_slot(const oracle_cfg* cfg, const void* q_req, const float* w_
                        const void* key, float scale, int32_t rows, float* z_out,
                        double* mag_out);
 
-/* Post-indexer top-K (Algorithm 1 line 7) per request and row over the scored slots. */
+/* Post-indexer top-K (Algorithm 1's top-K step) per request and row over the scored slots. */
 int oracle_topk(const oracle_cfg* cfg, const float* scores, const int32_t* list,
                 const int32_t* n_list, const int32_t* n_slots, int32_t rows,
                 int32_t* topk_idx);
 
-/* EMA update (Algorithm 1 lines 8-10) replayed for rows 0..a in order (§3.2.2);
+/* EMA update (Algorithm 1's EMA update) replayed for rows 0..a in order (§3.2.2);
  * accepted == NULL means a = 0 for every request (the single-row update). */
 int oracle_replay_ema(const oracle_cfg* cfg, float* V, float* D, int32_t* warm,
                       const float* scores, int32_t rows, const int32_t* list,

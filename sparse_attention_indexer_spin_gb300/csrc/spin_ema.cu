@@ -1,7 +1,7 @@
 // spin_ema.cu -- EMA update and the deferred MTP replay.
 //
 // "SPIN: Shadow Predictive Indexer for Sparse Attention":
-//   Algorithm 1 lines 8-10: for every scored slot i,
+//   Algorithm 1's EMA update: for every scored slot i,
 //       V[i]   <- alpha V[i]   + (1 - alpha) z[i]
 //       D[q-i] <- alpha D[q-i] + (1 - alpha) z[i]
 //   §3.2.2: with a drafts accepted, the observations of verifier rows 0..a are replayed in

@@ -1,6 +1,6 @@
 // spin_score_generic.cu -- indexer score for any shape (a slow cross-check kernel).
 //
-// "SPIN: Shadow Predictive Indexer for Sparse Attention", §2 and Algorithm 1 line 6:
+// "SPIN: Shadow Predictive Indexer for Sparse Attention", §2 and Algorithm 1's scoring step:
 // z_t[i] = sum_h w_h ReLU(q_{t,h} . k_{i,h}) over the slots of the selected blocks; the
 // per-slot FP8 scale multiplies the dot product before the ReLU.
 //

@@ -1,6 +1,6 @@
 // spin_score_stream.cu -- indexer score with a key per head, on CUDA cores.
 //
-// "SPIN: Shadow Predictive Indexer for Sparse Attention", §2 and Algorithm 1 line 6:
+// "SPIN: Shadow Predictive Indexer for Sparse Attention", §2 and Algorithm 1's scoring step:
 // z_t[i] = sum_h w_h ReLU(q_{t,h} . k_{i,h}), run only over the slots of the selected
 // blocks, read through the paged block table.
 //

@@ -1,7 +1,7 @@
 // spin_score_tc.cu -- indexer score with one key shared by all heads, on tcgen05 tensor
 // cores (sm_103a).
 //
-// "SPIN: Shadow Predictive Indexer for Sparse Attention", §2 and Algorithm 1 line 6:
+// "SPIN: Shadow Predictive Indexer for Sparse Attention", §2 and Algorithm 1's scoring step:
 // z_t[i] = sum_h w_h ReLU(q_{t,h} . k_i) over the slots of the selected blocks only.
 // With one key per slot shared by the n_h heads (and, for speculative decoding, by the
 // rows' queries), the per-tile work is a dense contraction
@@ -22,13 +22,16 @@
 // the instruction count per tile low and interleaves two tiles (two accumulator chains)
 // when TMEM holds four accumulators.
 //
-// Warp roles of a persistent CTA (tiles = pairs of selected blocks of one request):
-//   warps 0, 2  producers (even and odd tiles): one (FP8) or two (bf16) 2D TMA loads per
-//               page into a ring
-//   warp 1      TMEM owner and MMA issuer (one thread): 4 (FP8) or 8 (bf16) tcgen05.mma
-//               per tile, two tiles interleaved when possible; stages q when the request
-//               changes
-//   warps 3-10  epilogue, two warps per TMEM lane quarter taking alternate tiles:
+// Warp roles of a persistent CTA (tiles = pairs of selected blocks of one request; a CTA
+// owns a contiguous range of whole tile pairs):
+//   warps 0, 2  producers of the even and odd tiles: one (FP8) or two (bf16) 2D TMA loads
+//               per page into a shared-memory ring
+//   warps 1, 3  MMA issuers (one elected thread each): 4 (FP8) or 8 (bf16) tcgen05.mma
+//               per tile.  With four accumulators in TMEM (N <= 128) warp 1 takes the even
+//               tiles and warp 3 the odd ones, two independent chains; with two, warp 1
+//               issues every tile.  Warp 1 owns the TMEM allocation; q is staged whenever
+//               the request changes.
+//   warps 4-11  epilogue, two warps per TMEM lane quarter taking alternate tiles:
 //               tcgen05.ld of a tile's accumulators (one slot per thread),
 //               z = sum_h w_h g_h max(s_i acc_h, 0) per row, masked to i < N, stored
 // Accumulators are 2-4 deep in TMEM (N <= 128: 4); the epilogue fetches the per-slot FP8

@@ -1,7 +1,7 @@
 // spin_select.cu -- block prediction and budgeted block selection.
 //
 // "SPIN: Shadow Predictive Indexer for Sparse Attention": Eq. 1 (predicted slot score
-// max(V[i], D[q-i])), Eq. 2 (max-pooling over the block's slots), Algorithm 1 lines 1-5
+// max(V[i], D[q-i])), Eq. 2 (max-pooling over the block's slots), Algorithm 1's prediction, budget and block top-m steps
 // (budget m_t, TopK over block scores), §3.2 practical details (warm-up step is dense;
 // sink and newest blocks always kept), §3.2.1 (a share gamma of m_t explores blocks
 // drawn at random from those not selected), §3.2.2 (masks of several verifier rows are

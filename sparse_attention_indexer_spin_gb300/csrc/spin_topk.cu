@@ -1,6 +1,6 @@
 // spin_topk.cu -- post-indexer top-K over the freshly scored slots.
 //
-// "SPIN: Shadow Predictive Indexer for Sparse Attention", Algorithm 1 line 7:
+// "SPIN: Shadow Predictive Indexer for Sparse Attention", Algorithm 1's top-K step:
 // T_t = TopK(z_t, K) over the slots the indexer scored (the selected blocks), which then
 // feeds core attention.  Equal scores at the K-th value go to the lower slot id.
 //
