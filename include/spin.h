@@ -148,10 +148,11 @@ spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const f
  * other allocations, plugin hosts that give the library no allocator, and latency-critical
  * loops that must not pay for an allocation.  This entry point takes the same arguments
  * minus the workspace and uses instead a scratch array that lives in the library itself
- * (a static device array of 4 MiB, held on every GPU that loads the library until the
+ * (a static device array of 8 MiB, held on every GPU that loads the library until the
  * process exits).  It calls no cudaMalloc/cudaFree and no allocating library routine.
- *   - Capacity: n_req * rows * ceil(max_slots/64) <= 1048576 (one float per block and
- *     row); larger configurations are rejected with SPIN_ERR_CAPACITY.
+ *   - Capacity: n_req * rows * ceil(max_slots/64) <= 1048576 (a block score and an
+ *     exploration draw per block and row); larger configurations are rejected with
+ *     SPIN_ERR_CAPACITY.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
  *   - Every call shares the one array, which keeps the last call's contents: calls that

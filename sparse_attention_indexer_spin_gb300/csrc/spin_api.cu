@@ -137,8 +137,8 @@ spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const f
 // ---------------------------------------------------------------------------------------
 namespace spin {
 
-constexpr size_t kNoAllocScratchFloats = (size_t)1 << 20;  // 4 MiB
-static __device__ __align__(256) float g_select_scratch[kNoAllocScratchFloats];
+constexpr size_t kNoAllocScratchEntries = (size_t)1 << 20;  // block-row entries of each of its two arrays
+static __device__ __align__(256) float g_select_scratch[2 * kNoAllocScratchEntries];  // 8 MiB
 
 constexpr int kMaxDevices = 128;
 static std::mutex g_scratch_mu;
@@ -179,11 +179,11 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
         return fail(SPIN_ERR_CAPACITY, "max_slots %d needs %d blocks; selection supports %d", cfg->max_slots, dm.MB,
                     kSelectMaxBlocks);
     const size_t need = (size_t)dm.R * (size_t)rows * (size_t)dm.MB;
-    if (need > kNoAllocScratchFloats)
+    if (need > kNoAllocScratchEntries || select_workspace_bytes(*cfg, rows) > sizeof(g_select_scratch))
         return fail(SPIN_ERR_CAPACITY,
                     "spin_select_blocks_noalloc: n_req * rows * max_blocks = %zu exceeds its built-in scratch of %zu "
                     "entries; use spin_select_blocks with a workspace",
-                    need, kNoAllocScratchFloats);
+                    need, kNoAllocScratchEntries);
     if (!V || !D || !Vmax || !warm || !n_slots || !q_pos || !blocks || !n_blocks)
         return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
     if (rows > 1 && (!union_blocks || !n_union))

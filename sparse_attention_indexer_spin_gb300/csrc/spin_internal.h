@@ -24,7 +24,7 @@ struct SelectArgs {
     int32_t* n_blocks;
     int32_t* union_blocks;
     int32_t* n_union;
-    float* block_scores;  // workspace [R][rows][MB]
+    float* block_scores;  // workspace: S [R][rows][MB] fp32, then exploration draws [R][rows][MB] u32
     uint32_t* status;
 };
 
@@ -70,6 +70,10 @@ cudaError_t launch_score_stream(const spin_config& cfg, const ScoreArgs& a, cuda
 bool score_stream_supported(const spin_config& cfg, int rows);
 cudaError_t launch_score_tc(const spin_config& cfg, const ScoreArgs& a, cudaStream_t s);
 bool score_tc_supported(const spin_config& cfg, int rows);
+bool topk_sample_fits(const spin_config& cfg);
+cudaError_t launch_topk_sample(const spin_config& cfg, const float* scores, const int32_t* list,
+                               const int32_t* n_list, const int32_t* n_slots, int rows, int32_t* topk_idx,
+                               uint32_t* status, cudaStream_t s);
 cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32_t* list,
                         const int32_t* n_list, const int32_t* n_slots, int rows,
                         int32_t* topk_idx, uint32_t* status, cudaStream_t s);

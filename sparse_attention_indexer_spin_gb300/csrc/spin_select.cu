@@ -18,6 +18,9 @@
 #include "spin_common.cuh"
 #include "spin_internal.h"
 
+#include <cooperative_groups.h>
+namespace cg = cooperative_groups;
+
 namespace spin {
 
 // ---------------------------------------------------------------------------------------
@@ -33,7 +36,8 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
                                                           const int32_t* __restrict__ warm,
                                                           const int32_t* __restrict__ n_slots,
                                                           const int32_t* __restrict__ q_pos, int rows,
-                                                          float* __restrict__ S) {
+                                                          uint64_t seed, uint64_t step, int layer,
+                                                          float* __restrict__ S, uint32_t* __restrict__ X) {
     const Dims dm = dims_of(cfg);
     const int rr = blockIdx.y;
     const int req = rr / rows, r = rr - req * rows;
@@ -46,6 +50,7 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
     const float* Vq = V + (int64_t)req * dm.max_slots;
     const float* Vm = Vmax + (int64_t)req * dm.MB;
     float* Sq = S + (int64_t)rr * dm.MB;
+    uint32_t* Xq = X + (int64_t)rr * dm.MB;
     const bool sum = cfg.combine == SPIN_COMBINE_SUM;
     // each warp owns kBsBlocksPerWarp consecutive blocks and issues all their loads first
     for (int64_t j0 = ((int64_t)blockIdx.x * nw + wid) * kBsBlocksPerWarp; j0 < nb;
@@ -67,6 +72,10 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
             const float vmb = __shfl_sync(0xffffffffu, vm, b);
             if (lane == 0 && j0 + b < nb) Sq[j0 + b] = sum ? m : fmaxf(vmb, m);
         }
+        // the exploration draw of each block (used only if the block ends up unselected):
+        // computed here, where every block has a thread, off the selection's serial path
+        if (lane < kBsBlocksPerWarp && j0 + lane < nb)
+            Xq[j0 + lane] = explore_key(seed, layer, step, r, req, (int)(j0 + lane));
     }
 }
 
@@ -258,11 +267,284 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
     }
 }
 
-size_t select_workspace_bytes(const spin_config& cfg, int rows) {
+// ---------------------------------------------------------------------------------------
+// Register-resident selection (MB <= 512 * 16, rows <= 8): one 512-thread CTA per
+// (request, row), rows of a request in one thread-block cluster.  Thread t keeps the keys
+// of blocks j = t + 512 i (i < KPT) in registers, so the ascending-j order of equal keys is
+// the (i, t) order.  A radix select needs one CTA barrier per 8-bit digit: every warp
+// finds the digit itself from the shared histogram, and the three histogram buffers rotate
+// so that the buffer a pass fills was cleared two passes earlier.  The union of the rows
+// is taken by the cluster's first CTA from the others' selection bitmaps in distributed
+// shared memory.
+// ---------------------------------------------------------------------------------------
+constexpr int kSrThreads = 512;
+constexpr int kSrWarps = kSrThreads / 32;
+constexpr int kSrMaxKpt = 16;
+constexpr int kSrMaxBlocks = kSrThreads * kSrMaxKpt;
+
+struct SrShared {
+    __align__(16) int hist[3][256];
+    int cnt[kSrMaxKpt * kSrWarps];       // per (i, warp) counts, (i, warp) order
+    int base[kSrMaxKpt * kSrWarps + 1];  // their exclusive scan (+ total)
+    uint32_t bitmap[kSrMaxBlocks / 32];  // selected blocks of this row, bit j % 32 of word j / 32
+};
+
+// Adds the warp's bins (-1: none) to a shared histogram: the lanes that share the first
+// active lane's bin with one atomic, the others one atomic each (keys of one warp mostly
+// share a bin when they are concentrated, and mostly differ when they are spread).
+__device__ __forceinline__ void sr_hist_add(int* h, int bin) {
+    const int lane = threadIdx.x & 31;
+    const unsigned act = __ballot_sync(0xffffffffu, bin >= 0);
+    if (act == 0u) return;
+    const int lead = __ffs(act) - 1;
+    const int b0 = __shfl_sync(0xffffffffu, bin, lead);
+    const unsigned m0 = __ballot_sync(0xffffffffu, bin == b0);
+    if (lane == lead) atomicAdd(&h[b0], __popc(m0));
+    else if (bin >= 0 && bin != b0) atomicAdd(&h[bin], 1);
+}
+
+// Exclusive scan of sh.cnt[0 .. n) in place into sh.base (warp 0), total in sh.base[n].
+// Callers bracket it with barriers.
+__device__ __forceinline__ void sr_scan_counts(SrShared& sh, int n) {
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int v = c0 + lane < n ? sh.cnt[c0 + lane] : 0;
+        const int inc = warp_incl_scan(v);
+        if (c0 + lane < n) sh.base[c0 + lane] = carry + inc - v;
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) sh.base[n] = carry;
+}
+
+// Marks in `sel` the k eligible entries with the largest keys, equal keys in ascending j.
+// Requires 0 < k < (number of eligible entries).  `pass` counts histogram passes across
+// calls (buffer rotation); on entry buffers pass % 3 and (pass + 1) % 3 are zero.
+template <int KPT>
+__device__ void sr_top(const uint32_t (&key)[KPT], uint32_t elig, uint32_t& sel, int k, int& pass, SrShared& sh) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    uint32_t prefix = 0, mask = 0;
+    int kk = k, n_eq = 0;
+    for (int d = 0; d < 4; ++d, ++pass) {
+        const int shift = 24 - 8 * d;
+        int* h = sh.hist[pass % 3];
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) {
+            const bool in = ((elig >> i) & 1u) && (key[i] & mask) == prefix;
+            sr_hist_add(h, in ? (int)((key[i] >> shift) & 255u) : -1);
+        }
+        __syncthreads();
+        // every warp: lane l holds bins 255-8l .. 248-8l (descending key order), read as two
+        // 16-byte vectors (a warp reads the 1 KB histogram without bank conflicts)
+        const int4 v_hi = reinterpret_cast<const int4*>(h)[63 - 2 * lane];
+        const int4 v_lo = reinterpret_cast<const int4*>(h)[62 - 2 * lane];
+        const int cnt[8] = {v_hi.w, v_hi.z, v_hi.y, v_hi.x, v_lo.w, v_lo.z, v_lo.y, v_lo.x};
+        int sum = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) sum += cnt[b];
+        const int inc = warp_incl_scan(sum);
+        const unsigned ball = __ballot_sync(0xffffffffu, inc >= kk);
+        const int src = __ffs(ball) - 1;
+        int above = inc - sum, digit = 0, nbin = 0;
+#pragma unroll
+        for (int b = 0, found = 0; b < 8; ++b) {
+            if (!found) {
+                if (above + cnt[b] >= kk) { digit = 255 - 8 * lane - b; nbin = cnt[b]; found = 1; }
+                else above += cnt[b];
+            }
+        }
+        digit = __shfl_sync(0xffffffffu, digit, src);
+        above = __shfl_sync(0xffffffffu, above, src);
+        nbin = __shfl_sync(0xffffffffu, nbin, src);
+        // the buffer filled two passes from now was last read before this pass's barrier
+        if (tid < 256) sh.hist[(pass + 2) % 3][tid] = 0;
+        prefix |= (uint32_t)digit << shift;
+        mask |= 0xFFu << shift;
+        kk -= above;
+        n_eq = nbin;
+    }
+    // keys above the threshold, then the first kk of the keys equal to it
+    uint32_t eq = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        if (!((elig >> i) & 1u)) continue;
+        if (key[i] > prefix) sel |= 1u << i;
+        else if (key[i] == prefix) eq |= 1u << i;
+    }
+    if (kk == n_eq) {
+        sel |= eq;
+        return;
+    }
+    // tie ranks in (i, t) order
+    unsigned ball[KPT];
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        ball[i] = __ballot_sync(0xffffffffu, (eq >> i) & 1u);
+        if (lane == 0) sh.cnt[i * kSrWarps + wid] = __popc(ball[i]);
+    }
+    __syncthreads();
+    sr_scan_counts(sh, KPT * kSrWarps);
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        if (((eq >> i) & 1u) && sh.base[i * kSrWarps + wid] + __popc(ball[i] & lt) < kk) sel |= 1u << i;
+    __syncthreads();  // sh.cnt / sh.base are reused
+}
+
+// Writes the ascending list of selected j (and the bitmap); returns the count.
+template <int KPT>
+__device__ int sr_compact(uint32_t sel, int32_t* out, SrShared& sh) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    unsigned ball[KPT];
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        ball[i] = __ballot_sync(0xffffffffu, (sel >> i) & 1u);
+        if (lane == 0) {
+            sh.cnt[i * kSrWarps + wid] = __popc(ball[i]);
+            sh.bitmap[i * kSrWarps + wid] = ball[i];
+        }
+    }
+    __syncthreads();
+    sr_scan_counts(sh, KPT * kSrWarps);
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        if ((sel >> i) & 1u) out[sh.base[i * kSrWarps + wid] + __popc(ball[i] & lt)] = i * kSrThreads + tid;
+    return sh.base[KPT * kSrWarps];
+}
+
+template <int KPT>
+__global__ void __launch_bounds__(kSrThreads, 1) select_reg_kernel(
+    spin_config cfg, const int32_t* __restrict__ warm, const int32_t* __restrict__ n_slots,
+    const int32_t* __restrict__ q_pos, int rows, const int32_t* __restrict__ rho_override, uint64_t step,
+    int layer, const float* __restrict__ S, const uint32_t* __restrict__ X, int32_t* __restrict__ blocks,
+    int32_t* __restrict__ n_blocks, int32_t* __restrict__ union_blocks, int32_t* __restrict__ n_union,
+    uint32_t* status) {
+    __shared__ SrShared sh;
     const Dims dm = dims_of(cfg);
-    size_t b = sizeof(float) * (size_t)dm.R * (size_t)rows * (size_t)dm.MB;
+    const int MB = dm.MB;
+    const int tid = threadIdx.x;
+    const int req = blockIdx.x / rows, r = blockIdx.x % rows;  // a cluster = the rows of a request
+    const int64_t rr = (int64_t)req * rows + r;
+    // the row's block scores and exploration draws are loaded up front, together with the
+    // request's sizes (entries at j >= N/64 are not used)
+    float sv[KPT];
+    uint32_t xv[KPT];
+#pragma unroll
+    for (int i = 0; i < KPT; ++i) {
+        const int j = i * kSrThreads + tid;
+        sv[i] = j < MB ? __ldg(S + rr * MB + j) : 0.0f;
+        xv[i] = j < MB ? __ldg(X + rr * MB + j) : 0u;
+    }
+    const int64_t n = n_slots[req], q = q_pos[req];
+    uint32_t bad = request_check(n, q, rows, dm);
+    int32_t rho = cfg.rho_bp;
+    if (rho_override) {
+        rho = *rho_override;
+        if (rho < 0 || rho > 10000) bad |= SPIN_STATUS_BAD_RHO;
+    }
+    // (bad is uniform over the cluster: it depends on the request only)
+    if (bad) {
+        if (tid == 0) {
+            if (r == 0) set_status(status, bad);
+            n_blocks[rr] = 0;
+            if (r == 0 && union_blocks && n_union) n_union[req] = 0;
+        }
+        return;
+    }
+    const int nb = (int)((n + kBlock - 1) / kBlock);
+    for (int b = tid; b < 3 * 256; b += kSrThreads) (&sh.hist[0][0])[b] = 0;
+    uint32_t valid = 0, sel = 0;
+#pragma unroll
+    for (int i = 0; i < KPT; ++i)
+        if (i * kSrThreads + tid < nb) valid |= 1u << i;
+    if (warm[req] == 0 || nb <= 2) {
+        sel = valid;  // dense warm-up step (and contexts whose every block is forced)
+        __syncthreads();
+    } else {
+        const int64_t m = budget_blocks(nb, cfg.top_k, rho);
+        const int64_t f = 2;
+        int64_t e = 0, t = 0;
+        if (m > f) {
+            e = ((int64_t)cfg.gamma_bp * m) / 10000;
+            if (e > m - f) e = m - f;
+            t = m - f - e;
+        }
+        uint32_t key[KPT];
+        uint32_t elig = 0;
+#pragma unroll
+        for (int i = 0; i < KPT; ++i) {
+            const int j = i * kSrThreads + tid;
+            key[i] = 0;
+            if (j < nb) {
+                if (j == 0 || j == nb - 1) sel |= 1u << i;
+                else { key[i] = order_key(sv[i]); elig |= 1u << i; }
+            }
+        }
+        __syncthreads();  // histogram buffers cleared
+        int pass = 0;
+        const int64_t n_rest = (int64_t)nb - f;
+        if (t >= n_rest) sel |= elig;
+        else if (t > 0) sr_top<KPT>(key, elig, sel, (int)t, pass, sh);
+        if (e > 0) {
+            const int64_t n_left = n_rest - t;
+            uint32_t elig2 = 0;
+#pragma unroll
+            for (int i = 0; i < KPT; ++i) {
+                if (((elig >> i) & 1u) && !((sel >> i) & 1u)) {
+                    elig2 |= 1u << i;
+                    // smallest Philox key first == largest complement
+                    key[i] = ~xv[i];
+                }
+            }
+            if (e >= n_left) sel |= elig2;
+            else sr_top<KPT>(key, elig2, sel, (int)e, pass, sh);
+        }
+    }
+    const int cnt = sr_compact<KPT>(sel, blocks + rr * MB, sh);
+    if (tid == 0) n_blocks[rr] = cnt;
+    if (rows > 1 && union_blocks && n_union) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();  // every row's bitmap is complete
+        if (cluster.block_rank() == 0) {
+            const int nwords = (nb + 31) / 32;
+            uint32_t u = 0;
+            if (tid < nwords)
+                for (int p = 0; p < rows; ++p) u |= cluster.map_shared_rank(sh.bitmap, p)[tid];
+            // the bitmap words beyond nb's are zero: rows select only j < nb
+            int total;
+            const int pos0 = block_excl_scan(tid < nwords ? __popc(u) : 0, sh.base, &total);
+            int pos = pos0;
+            while (u) {
+                const int b = __ffs(u) - 1;
+                u &= u - 1u;
+                union_blocks[(int64_t)req * MB + pos++] = tid * 32 + b;
+            }
+            if (tid == 0) n_union[req] = total;
+        }
+        cluster.sync();  // the first CTA has finished reading the others' shared memory
+    } else if (union_blocks && n_union) {
+        // one row: the union is the row's list
+        int32_t* out = union_blocks + (int64_t)req * MB;
+        const int32_t* in = blocks + rr * MB;
+        __syncthreads();
+        for (int c = tid; c < cnt; c += kSrThreads) out[c] = in[c];
+        if (tid == 0) n_union[req] = cnt;
+    }
+}
+
+// Workspace: block scores S [R][rows][MB] (fp32), then exploration draws X [R][rows][MB]
+// (u32), each 256-byte aligned.
+static size_t select_array_bytes(const spin_config& cfg, int rows) {
+    const Dims dm = dims_of(cfg);
+    const size_t b = sizeof(float) * (size_t)dm.R * (size_t)rows * (size_t)dm.MB;
     return (b + 255) & ~(size_t)255;
 }
+
+size_t select_workspace_bytes(const spin_config& cfg, int rows) { return 2 * select_array_bytes(cfg, rows); }
 
 cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
@@ -270,10 +552,36 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
     int gx = (dm.MB + per_cta - 1) / per_cta;
     if (gx > 512) gx = 512;
     dim3 g1(gx, dm.R * a.rows);
-    block_score_kernel<<<g1, 256, 0, s>>>(cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,
-                                          a.block_scores);
+    float* S = a.block_scores;
+    uint32_t* X = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.block_scores) +
+                                              select_array_bytes(cfg, a.rows));
+    block_score_kernel<<<g1, 256, 0, s>>>(cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows, cfg.seed,
+                                          a.step, a.layer, S, X);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (dm.MB <= kSrMaxBlocks && a.rows >= 1 && a.rows <= 8) {
+        const int kpt = dm.MB <= kSrThreads ? 1 : dm.MB <= 2 * kSrThreads ? 2 : dm.MB <= 4 * kSrThreads ? 4
+                        : dm.MB <= 8 * kSrThreads ? 8 : 16;
+        void (*kern)(spin_config, const int32_t*, const int32_t*, const int32_t*, int, const int32_t*, uint64_t,
+                     int, const float*, const uint32_t*, int32_t*, int32_t*, int32_t*, int32_t*, uint32_t*) =
+            kpt == 1 ? select_reg_kernel<1> : kpt == 2 ? select_reg_kernel<2> : kpt == 4 ? select_reg_kernel<4>
+            : kpt == 8 ? select_reg_kernel<8> : select_reg_kernel<16>;
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3((unsigned)(dm.R * a.rows));
+        lc.blockDim = dim3(kSrThreads);
+        lc.dynamicSmemBytes = 0;
+        lc.stream = s;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = (unsigned)a.rows;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+        return cudaLaunchKernelEx(&lc, kern, cfg, a.warm, a.n_slots, a.q_pos, a.rows, a.rho_override, a.step,
+                                  a.layer, (const float*)S, (const uint32_t*)X, a.blocks, a.n_blocks,
+                                  a.union_blocks, a.n_union, a.status);
+    }
     const size_t smem = ((size_t)dm.MB * 6 + 15) & ~(size_t)15;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

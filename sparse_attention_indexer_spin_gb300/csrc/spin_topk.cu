@@ -8,8 +8,10 @@
 // ascending slot order because block lists are ascending.  A three-pass radix select
 // (11 + 11 + 10 bits of the order-preserving 32-bit key) finds the K-th key T and how many
 // keys equal to T to keep; one ordered pass then writes the kept slot ids in ascending
-// order and pads with -1.  The cluster kernel below is the one used; the single-CTA
-// kernel serves candidate sets too large to stage in the cluster's shared memory.
+// order and pads with -1.  Launches with at least 32 request rows use the sampled-bracket
+// kernel of spin_topk_sample.cu (one CTA per row) when its shared memory fits; fewer rows
+// use the 8-CTA cluster kernel below, and the row and single-CTA kernels serve lists too
+// long for either.
 #include <cooperative_groups.h>
 
 #include "spin_common.cuh"
@@ -634,6 +636,9 @@ static size_t topk_cluster_smem(const spin_config& cfg) {
 cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32_t* list,
                         const int32_t* n_list, const int32_t* n_slots, int rows, int32_t* topk_idx,
                         uint32_t* status, cudaStream_t s) {
+    // enough rows to fill the GPU with one CTA each: the sampled-bracket kernel
+    if ((int64_t)cfg.n_req * rows >= 32 && topk_sample_fits(cfg))
+        return launch_topk_sample(cfg, scores, list, n_list, n_slots, rows, topk_idx, status, s);
     const Dims dm = dims_of(cfg);
     const size_t row_smem = sizeof(TrShared) + (size_t)dm.MB * 4;
     if ((int64_t)cfg.n_req * rows >= 32 && row_smem <= 200 * 1024) {

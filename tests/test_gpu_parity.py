@@ -66,11 +66,14 @@ def test_ragged_requests_tiny_heads():
     run_steps(h, 8)
 
 
-def test_integer_inputs_free_running_bit_exact():
+@pytest.mark.parametrize("n_req,n0,top_k", [(2, 1500, 128), (32, 1500, 128), (2, 40000, 2048)])
+def test_integer_inputs_free_running_bit_exact(n_req, n0, top_k):
     """Integer-valued q, k, w make every score exact: the GPU and the oracle run free
-    (each on its own state) and must agree bit for bit at every step."""
-    wl = syn.Workload("int", n_req=2, n_layers=1, n0=1500, n_heads=8, head_dim=64, kv_heads=8,
-                      q_dtype="f32", k_dtype="f32", top_k=128, rho_bp=4000, gamma_bp=1000,
+    (each on its own state) and must agree bit for bit at every step.  Integer scores tie
+    often, so the K-th score is usually shared (cut in slot order); the longer context
+    takes the top-K's sampled bracket, and 32 requests the one-CTA-per-row top-K."""
+    wl = syn.Workload("int", n_req=n_req, n_layers=1, n0=n0, n_heads=8, head_dim=64, kv_heads=8,
+                      q_dtype="f32", k_dtype="f32", top_k=top_k, rho_bp=4000, gamma_bp=1000,
                       alpha=0.9, steps=10, heavy=0, rope_dims=0, seed=5)
     h = Harness(wl)
     g = torch.Generator(device="cuda").manual_seed(9)
@@ -82,8 +85,8 @@ def test_integer_inputs_free_running_bit_exact():
     bt = np_(h.inp.block_table)
     st = h.states[0]
     for step in range(wl.steps):
-        q = torch.randint(-2, 3, (2, 1, 8, 64), generator=g, device="cuda").float()
-        w = torch.randint(0, 3, (2, 1, 8), generator=g, device="cuda").float()
+        q = torch.randint(-2, 3, (n_req, 1, 8, 64), generator=g, device="cuda").float()
+        w = torch.randint(0, 3, (n_req, 1, 8), generator=g, device="cuda").float()
         qp = (h.inp.n_slots - 1).clamp_min(0).to(torch.int32)
         h.buf.status.zero_()
         spin.run_step(h.cfg, st, h.buf, q, w, h.inp.k_pool[0], None, h.inp.n_pages,
@@ -112,6 +115,25 @@ def test_rho_override_device_table():
     h = Harness(wl)
     rho = torch.tensor([6500], dtype=torch.int32, device="cuda")
     run_steps(h, 4, rho=rho)
+
+
+def test_long_context_selection_fallback():
+    """More than 8192 blocks per request: selection takes the shared-memory kernel instead of
+    the register-resident one (and top-K the single-CTA kernel)."""
+    wl = syn.Workload("long", n_req=2, n_layers=1, n0=530000, n_heads=2, head_dim=16, kv_heads=1,
+                      q_dtype="f32", k_dtype="bf16", top_k=256, rho_bp=4000, gamma_bp=500,
+                      alpha=0.9, steps=3, heavy=4, rope_dims=8, seed=3)
+    assert wl.max_blocks > 8192
+    h = Harness(wl)
+    run_steps(h, 3)
+
+
+def test_eight_verifier_rows():
+    """The largest row count (one 8-CTA cluster per request in the selection)."""
+    wl = syn.CONFIGS["mtp"].replace(n_req=2, n0=5000, steps=3, n_heads=8, head_dim=64, rows=8,
+                                    mean_accept=3.0)
+    h = Harness(wl)
+    run_steps(h, 3)
 
 
 # --------------------------------------------------------------- tensor-core kernel
