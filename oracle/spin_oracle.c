@@ -74,13 +74,18 @@ void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
+/* Exploration draw of block j: one Philox4x64-10 output (256 bits) serves the eight blocks
+ * 8m .. 8m+7, counter {step, row, req, m}; block j takes 32-bit half (j mod 8) in order:
+ * word (j mod 8)/2, its high half first. */
 uint32_t oracle_explore_key(uint64_t seed, int32_t layer, uint64_t step, int32_t row,
                             int32_t req, int64_t j) {
-    uint64_t ctr[4] = {step, (uint64_t)(uint32_t)row, (uint64_t)(uint32_t)req, (uint64_t)j};
+    uint64_t ctr[4] = {step, (uint64_t)(uint32_t)row, (uint64_t)(uint32_t)req, (uint64_t)(j >> 3)};
     uint64_t key[2] = {seed, (uint64_t)(uint32_t)layer};
     uint64_t out[4];
     oracle_philox4x64_10(ctr, key, out);
-    return (uint32_t)(out[0] >> 32);
+    const int h = (int)(j & 7);
+    const uint64_t w = out[h >> 1];
+    return (h & 1) ? (uint32_t)(w & 0xFFFFFFFFu) : (uint32_t)(w >> 32);
 }
 
 /* ------------------------------------------------------------------------------

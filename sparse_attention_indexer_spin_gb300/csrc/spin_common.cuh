@@ -72,12 +72,24 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64
     }
 }
 
-// Exploration draw of block j (reading R7): high 32 bits of word 0.
+// Exploration draws: one Philox4x64-10 output (key {seed, layer}, counter {step, row, req, m})
+// serves blocks 8m .. 8m+7; block 8m+h takes 32-bit half h, word h/2, high half first.
+__device__ __forceinline__ void explore_keys8(uint64_t seed, int layer, uint64_t step, int row, int req,
+                                              int64_t m, uint32_t (&out)[8]) {
+    uint64_t c[4] = {step, (uint64_t)(uint32_t)row, (uint64_t)(uint32_t)req, (uint64_t)m};
+    philox4x64_10(c, seed, (uint64_t)(uint32_t)layer);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        out[2 * w] = (uint32_t)(c[w] >> 32);
+        out[2 * w + 1] = (uint32_t)(c[w] & 0xFFFFFFFFu);
+    }
+}
+
 __device__ __forceinline__ uint32_t explore_key(uint64_t seed, int layer, uint64_t step, int row,
                                                 int req, int64_t j) {
-    uint64_t c[4] = {step, (uint64_t)(uint32_t)row, (uint64_t)(uint32_t)req, (uint64_t)j};
-    philox4x64_10(c, seed, (uint64_t)(uint32_t)layer);
-    return (uint32_t)(c[0] >> 32);
+    uint32_t k8[8];
+    explore_keys8(seed, layer, step, row, req, j >> 3, k8);
+    return k8[j & 7];
 }
 
 // ---------------------------------------------------------------------------------------

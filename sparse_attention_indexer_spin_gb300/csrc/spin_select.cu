@@ -30,12 +30,22 @@ namespace spin {
 // ---------------------------------------------------------------------------------------
 constexpr int kBsBlocksPerWarp = 8;
 
+// Block budget m_t (Algorithm 1's budget step) with rho in basis points.
+__device__ __forceinline__ int64_t budget_blocks(int64_t nb, int64_t top_k, int32_t rho_bp) {
+    const int64_t floor_k = (top_k + kBlock - 1) / kBlock;
+    const int64_t keep = ((int64_t)(10000 - rho_bp) * nb + 9999) / 10000;
+    const int64_t m = floor_k > keep ? floor_k : keep;
+    return m < nb ? m : nb;
+}
+
+
 __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const float* __restrict__ V,
                                                           const float* __restrict__ D,
                                                           const float* __restrict__ Vmax,
                                                           const int32_t* __restrict__ warm,
                                                           const int32_t* __restrict__ n_slots,
                                                           const int32_t* __restrict__ q_pos, int rows,
+                                                          const int32_t* __restrict__ rho_override,
                                                           uint64_t seed, uint64_t step, int layer,
                                                           float* __restrict__ S, uint32_t* __restrict__ X) {
     const Dims dm = dims_of(cfg);
@@ -45,6 +55,9 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
     if (request_check(n, q, rows, dm) != 0u || warm[req] == 0) return;
     const int64_t qr = q + r;
     const int64_t nb = (n + kBlock - 1) / kBlock;
+    // a budget of every block (sparsity 0) selects them all: nothing to predict
+    const int32_t rho = rho_override ? *rho_override : cfg.rho_bp;
+    if (rho >= 0 && rho <= 10000 && budget_blocks(nb, cfg.top_k, rho) >= nb) return;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const float* Dq = D + (int64_t)req * dm.DL;
     const float* Vq = V + (int64_t)req * dm.max_slots;
@@ -72,10 +85,17 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
             const float vmb = __shfl_sync(0xffffffffu, vm, b);
             if (lane == 0 && j0 + b < nb) Sq[j0 + b] = sum ? m : fmaxf(vmb, m);
         }
-        // the exploration draw of each block (used only if the block ends up unselected):
-        // computed here, where every block has a thread, off the selection's serial path
-        if (lane < kBsBlocksPerWarp && j0 + lane < nb)
-            Xq[j0 + lane] = explore_key(seed, layer, step, r, req, (int)(j0 + lane));
+    }
+    // the exploration draws (used only for blocks that end up unselected), off the
+    // selection's serial path: a lane computes one Philox output, the draws of 8 blocks
+    // (groups interleaved over the CTAs: a short list needs few of them)
+    for (int64_t g = (int64_t)threadIdx.x * gridDim.x + blockIdx.x; g * 8 < nb;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t k8[8];
+        explore_keys8(seed, layer, step, r, req, g, k8);
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+            if (g * 8 + h < nb) Xq[g * 8 + h] = k8[h];
     }
 }
 
@@ -186,12 +206,6 @@ __device__ int compact_flags(const uint8_t* flag, int n, int32_t* out, SelShared
     return total;
 }
 
-__device__ __forceinline__ int64_t budget_blocks(int64_t nb, int64_t top_k, int32_t rho_bp) {
-    const int64_t floor_k = (top_k + kBlock - 1) / kBlock;
-    const int64_t keep = ((int64_t)(10000 - rho_bp) * nb + 9999) / 10000;
-    const int64_t m = floor_k > keep ? floor_k : keep;
-    return m < nb ? m : nb;
-}
 
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
     spin_config cfg, const int32_t* __restrict__ warm, const int32_t* __restrict__ n_slots,
@@ -227,8 +241,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
     __syncthreads();
     for (int r = 0; r < rows; ++r) {
         const int64_t rr = (int64_t)req * rows + r;
-        if (!is_warm || nb <= 2) {
-            // dense warm-up step (and contexts whose every block is forced)
+        if (!is_warm || nb <= 2 || budget_blocks(nb, cfg.top_k, rho) >= nb) {
+            // dense: warm-up step, every block forced, or a budget of every block
             for (int j = tid; j < nb; j += kSelThreads) flag[j] = 1;
             __syncthreads();
         } else {
@@ -461,8 +475,10 @@ __global__ void __launch_bounds__(kSrThreads, 1) select_reg_kernel(
 #pragma unroll
     for (int i = 0; i < KPT; ++i)
         if (i * kSrThreads + tid < nb) valid |= 1u << i;
-    if (warm[req] == 0 || nb <= 2) {
-        sel = valid;  // dense warm-up step (and contexts whose every block is forced)
+    if (warm[req] == 0 || nb <= 2 || budget_blocks(nb, cfg.top_k, rho) >= nb) {
+        // dense: the warm-up step, contexts whose every block is forced, and budgets of
+        // every block (forced, top and exploration blocks then cover all of them)
+        sel = valid;
         __syncthreads();
     } else {
         const int64_t m = budget_blocks(nb, cfg.top_k, rho);
@@ -555,8 +571,8 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
     float* S = a.block_scores;
     uint32_t* X = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.block_scores) +
                                               select_array_bytes(cfg, a.rows));
-    block_score_kernel<<<g1, 256, 0, s>>>(cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows, cfg.seed,
-                                          a.step, a.layer, S, X);
+    block_score_kernel<<<g1, 256, 0, s>>>(cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,
+                                          a.rho_override, cfg.seed, a.step, a.layer, S, X);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (dm.MB <= kSrMaxBlocks && a.rows >= 1 && a.rows <= 8) {

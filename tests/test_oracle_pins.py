@@ -67,9 +67,18 @@ def test_philox_matches_numpy(oracle_mod, ctr, key):
     assert oracle_mod.philox4x64_10(ctr, key) == _numpy_philox(ctr, key)
 
 
-def test_explore_key_is_high_word0(oracle_mod):
-    out = oracle_mod.philox4x64_10([11, 2, 5, 300], [99, 3])
-    assert oracle_mod.explore_key(99, 3, 11, 2, 5, 300) == out[0] >> 32
+def test_explore_keys_are_the_halves_of_one_philox_output(oracle_mod):
+    """Blocks 8m .. 8m+7 take the eight 32-bit halves of the output for counter m, word by
+    word, high half first."""
+    m = 37
+    out = oracle_mod.philox4x64_10([11, 2, 5, m], [99, 3])
+    halves = []
+    for w in out:
+        halves += [w >> 32, w & 0xFFFFFFFF]
+    assert [oracle_mod.explore_key(99, 3, 11, 2, 5, 8 * m + h) for h in range(8)] == halves
+    # the next counter serves the next eight blocks
+    out2 = oracle_mod.philox4x64_10([11, 2, 5, m + 1], [99, 3])
+    assert oracle_mod.explore_key(99, 3, 11, 2, 5, 8 * m + 8) == out2[0] >> 32
 
 
 # --------------------------------------------------------------------- number formats
