@@ -175,6 +175,42 @@ __device__ __forceinline__ float q_row_scale(const __nv_bfloat16* qrow) {
     return g;
 }
 
+// FP8 query terms of one query vector (128 bf16 values, row n of both B regions) for its
+// 16-element chunks [c0, c1): hi = e4m3(q/g) into the region at sHi, lo = e4m3(q/g - hi)
+// into the region at sLo, each in the 128-byte-swizzled K-major layout the MMA reads.
+__device__ __forceinline__ void q8_convert(const __nv_bfloat16* qrow, float inv_g, int n, int c0, int c1,
+                                           unsigned char* sHi, unsigned char* sLo) {
+    const uint4* src = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll 2
+    for (int ch = c0; ch < c1; ++ch) {
+        const uint4 u0 = src[2 * ch], u1 = src[2 * ch + 1];
+        const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            uint32_t hv = 0, lv = 0;
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t wd = wds[2 * e + pr];
+                const float2 x = make_float2(__uint_as_float(wd << 16) * inv_g, __uint_as_float(wd & 0xffff0000u) * inv_g);
+                const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+                const __half2 hf = *reinterpret_cast<const __half2*>(
+                    &static_cast<const __half2_raw&>(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+                const float2 hx = __half22float2(hf);
+                const float2 rx = make_float2(x.x - hx.x, x.y - hx.y);
+                const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(rx, __NV_SATFINITE, __NV_E4M3);
+                hv |= (uint32_t)h2 << (16 * pr);
+                lv |= (uint32_t)l2 << (16 * pr);
+            }
+            hw[e] = hv;
+            lw[e] = lv;
+        }
+        const uint32_t o = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((ch ^ (n & 7)) << 4));
+        *reinterpret_cast<uint4*>(sHi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(sLo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+}
+
 struct TileInfo {
     int req, k0, blk0, blk1, page0, page1, n;
 };
@@ -225,7 +261,7 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     const Dims dm = dims_of(cfg);
     const int rows = a.rows;
     const int NQ = kTcNH * rows;          // query vectors (rows x heads)
-    const int N = FP8 ? 2 * NQ : NQ;      // MMA N = accumulator columns per tile
+    const int N = NQ;                     // MMA N = accumulator columns per tile
     const TcLayout L = tc_layout(dm.R, rows, FP8);
     TcHdr* hdr = reinterpret_cast<TcHdr*>(smem);
     int* prefix = reinterpret_cast<int*>(smem + L.prefix);
@@ -235,7 +271,8 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int NACC = tc_nacc(N);
     const uint32_t tmem_cols = (uint32_t)(NACC * N) <= 256u ? 256u : 512u;
-    const uint32_t qregion = (uint32_t)NQ * 128;  // bf16: bytes of one K half of B
+    // bytes of one B region: bf16, one K half of q; FP8, the hi (or lo) terms of q
+    const uint32_t qregion = (uint32_t)NQ * 128;
     constexpr int kTcStages = tc_stages(FP8);
 
     // ------------------------------------------------------------------ set-up
@@ -268,7 +305,7 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 mbar_init(&hdr->tempty[s], 128);
             }
             mbar_init(&hdr->qfull, 1);
-            mbar_init(&hdr->qdone, tc_nacc(FP8 ? 2 * kTcNH * rows : kTcNH * rows) >= 4 ? 2 : 1);
+            mbar_init(&hdr->qdone, tc_nacc(kTcNH * rows) >= 4 ? 2 : 1);
             mbar_init(&hdr->qready, 1);
             mbar_init(&hdr->fin[0], 1);
             mbar_init(&hdr->fin[1], 1);
@@ -290,6 +327,29 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     // range, so the even- and odd-tile pipelines see the same sequence of requests
     const int t0 = 2 * (int)(((int64_t)(total / 2) * blockIdx.x) / gridDim.x);
     const int t1 = 2 * (int)(((int64_t)(total / 2) * (blockIdx.x + 1)) / gridDim.x);
+
+    // FP8: the ten warps that are not producers stage the first request's query terms
+    // together (a quarter of a vector per thread) while the producers start loading keys;
+    // the issuers wait for them on named barrier 1, the epilogue warps only arrive
+    const bool prestaged = FP8 && t0 < t1;
+    if (prestaged && wid != 0 && wid != 2) {
+        int lo = 0, hi = dm.R - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= t0) lo = mid; else hi = mid - 1;
+        }
+        const int req0 = lo;
+        const int part = (wid == 1 ? 0 : wid == 3 ? 1 : wid - 2) * 32 + lane;  // 0 .. 319
+        for (int p = part; p < NQ * 4; p += 320) {
+            const int n = p >> 2, c = p & 3, r = n / kTcNH, h = n % kTcNH;
+            const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                        (((int64_t)req0 * rows + r) * kTcNH + h) * kTcD;
+            q8_convert(qrow, 1.0f / q_row_scale(qrow), r * kTcNH + h, 2 * c, 2 * c + 2, sQ, sQ + qregion);
+        }
+        fence_async_smem();
+        if (wid == 1 || wid == 3) named_barrier(1, 320);
+        else asm volatile("bar.arrive 1, 320;" ::: "memory");
+    }
 
     // tile -> request, first list entry, its two blocks and their pages (-1: none / invalid)
     auto decode = [&](int t, TileInfo& ti) {
@@ -420,46 +480,16 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 if (par == 0) {
                     if (nchange > 0 && !mbar_wait(&hdr->qdone, (nchange - 1) & 1u, &hdr->abort_flag)) { fail_wait(); break; }
                     if (FP8) {
-                        // B rows r*128 + h (hi) and r*128 + 64 + h (lo), 128 e4m3 each; lane
-                        // handles the query vectors n = lane, lane + 32, ...
-                        for (int n = lane; n < NQ; n += 32) {
-                            const int r = n / kTcNH, h = n % kTcNH;
-                            const __nv_bfloat16* qrow =
-                                reinterpret_cast<const __nv_bfloat16*>(a.q) + (((int64_t)req * rows + r) * kTcNH + h) * kTcD;
-                            const float inv_g = 1.0f / q_row_scale(qrow);   // exact: a power of two
-                            const uint4* src = reinterpret_cast<const uint4*>(qrow);
-                            const int nh = r * 2 * kTcNH + h, nl = nh + kTcNH;
-    #pragma unroll 2
-                            for (int ch = 0; ch < kTcD / 16; ++ch) {         // 16 elements -> 16 B of e4m3
-                                const uint4 u0 = src[2 * ch], u1 = src[2 * ch + 1];
-                                const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-                                uint32_t hw[4], lw[4];
-    #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    uint32_t hv = 0, lv = 0;
-    #pragma unroll
-                                    for (int pr = 0; pr < 2; ++pr) {
-                                        const uint32_t wd = wds[2 * e + pr];
-                                        const float2 x = make_float2(__uint_as_float(wd << 16) * inv_g,
-                                                                     __uint_as_float(wd & 0xffff0000u) * inv_g);
-                                        const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
-                                        const __half2 hf = *reinterpret_cast<const __half2*>(
-                                            &static_cast<const __half2_raw&>(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
-                                        const float2 hx = __half22float2(hf);
-                                        const float2 rx = make_float2(x.x - hx.x, x.y - hx.y);
-                                        const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(rx, __NV_SATFINITE, __NV_E4M3);
-                                        hv |= (uint32_t)h2 << (16 * pr);
-                                        lv |= (uint32_t)l2 << (16 * pr);
-                                    }
-                                    hw[e] = hv;
-                                    lw[e] = lv;
-                                }
-                                const uint32_t oh = (uint32_t)((nh >> 3) * 1024 + (nh & 7) * 128 + ((ch ^ (nh & 7)) << 4));
-                                const uint32_t ol = (uint32_t)((nl >> 3) * 1024 + (nl & 7) * 128 + ((ch ^ (nl & 7)) << 4));
-                                *reinterpret_cast<uint4*>(sQ + oh) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                                *reinterpret_cast<uint4*>(sQ + ol) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        // row n = r*64 + h of the hi and of the lo region, 128 e4m3 each; lane
+                        // handles the query vectors n = lane, lane + 32, ... (the first request
+                        // of the range was staged by ten warps before the loops started)
+                        if (!(nchange == 0 && prestaged))
+                            for (int n = lane; n < NQ; n += 32) {
+                                const int r = n / kTcNH, h = n % kTcNH;
+                                const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                                            (((int64_t)req * rows + r) * kTcNH + h) * kTcD;
+                                q8_convert(qrow, 1.0f / q_row_scale(qrow), n, 0, kTcD / 16, sQ, sQ + qregion);
                             }
-                        }
                         fence_async_smem();
                         __syncwarp();
                     } else {
@@ -492,8 +522,13 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 const uint64_t b0 = smem_desc_sw128(smem_u32(sQ));
                 const uint32_t d0 = tmem_base + (uint32_t)(ac * N);
                 if (FP8) {
+                    // k.(q_hi + q_lo): the hi terms' four k-steps, then the lo terms' into the same
+                    // accumulator
+                    const uint64_t bl = b0 + (qregion >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) tc_mma_f8(d0, a0 + 2 * kk, b0 + 2 * kk, idesc, kk ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) tc_mma_f8(d0, a0 + 2 * kk, bl + 2 * kk, idesc, 1u);
                 } else {
                     const uint64_t bh = qregion >> 4;
 #pragma unroll
@@ -567,38 +602,30 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
             for (int r = 0; r < rows; ++r) {
-                float z4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                if (FP8) {
+                // the 64 heads' dot products of this slot and row (FP8: k.(q_hi + q_lo), the
+                // per-slot scale s not yet applied)
+                float v[64];
+                tc_ld64(trow + (uint32_t)(r * kTcNH), v);
+                // FP8: sum_h w_h max(s x_h, 0) = |s| sum_h w_h max(sign(s) x_h, 0)
+                if (FP8 && scale < 0.0f) {
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {  // heads 32*half .. 32*half + 31
-                        // columns r*128 + h (k.hi) and r*128 + 64 + h (k.lo)
-                        float v[32], u[32];
-                        tc_ld32(trow + (uint32_t)(r * 2 * kTcNH + half * 32), v);
-                        tc_ld32(trow + (uint32_t)(r * 2 * kTcNH + kTcNH + half * 32), u);
-                        const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH + half * 32);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 wv = wr[j];
-                            z4[0] = fmaf(wv.x, fmaxf(scale * (v[4 * j + 0] + u[4 * j + 0]), 0.0f), z4[0]);
-                            z4[1] = fmaf(wv.y, fmaxf(scale * (v[4 * j + 1] + u[4 * j + 1]), 0.0f), z4[1]);
-                            z4[2] = fmaf(wv.z, fmaxf(scale * (v[4 * j + 2] + u[4 * j + 2]), 0.0f), z4[2]);
-                            z4[3] = fmaf(wv.w, fmaxf(scale * (v[4 * j + 3] + u[4 * j + 3]), 0.0f), z4[3]);
-                        }
-                    }
-                } else {
-                    float v[64];
-                    tc_ld64(trow + (uint32_t)(r * kTcNH), v);
-                    const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float4 wv = wr[j];
-                        z4[0] = fmaf(wv.x, fmaxf(v[4 * j + 0], 0.0f), z4[0]);
-                        z4[1] = fmaf(wv.y, fmaxf(v[4 * j + 1], 0.0f), z4[1]);
-                        z4[2] = fmaf(wv.z, fmaxf(v[4 * j + 2], 0.0f), z4[2]);
-                        z4[3] = fmaf(wv.w, fmaxf(v[4 * j + 3], 0.0f), z4[3]);
-                    }
+                    for (int i = 0; i < 64; ++i) v[i] = -v[i];
                 }
+                float2 z2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
+                const float4* wr = reinterpret_cast<const float4*>(wloc + r * kTcNH);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float4 wv = wr[j];
+                    const float2 x0 = make_float2(fmaxf(v[4 * j + 0], 0.0f), fmaxf(v[4 * j + 1], 0.0f));
+                    const float2 x1 = make_float2(fmaxf(v[4 * j + 2], 0.0f), fmaxf(v[4 * j + 3], 0.0f));
+                    const int c = (j & 1) * 2;
+                    z2[c] = __ffma2_rn(make_float2(wv.x, wv.y), x0, z2[c]);
+                    z2[c + 1] = __ffma2_rn(make_float2(wv.z, wv.w), x1, z2[c + 1]);
+                }
+                const float z4[4] = {z2[0].x + z2[0].y, z2[1].x + z2[1].y, z2[2].x + z2[2].y, z2[3].x + z2[3].y};
                 float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+                if (FP8) z *= fabsf(scale);
                 if (!live || z == 0.0f) z = 0.0f;
                 if (listed) a.scores[(((int64_t)req * rows + r) * dm.MB + k) * kBlock + s] = z;
             }
@@ -651,7 +678,6 @@ static bool encode_rows(CUtensorMap* map, CUtensorMapDataType dt, int elt, const
 }
 
 bool score_tc_supported(const spin_config& cfg, int rows) {
-    if (cfg.k_dtype == SPIN_DTYPE_E4M3 && rows > 2) return false;  // N = 2 x 64 x rows <= 256
     return cfg.kv_heads == 1 && cfg.n_heads == kTcNH && cfg.head_dim == kTcD && rows >= 1 && rows <= kTcMaxRows &&
            cfg.n_req <= kTcMaxReq && cfg.q_dtype == SPIN_DTYPE_BF16 &&
            (cfg.k_dtype == SPIN_DTYPE_BF16 || cfg.k_dtype == SPIN_DTYPE_E4M3);

@@ -146,13 +146,24 @@ def _tc_workload(k_dtype, rows, n_req=3, n0=2000, seed=21):
 
 
 @pytest.mark.parametrize("k_dtype,rows", [("bf16", 1), ("e4m3", 1), ("bf16", 4), ("e4m3", 2),
-                                          ("bf16", 3)])
+                                          ("bf16", 3), ("e4m3", 3), ("e4m3", 4)])
 def test_tcgen05_small_ragged(k_dtype, rows):
     """Shared key, 64 heads x 128 dims: requests of 2000, 130 and 64 slots (odd block lists
     leave half-empty 128-slot tiles), through the tcgen05 kernel."""
     h = Harness(_tc_workload(k_dtype, rows), score_path="tcgen05")
     h.inp.n_slots.copy_(torch.tensor([2000, 130, 64], dtype=torch.int32))
     run_steps(h, 4)
+
+
+def test_tcgen05_negative_fp8_scales():
+    """FP8 per-slot scales of either sign: the scale multiplies the dot product before the
+    ReLU, so a negative scale selects the negative dot products."""
+    h = Harness(_tc_workload("e4m3", 1, seed=23), score_path="tcgen05")
+    g = torch.Generator(device="cuda").manual_seed(3)
+    sc = h.inp.k_scale[0]
+    flip = torch.rand(sc.shape, generator=g, device="cuda") < 0.3
+    sc[flip] = -sc[flip]
+    run_steps(h, 3)
 
 
 @pytest.mark.parametrize("k_dtype", ["bf16", "e4m3"])
