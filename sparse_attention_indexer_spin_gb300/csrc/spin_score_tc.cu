@@ -59,8 +59,14 @@ constexpr int kTcEpiWarps = 8;                      // two per TMEM lane quarter
 constexpr int kTcEpiWarp0 = 4;  // warps 0, 2: producers; 1, 3: MMA issuers; 4-11: epilogue
 constexpr int kTcThreads = (kTcEpiWarp0 + kTcEpiWarps) * 32;
 constexpr int kTcMaxAcc = 4;                        // accumulator buffers in TMEM
-constexpr int kTcStagesMax = 8;  // operand ring depth (tiles in flight per CTA): 128 KB either way
-__host__ __device__ constexpr int tc_stages(bool fp8) { return fp8 ? 8 : 4; }
+// operand ring depth (tiles in flight per CTA): as many as the shared memory budget holds, at
+// most kTcStagesMax, an even number (the producers and issuers alternate tiles)
+constexpr int kTcStagesMax = 8;
+constexpr uint32_t kTcSmemBudget = 220 * 1024;
+// FP8 slot scales travel in their own ring: a tile's scales stay until its epilogue has read
+// them, i.e. up to (key stages + accumulators) tiles after they were loaded
+constexpr int kTcScSlots = 12;
+constexpr int kTcScBytes = 128 * 4;  // one tile: 128 slots
 
 // ------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -224,13 +230,18 @@ struct TcHdr {
     uint64_t qdone;             // both issuers' MMAs of the previous request finished (2 arrivals)
     uint64_t qready;            // q of the next request staged (issuer 0 -> issuer 1)
     uint64_t fin[2];            // an issuer's MMAs all finished (teardown)
+    uint64_t sfull[kTcScSlots];   // FP8: a tile's slot scales landed
+    uint64_t sempty[kTcScSlots];  // FP8: a tile's slot scales read by its epilogue (4 warps)
     uint32_t tmem_base;
     int abort_flag;
     int total_tiles;
 };
 
+static_assert(sizeof(TcHdr) <= 1024, "the header fits its 1 KB");
+
 struct TcLayout {
-    uint32_t prefix, stage_a, qbuf, wbuf, tile_bytes, total;
+    uint32_t prefix, stage_a, qbuf, wbuf, sbuf, tile_bytes, total;
+    int stages;
 };
 
 // accumulator buffers that fit in TMEM's 512 columns
@@ -242,12 +253,21 @@ __host__ __device__ inline TcLayout tc_layout(int R, int rows, bool fp8) {
     uint32_t off = 1024;                                 // header
     L.prefix = off;
     off += ((uint32_t)(R + 1) * 4 + 1023) & ~1023u;
+    const uint32_t qbytes = (uint32_t)(64 * rows) * 256;             // two regions of N rows x 128 B
+    const uint32_t wbytes = (uint32_t)kTcEpiWarps * 64 * rows * 4;    // w (times g) per epilogue warp
+    const uint32_t sbytes = fp8 ? (uint32_t)(kTcScSlots * kTcScBytes) : 0u;  // slot scale ring
+    const uint32_t fixed = off + qbytes + wbytes + sbytes + 1024;     // (+ slack for 1024-byte alignment)
+    int st = fixed < kTcSmemBudget ? (int)((kTcSmemBudget - fixed) / L.tile_bytes) : 0;
+    st = st > kTcStagesMax ? kTcStagesMax : st;
+    L.stages = st & ~1;
     L.stage_a = off;
-    off += tc_stages(fp8) * L.tile_bytes;
+    off += (uint32_t)L.stages * L.tile_bytes;
     L.qbuf = off;
-    off += (uint32_t)(64 * rows) * 256;                  // two regions of N rows x 128 B
+    off += qbytes;
     L.wbuf = off;
-    off += (uint32_t)kTcEpiWarps * 64 * rows * 4;        // w (times g) per epilogue warp
+    off += wbytes;
+    L.sbuf = off;
+    off += sbytes;
     L.total = off + 1024;                                // slack for 1024-byte alignment
     return L;
 }
@@ -268,12 +288,13 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     unsigned char* sA = smem + L.stage_a;
     unsigned char* sQ = smem + L.qbuf;
     float* sW = reinterpret_cast<float*>(smem + L.wbuf);
+    float* sScale = reinterpret_cast<float*>(smem + L.sbuf);  // FP8: [kTcScSlots][128]
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int NACC = tc_nacc(N);
     const uint32_t tmem_cols = (uint32_t)(NACC * N) <= 256u ? 256u : 512u;
     // bytes of one B region: bf16, one K half of q; FP8, the hi (or lo) terms of q
     const uint32_t qregion = (uint32_t)NQ * 128;
-    constexpr int kTcStages = tc_stages(FP8);
+    const int kTcStages = L.stages;
 
     // ------------------------------------------------------------------ set-up
     if (wid == 0) {
@@ -309,6 +330,10 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             mbar_init(&hdr->qready, 1);
             mbar_init(&hdr->fin[0], 1);
             mbar_init(&hdr->fin[1], 1);
+            for (int c = 0; c < kTcScSlots; ++c) {
+                mbar_init(&hdr->sfull[c], 1);
+                mbar_init(&hdr->sempty[c], 4);
+            }
             fence_barrier_init();
         }
     } else if (wid == 1) {
@@ -414,7 +439,8 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         // -------------------------------------------------------------- producers
         // warp 0 loads the even tiles, warp 2 the odd ones (stages alternate with them)
         const int par = wid >> 1;
-        uint32_t issued = 0, phases = 0;  // per stage: ever filled, parity of its last fill
+        uint32_t issued = 0, phases = 0;        // per stage: ever filled, parity of its last fill
+        uint32_t sc_issued = 0, sc_phases = 0;  // the same for the FP8 scale ring
         for (int t = t0 + par, it = par; t < t1; t += 2, it += 2) {
             refresh(t);
             const int page0 = bc(mine.page0, t), page1 = bc(mine.page1, t);
@@ -447,12 +473,43 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             }
             issued |= 1u << s;
             phases = (phases & ~(1u << s)) | (ph << s);
+            if (FP8) {
+                // the tile's slot scales (256 B per page) into scale-ring entry it % kTcScSlots,
+                // once the epilogue of tile it - kTcScSlots has read that entry
+                const int c = it % kTcScSlots;
+                const uint32_t pc = (uint32_t)(it / kTcScSlots) & 1u;
+                int ok2 = 1;
+                if (lane == 0) ok2 = mbar_wait(&hdr->sempty[c], pc ^ 1u, &hdr->abort_flag);
+                if (!__shfl_sync(0xffffffffu, ok2, 0)) {
+                    if (lane == 0) fail_wait();
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t sb = (page0 >= 0 ? 256u : 0u) + (page1 >= 0 ? 256u : 0u);
+                    if (sb == 0) {
+                        mbar_arrive(&hdr->sfull[c]);
+                    } else {
+                        mbar_arrive_expect_tx(&hdr->sfull[c], sb);
+                        if (page0 >= 0)
+                            bulk_g2s(sScale + c * 128, a.k_scale + (int64_t)page0 * kBlock, 256u, &hdr->sfull[c]);
+                        if (page1 >= 0)
+                            bulk_g2s(sScale + c * 128 + 64, a.k_scale + (int64_t)page1 * kBlock, 256u, &hdr->sfull[c]);
+                    }
+                }
+                sc_issued |= 1u << c;
+                sc_phases = (sc_phases & ~(1u << c)) | (pc << c);
+            }
             __syncwarp();
         }
-        if (lane == 0)
+        // never leave with copies in flight: wait (bounded) for the last fill of every entry
+        if (lane == 0) {
             for (int s = 0; s < kTcStages; ++s)
                 if (((issued >> s) & 1u) && !mbar_wait(&hdr->full[s], (phases >> s) & 1u, nullptr))
                     set_status(a.status, SPIN_STATUS_TIMEOUT);
+            for (int c = 0; c < kTcScSlots; ++c)
+                if (((sc_issued >> c) & 1u) && !mbar_wait(&hdr->sfull[c], (sc_phases >> c) & 1u, nullptr))
+                    set_status(a.status, SPIN_STATUS_TIMEOUT);
+        }
     } else if (wid == 1 || wid == 3) {
         // ------------------------------------------------------------ MMA issuers
         // warp 1 issues the even tiles' MMAs, warp 3 the odd ones' (each issuing thread
@@ -562,16 +619,20 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         const int h = m >> 6, s = m & 63;
         float* wloc = sW + (size_t)(wid - kTcEpiWarp0) * NQ;
         int cur_req = -1;
-        // FP8: the slot scale of this warp's next tile is loaded one tile ahead
-        auto scale_of = [&](int t) -> float {
-            if (!FP8 || t >= t1) return 1.0f;
-            refresh(t);
-            const int pg = bc(h ? mine.page1 : mine.page0, t);
-            return pg >= 0 ? __ldg(a.k_scale + (int64_t)pg * kBlock + s) : 1.0f;
-        };
-        float scale_next = scale_of(t0 + parity);
         for (int t = t0 + parity, it = parity; t < t1; t += 2, it += 2) {
-            const float scale = scale_next;
+            // FP8: this slot's scale, from the scale-ring entry the producer filled for tile it
+            // (the four warps of the tile free the entry once they have read it)
+            float scale = 1.0f;
+            if (FP8) {
+                const int c = it % kTcScSlots;
+                if (!mbar_wait(&hdr->sfull[c], (uint32_t)(it / kTcScSlots) & 1u, &hdr->abort_flag)) {
+                    fail_wait();
+                    break;
+                }
+                scale = sScale[c * 128 + m];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hdr->sempty[c]);
+            }
             const TileInfo ti = tile(t);
             const int req = ti.req;
             if (req != cur_req) {
@@ -597,7 +658,6 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 set_status(a.status, blk == -2 ? SPIN_STATUS_BAD_LIST : SPIN_STATUS_BAD_PAGE);
             const int acc = it % NACC;
             const uint32_t phc = (uint32_t)(it / NACC) & 1u;
-            scale_next = scale_of(t + 2);  // (ti holds everything tile t still needs)
             if (!mbar_wait(&hdr->tfull[acc], phc, &hdr->abort_flag)) { fail_wait(); break; }
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
@@ -680,7 +740,8 @@ static bool encode_rows(CUtensorMap* map, CUtensorMapDataType dt, int elt, const
 bool score_tc_supported(const spin_config& cfg, int rows) {
     return cfg.kv_heads == 1 && cfg.n_heads == kTcNH && cfg.head_dim == kTcD && rows >= 1 && rows <= kTcMaxRows &&
            cfg.n_req <= kTcMaxReq && cfg.q_dtype == SPIN_DTYPE_BF16 &&
-           (cfg.k_dtype == SPIN_DTYPE_BF16 || cfg.k_dtype == SPIN_DTYPE_E4M3);
+           (cfg.k_dtype == SPIN_DTYPE_BF16 || cfg.k_dtype == SPIN_DTYPE_E4M3) &&
+           tc_layout(cfg.n_req, rows, cfg.k_dtype == SPIN_DTYPE_E4M3).stages >= 2;
 }
 
 cudaError_t launch_score_tc(const spin_config& cfg, const ScoreArgs& a, cudaStream_t s) {
