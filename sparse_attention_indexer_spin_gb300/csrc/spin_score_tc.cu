@@ -321,18 +321,21 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 mbar_init(&hdr->full[s], 1);
                 mbar_init(&hdr->empty[s], 1);
             }
+            // two accumulators (N > 128): all eight epilogue warps drain every tile, each
+            // parity half of its rows; otherwise four warps drain a tile
+            const bool split_rows = tc_nacc(kTcNH * rows) < 4;
             for (int s = 0; s < kTcMaxAcc; ++s) {
                 mbar_init(&hdr->tfull[s], 1);
-                mbar_init(&hdr->tempty[s], 128);
+                mbar_init(&hdr->tempty[s], split_rows ? 256 : 128);
             }
             mbar_init(&hdr->qfull, 1);
-            mbar_init(&hdr->qdone, tc_nacc(kTcNH * rows) >= 4 ? 2 : 1);
+            mbar_init(&hdr->qdone, 2);
             mbar_init(&hdr->qready, 1);
             mbar_init(&hdr->fin[0], 1);
             mbar_init(&hdr->fin[1], 1);
             for (int c = 0; c < kTcScSlots; ++c) {
                 mbar_init(&hdr->sfull[c], 1);
-                mbar_init(&hdr->sempty[c], 4);
+                mbar_init(&hdr->sempty[c], split_rows ? 8 : 4);
             }
             fence_barrier_init();
         }
@@ -516,9 +519,9 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         // sustains only so many tcgen05.mma, so two double the rate).  Both read sQ: on a
         // request change both commit to qdone, warp 1 waits for both, restages q and
         // signals qready, warp 3 waits for qready.
-        // two issuers when each can own two accumulators (NACC = 4); with NACC = 2 one
-        // issuer alternates both, so its MMAs overlap the epilogue of the previous tile
-        const int nis = NACC >= 4 ? 2 : 1;
+        // two issuers: with four accumulators each owns two, with two each owns one (the
+        // epilogue then drains every tile with all eight warps)
+        const int nis = 2;
         const int par = wid >> 1;
         const uint32_t idesc = idesc_mma(FP8 ? 0u : 1u, (uint32_t)N, (uint32_t)kTcM);
         int cur_req = -1;
@@ -614,14 +617,18 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     } else {
         // ------------------------------------------------------------- epilogue
         const int quarter = wid & 3;
-        const int parity = (wid - kTcEpiWarp0) / 4;  // this warp takes the tiles it with it % 2 == parity
+        // four accumulators: this warp takes the tiles it with it % 2 == parity, all rows;
+        // two: every tile, the rows r with r % 2 == parity (the accumulator frees sooner)
+        const int parity = (wid - kTcEpiWarp0) / 4;
+        const bool split_rows = NACC < 4;
+        const int tstep = split_rows ? 1 : 2;
         const int m = quarter * 32 + lane;      // slot row of the tile = TMEM lane
         const int h = m >> 6, s = m & 63;
         float* wloc = sW + (size_t)(wid - kTcEpiWarp0) * NQ;
         int cur_req = -1;
-        for (int t = t0 + parity, it = parity; t < t1; t += 2, it += 2) {
+        for (int t = t0 + (split_rows ? 0 : parity), it = split_rows ? 0 : parity; t < t1; t += tstep, it += tstep) {
             // FP8: this slot's scale, from the scale-ring entry the producer filled for tile it
-            // (the four warps of the tile free the entry once they have read it)
+            // (the warps that drain the tile free the entry once they have read it)
             float scale = 1.0f;
             if (FP8) {
                 const int c = it % kTcScSlots;
@@ -661,7 +668,7 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             if (!mbar_wait(&hdr->tfull[acc], phc, &hdr->abort_flag)) { fail_wait(); break; }
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
-            for (int r = 0; r < rows; ++r) {
+            for (int r = split_rows ? parity : 0; r < rows; r += split_rows ? 2 : 1) {
                 // the 64 heads' dot products of this slot and row (FP8: k.(q_hi + q_lo), the
                 // per-slot scale s not yet applied)
                 float v[64];
