@@ -668,12 +668,9 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             if (!mbar_wait(&hdr->tfull[acc], phc, &hdr->abort_flag)) { fail_wait(); break; }
             tc_fence_after();
             const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * N);
-            for (int r = split_rows ? parity : 0; r < rows; r += split_rows ? 2 : 1) {
-                // the 64 heads' dot products of this slot and row (FP8: k.(q_hi + q_lo), the
-                // per-slot scale s not yet applied)
-                float v[64];
-                tc_ld64(trow + (uint32_t)(r * kTcNH), v);
-                // FP8: sum_h w_h max(s x_h, 0) = |s| sum_h w_h max(sign(s) x_h, 0)
+            // sum_h w_h max(x_h, 0) of one row from its 64 heads' dot products (FP8:
+            // k.(q_hi + q_lo) before the per-slot scale s, applied as |s| with sign(s) in x)
+            auto head_sum = [&](float* v, int r) -> float {
                 if (FP8 && scale < 0.0f) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) v[i] = -v[i];
@@ -690,11 +687,20 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                     z2[c] = __ffma2_rn(make_float2(wv.x, wv.y), x0, z2[c]);
                     z2[c + 1] = __ffma2_rn(make_float2(wv.z, wv.w), x1, z2[c + 1]);
                 }
-                const float z4[4] = {z2[0].x + z2[0].y, z2[1].x + z2[1].y, z2[2].x + z2[2].y, z2[3].x + z2[3].y};
-                float z = (z4[0] + z4[1]) + (z4[2] + z4[3]);
+                float z = ((z2[0].x + z2[0].y) + (z2[1].x + z2[1].y)) + ((z2[2].x + z2[2].y) + (z2[3].x + z2[3].y));
                 if (FP8) z *= fabsf(scale);
-                if (!live || z == 0.0f) z = 0.0f;
+                return (!live || z == 0.0f) ? 0.0f : z;
+            };
+            auto emit = [&](float z, int r) {
                 if (listed) a.scores[(((int64_t)req * rows + r) * dm.MB + k) * kBlock + s] = z;
+            };
+            // this warp's rows (paired TMEM loads measured slower)
+            const int rstep = split_rows ? 2 : 1;
+            int r = split_rows ? parity : 0;
+            for (; r < rows; r += rstep) {
+                float v[64];
+                tc_ld64(trow + (uint32_t)(r * kTcNH), v);
+                emit(head_sum(v, r), r);
             }
             tc_fence_before();
             mbar_arrive(&hdr->tempty[acc]);
