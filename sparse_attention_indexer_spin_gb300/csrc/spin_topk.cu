@@ -181,25 +181,70 @@ topk_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __
 // ---------------------------------------------------------------------------------------
 // Cluster version: the candidates of one (request, row) are split over the 8 CTAs of a
 // thread-block cluster in candidate order.  Each CTA keeps its slice's keys in shared
-// memory (one global read), builds per-pass histograms with warp-aggregated shared
-// atomics, and reads its peers' histograms over distributed shared memory, so all CTAs
-// take the same digit decisions.  The ordered write uses the peers' kept counts as the
-// output offset of each slice.
+// memory (one global read) and builds per-pass histograms with warp-aggregated shared
+// atomics.  The cluster-wide histogram is reduced in distributed shared memory: CTA r
+// sums bins [r S, (r+1) S) of every peer (S = bins / 8, 16-byte loads), and every CTA
+// then gathers the eight shares, so all CTAs take the same digit decisions from one
+// scan.  The live-candidate count is the first pass's histogram total.  The ordered
+// write uses the peers' kept counts as the output offset of each slice.
 // ---------------------------------------------------------------------------------------
 constexpr int kTkCluster = 8;
 
-// keys of a slice, then (at this offset, in 4-byte words) the slice's list entries
-__host__ __device__ inline int64_t kTkListOffset(const spin_config& cfg) {
+// candidates of the largest slice, rounded up to whole 16-byte words
+__host__ __device__ inline int64_t kTkSliceKeys(const spin_config& cfg) {
     const Dims dm = dims_of(cfg);
     const int64_t per = ((int64_t)dm.MB * kBlock + kTkCluster - 1) / kTkCluster;
     return (per + 3) & ~(int64_t)3;
 }
 
+// Adds the warp's bins (-1: none) to a shared histogram: the lanes that share the first
+// active lane's bin with one atomic, the others one atomic each.
+__device__ __forceinline__ void tk_hist_add(int* h, int bin) {
+    const int lane = threadIdx.x & 31;
+    const unsigned act = __ballot_sync(0xffffffffu, bin >= 0);
+    if (act == 0u) return;
+    const int lead = __ffs(act) - 1;
+    const int b0 = __shfl_sync(0xffffffffu, bin, lead);
+    const unsigned m0 = __ballot_sync(0xffffffffu, bin == b0);
+    if (lane == lead) atomicAdd(&h[b0], __popc(m0));
+    else if (bin >= 0 && bin != b0) atomicAdd(&h[bin], 1);
+}
+
+// Exclusive scan of unsigned words over the CTA (blockDim.x == kTopkThreads); `smem`
+// holds 33 words.  Sums wrap modulo 2^32, which two packed 16-bit counts never reach.
+__device__ __forceinline__ uint32_t tk_block_excl_scan_u(uint32_t v, uint32_t* smem, uint32_t* total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
+    if (lane == 31) smem[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        const uint32_t s = smem[lane];
+        uint32_t si = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) si += t;
+        }
+        smem[lane] = si - s;
+        if (lane == 31) smem[32] = si;
+    }
+    __syncthreads();
+    const uint32_t res = smem[wid] + inc - v;
+    *total = smem[32];
+    __syncthreads();
+    return res;
+}
+
 struct TkClusterShared {
-    int hist[2][kTopkBins];   // double-buffered local histogram (peers read it)
-    int merged[kTopkBins];
-    int scan[33];
-    int counts[4];            // valid, gt, eq (published to peers)
+    __align__(16) int hist[2][kTopkBins];             // double-buffered local histogram
+    __align__(16) int share[kTopkBins / kTkCluster];  // this CTA's bins of the cluster sum
+    uint32_t scan[33];
+    int counts[4];                                    // gt, eq of the slice (peers read them)
     uint32_t prefix;
     int kk;
 };
@@ -235,164 +280,137 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
     const int nloc_pad = (nloc + 31) & ~31;
 
     // 1. keys of this slice (0 = not a live candidate; live keys are never 0).  The slice
-    // [c0, c1) is a multiple of 8 candidates long and starts 32-byte aligned: its list
-    // entries are staged first, then the scores are read as float4 with every load of a
-    // thread in flight together.
-    int* slist = reinterpret_cast<int*>(keys + kTkListOffset(cfg));
-    const int64_t e0 = c0 >> 6;
-    const int ne = (int)(nloc > 0 ? ((c1 - 1) >> 6) - e0 + 1 : 0);
-    for (int i = tid; i < ne; i += kTopkThreads) slist[i] = lst[e0 + i];
-    __syncthreads();
-    int v = 0;
-    bool bad_list = false;
-    const float4* sc4 = reinterpret_cast<const float4*>(sc + c0);
-    uint4* keys4 = reinterpret_cast<uint4*>(keys);
+    // [c0, c1) is a multiple of 8 candidates long and starts 32-byte aligned; the list
+    // entry of each group of 4 candidates is read with its scores (16 consecutive groups
+    // share one entry).
+    {
+        bool bad_list = false;
+        const float4* sc4 = reinterpret_cast<const float4*>(sc + c0);
+        uint4* keys4 = reinterpret_cast<uint4*>(keys);
 #pragma unroll 4
-    for (int i4 = tid; i4 < nloc / 4; i4 += kTopkThreads) {
-        const int64_t c = c0 + 4 * (int64_t)i4;
-        const int blk = slist[(c >> 6) - e0];
-        const float4 z = sc4[i4];
-        const int64_t slot = (int64_t)blk * kBlock + (c & 63);
-        uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-        if (blk >= 0 && blk < nb) {
-            kv.x = slot + 0 < n ? order_key(z.x) : 0u;
-            kv.y = slot + 1 < n ? order_key(z.y) : 0u;
-            kv.z = slot + 2 < n ? order_key(z.z) : 0u;
-            kv.w = slot + 3 < n ? order_key(z.w) : 0u;
-        } else {
-            bad_list = true;
+        for (int i4 = tid; i4 < nloc / 4; i4 += kTopkThreads) {
+            const int64_t c = c0 + 4 * (int64_t)i4;
+            const int blk = __ldg(lst + (c >> 6));
+            const float4 z = __ldg(sc4 + i4);
+            const int64_t slot = (int64_t)blk * kBlock + (c & 63);
+            uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+            if (blk >= 0 && blk < nb) {
+                kv.x = slot + 0 < n ? order_key(z.x) : 0u;
+                kv.y = slot + 1 < n ? order_key(z.y) : 0u;
+                kv.z = slot + 2 < n ? order_key(z.z) : 0u;
+                kv.w = slot + 3 < n ? order_key(z.w) : 0u;
+            } else {
+                bad_list = true;
+            }
+            keys4[i4] = kv;
         }
-        keys4[i4] = kv;
-        v += (kv.x != 0u) + (kv.y != 0u) + (kv.z != 0u) + (kv.w != 0u);
-    }
-    if (bad_list && rr % rows == 0) set_status(status, SPIN_STATUS_BAD_LIST);
-    int nvalid_loc;
-    block_excl_scan(v, sh.scan, &nvalid_loc);
-    if (tid == 0) sh.counts[0] = nvalid_loc;
-    cluster.sync();
-    int nvalid = 0;
-    for (int p = 0; p < kTkCluster; ++p) nvalid += cluster.map_shared_rank(&sh.counts[0], p)[0];
-
-    uint32_t T = 0;
-    int kk = 0;
-    if (nvalid > K) {
-        uint32_t prefix = 0, mask = 0;
-        kk = K;
-        const int shifts[3] = {21, 10, 0};
-        const int widths[3] = {11, 11, 10};
-        for (int pass = 0; pass < 3; ++pass) {
-            const int shift = shifts[pass];
-            const uint32_t dmask = (1u << widths[pass]) - 1u;
-            int* hist = sh.hist[pass & 1];
-            for (int b = tid; b < kTopkBins; b += kTopkThreads) hist[b] = 0;
-            __syncthreads();
-            for (int i = tid; i < nloc_pad; i += kTopkThreads) {
-                int bin = -1;
-                if (i < nloc) {
-                    const uint32_t key = keys[i];
-                    if (key != 0u && (key & mask) == prefix) bin = (int)((key >> shift) & dmask);
-                }
-                const unsigned same = __match_any_sync(0xffffffffu, bin);
-                if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
-            }
-            cluster.sync();  // local histograms complete and visible to the peers
-            const int nbins = (int)dmask + 1;
-            for (int b = tid; b < nbins; b += kTopkThreads) {
-                int s = 0;
-                for (int p = 0; p < kTkCluster; ++p) s += cluster.map_shared_rank(hist, p)[b];
-                sh.merged[b] = s;
-            }
-            __syncthreads();
-            if (wid == 0) {
-                const int per = nbins / 32;
-                int s = 0;
-                for (int b = 0; b < per; ++b) s += sh.merged[(int)dmask - per * lane - b];
-                const int inc = warp_incl_scan(s);
-                const unsigned ball = __ballot_sync(0xffffffffu, inc >= kk);
-                const int src = __ffs(ball) - 1;
-                if (lane == src) {
-                    int above = inc - s, digit = 0;
-                    for (int b = 0; b < per; ++b) {
-                        const int d = (int)dmask - per * lane - b;
-                        const int h = sh.merged[d];
-                        if (above + h >= kk) { digit = d; break; }
-                        above += h;
-                    }
-                    sh.prefix = prefix | ((uint32_t)digit << shift);
-                    sh.kk = kk - above;
-                }
-            }
-            __syncthreads();
-            prefix = sh.prefix;
-            kk = sh.kk;
-            mask |= dmask << shift;
-        }
-        T = prefix;
-    } else {
-        T = 0;   // every live key (> 0) is kept
-        kk = 0;
+        if (bad_list && rr % rows == 0) set_status(status, SPIN_STATUS_BAD_LIST);
     }
 
-    // 2. per-slice counts -> offsets
-    int g = 0, e = 0;
-    for (int i = tid; i < nloc; i += kTopkThreads) {
+    // 2. radix select of the K-th largest key over 11 + 11 + 10 bits
+    uint32_t prefix = 0, mask = 0;
+    int kk = K;
+    bool keep_all = false;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const uint32_t dmask = pass == 2 ? 1023u : 2047u;
+        const int nbins = (int)dmask + 1;
+        const int S = nbins / kTkCluster;  // bins of one share: 256 or 128
+        int* hist = sh.hist[pass & 1];
+        for (int b = tid; b < nbins; b += kTopkThreads) hist[b] = 0;
+        __syncthreads();
+        for (int i = tid; i < nloc_pad; i += kTopkThreads) {
+            int bin = -1;
+            if (i < nloc) {
+                const uint32_t key = keys[i];
+                if (key != 0u && (key & mask) == prefix) bin = (int)((key >> shift) & dmask);
+            }
+            tk_hist_add(hist, bin);
+        }
+        cluster.sync();  // local histograms complete and visible to the peers
+        if (tid < S / 4) {
+            int4 a = make_int4(0, 0, 0, 0);
+#pragma unroll
+            for (int p = 0; p < kTkCluster; ++p) {
+                const int4 h = reinterpret_cast<const int4*>(cluster.map_shared_rank(hist, p) + rank * S)[tid];
+                a.x += h.x; a.y += h.y; a.z += h.z; a.w += h.w;
+            }
+            reinterpret_cast<int4*>(sh.share)[tid] = a;
+        }
+        cluster.sync();  // shares complete
+        // thread t holds bins 4u .. 4u + 3 with u = nbins / 4 - 1 - t: bins in descending order
+        const int u = nbins / 4 - 1 - tid;
+        int4 h = make_int4(0, 0, 0, 0);
+        if (u >= 0) {
+            const int owner = (4 * u) / S;
+            h = reinterpret_cast<const int4*>(cluster.map_shared_rank(sh.share, owner) + (4 * u - owner * S))[0];
+        }
+        const int c4 = h.x + h.y + h.z + h.w;
+        const int inc = warp_incl_scan(c4);
+        if (lane == 31) sh.scan[wid] = (uint32_t)inc;
+        __syncthreads();
+        const int wtot = (int)sh.scan[lane];
+        const int winc = warp_incl_scan(wtot);
+        const int total = __shfl_sync(0xffffffffu, winc, 31);
+        if (pass == 0 && total <= K) {  // every live candidate is kept (same decision cluster-wide)
+            keep_all = true;
+            __syncthreads();
+            break;
+        }
+        const int excl = __shfl_sync(0xffffffffu, winc - wtot, wid) + inc - c4;
+        if (excl < kk && excl + c4 >= kk) {
+            int above = excl, d = 4 * u + 3;
+            if (above + h.w < kk) { above += h.w; d -= 1;
+                if (above + h.z < kk) { above += h.z; d -= 1;
+                    if (above + h.y < kk) { above += h.y; d -= 1; } } }
+            sh.prefix = prefix | ((uint32_t)d << shift);
+            sh.kk = kk - above;
+        }
+        __syncthreads();
+        prefix = sh.prefix;
+        kk = sh.kk;
+        mask |= dmask << shift;
+    }
+    const uint32_t T = keep_all ? 0u : prefix;
+    if (keep_all) kk = 0;
+
+    // 3. each thread owns a contiguous run of the slice: one packed scan of its gt and eq
+    // counts gives the slice totals (published to the peers) and the in-slice offsets
+    const int ipt = (nloc + kTopkThreads - 1) / kTopkThreads;
+    const int i0 = min(nloc, tid * ipt), i1 = min(nloc, i0 + ipt);
+    uint32_t g = 0, e = 0;
+    for (int i = i0; i < i1; ++i) {
         const uint32_t key = keys[i];
         g += key > T;
-        e += (key == T && key != 0u);
+        e += key == T && key != 0u;
     }
-    int gt_loc, eq_loc;
-    block_excl_scan(g, sh.scan, &gt_loc);
-    block_excl_scan(e, sh.scan, &eq_loc);
-    if (tid == 0) { sh.counts[1] = gt_loc; sh.counts[2] = eq_loc; }
+    uint32_t tot;
+    const uint32_t ex = tk_block_excl_scan_u((g << 16) | e, sh.scan, &tot);
+    if (tid == 0) { sh.counts[0] = (int)(tot >> 16); sh.counts[1] = (int)(tot & 0xFFFFu); }
     cluster.sync();
     // slice p keeps its gt keys and, of its eq keys, those ranked below kk cluster-wide
     int eq_before = 0, out_base = 0, kept_total = 0, eb = 0;
     for (int p = 0; p < kTkCluster; ++p) {
         const int* pc = cluster.map_shared_rank(sh.counts, p);
-        const int pk = pc[1] + max(0, min(pc[2], kk - eb));
-        if (p < rank) { out_base += pk; eq_before += pc[2]; }
+        const int pk = pc[0] + max(0, min(pc[1], kk - eb));
+        if (p < rank) { out_base += pk; eq_before += pc[1]; }
         kept_total += pk;
-        eb += pc[2];
+        eb += pc[1];
     }
-
-    // 3. ordered write of the kept slot ids of this slice
-    constexpr int kItems = 4;
-    int written = out_base, eq_seen = eq_before;
-    for (int base = 0; base < nloc; base += kTopkThreads * kItems) {
-        uint8_t gt[kItems], eq[kItems];
-        int n_eq = 0;
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int i = base + tid * kItems + it;
-            gt[it] = eq[it] = 0;
-            if (i < nloc) {
-                const uint32_t key = keys[i];
-                gt[it] = key > T;
-                eq[it] = key == T && key != 0u;
-            }
-            n_eq += eq[it];
-        }
-        int eq_total;
-        int eq_rank = eq_seen + block_excl_scan(n_eq, sh.scan, &eq_total);
-        int n_keep = 0;
-        uint8_t keep[kItems];
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            keep[it] = gt[it];
-            if (eq[it]) { keep[it] = eq_rank < kk; ++eq_rank; }
-            n_keep += keep[it];
-        }
-        int keep_total;
-        int pos = written + block_excl_scan(n_keep, sh.scan, &keep_total);
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            if (keep[it] && pos < K) {
-                const int64_t c = c0 + base + tid * kItems + it;
-                out[pos++] = (int32_t)((int64_t)slist[(c >> 6) - e0] * kBlock + (c & 63));
+    const int eq_keep = max(0, kk - eq_before);  // eq keys this slice keeps (its first ones)
+    int gb = (int)(ex >> 16), ebf = (int)(ex & 0xFFFFu);
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t key = keys[i];
+        const bool gt = key > T, eq = key == T && key != 0u;
+        if (gt || (eq && ebf < eq_keep)) {
+            const int pos = out_base + gb + min(ebf, eq_keep);
+            if (pos < K) {
+                const int64_t c = c0 + i;
+                out[pos] = (int32_t)((int64_t)__ldg(lst + (c >> 6)) * kBlock + (c & 63));
             }
         }
-        written += keep_total;
-        eq_seen += eq_total;
+        gb += gt;
+        ebf += eq;
     }
     if (rank == kTkCluster - 1)
         for (int k = kept_total + tid; k < K; k += kTopkThreads) out[k] = -1;
@@ -628,10 +646,7 @@ topk_row_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t
     for (int k = written + tid; k < K; k += kTrThreads) out[k] = -1;
 }
 
-static size_t topk_cluster_smem(const spin_config& cfg) {
-    const Dims dm = dims_of(cfg);
-    return (size_t)kTkListOffset(cfg) * 4 + (size_t)(dm.MB / kTkCluster + 2) * 4;
-}
+static size_t topk_cluster_smem(const spin_config& cfg) { return (size_t)kTkSliceKeys(cfg) * 4; }
 
 cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32_t* list,
                         const int32_t* n_list, const int32_t* n_slots, int rows, int32_t* topk_idx,
