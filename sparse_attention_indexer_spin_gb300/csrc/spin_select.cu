@@ -334,7 +334,8 @@ __device__ __forceinline__ void sr_scan_counts(SrShared& sh, int n) {
 
 // Marks in `sel` the k eligible entries with the largest keys, equal keys in ascending j.
 // Requires 0 < k < (number of eligible entries).  `pass` counts histogram passes across
-// calls (buffer rotation); on entry buffers pass % 3 and (pass + 1) % 3 are zero.
+// calls (buffer rotation); on entry buffers pass % 3 and (pass + 1) % 3 are zero, and
+// every pass leaves that so for the next one, also when the digits stop early.
 template <int KPT>
 __device__ void sr_top(const uint32_t (&key)[KPT], uint32_t elig, uint32_t& sel, int k, int& pass, SrShared& sh) {
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -377,6 +378,15 @@ __device__ void sr_top(const uint32_t (&key)[KPT], uint32_t elig, uint32_t& sel,
         mask |= 0xFFu << shift;
         kk -= above;
         n_eq = nbin;
+        if (kk == nbin && d < 3) {
+            // every key of the threshold bin is taken: the selection is the eligible keys
+            // whose digits so far are >= the prefix, and no tie is left to rank
+            ++pass;
+#pragma unroll
+            for (int i = 0; i < KPT; ++i)
+                if (((elig >> i) & 1u) && (key[i] & mask) >= prefix) sel |= 1u << i;
+            return;
+        }
     }
     // keys above the threshold, then the first kk of the keys equal to it
     uint32_t eq = 0;

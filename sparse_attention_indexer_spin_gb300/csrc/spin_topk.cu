@@ -246,7 +246,7 @@ struct TkClusterShared {
     uint32_t scan[33];
     int counts[4];                                    // gt, eq of the slice (peers read them)
     uint32_t prefix;
-    int kk;
+    int kk, nbin;
 };
 
 __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTopkThreads, 1)
@@ -282,7 +282,9 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
     // 1. keys of this slice (0 = not a live candidate; live keys are never 0).  The slice
     // [c0, c1) is a multiple of 8 candidates long and starts 32-byte aligned; the list
     // entry of each group of 4 candidates is read with its scores (16 consecutive groups
-    // share one entry).
+    // share one entry) and kept in shared memory for the write.
+    int* slist = reinterpret_cast<int*>(keys + kTkSliceKeys(cfg));
+    const int64_t e0 = c0 >> 6;
     {
         bool bad_list = false;
         const float4* sc4 = reinterpret_cast<const float4*>(sc + c0);
@@ -292,6 +294,7 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
             const int64_t c = c0 + 4 * (int64_t)i4;
             const int blk = __ldg(lst + (c >> 6));
             const float4 z = __ldg(sc4 + i4);
+            if (i4 == 0 || (c & 63) == 0) slist[(c >> 6) - e0] = blk;
             const int64_t slot = (int64_t)blk * kBlock + (c & 63);
             uint4 kv = make_uint4(0u, 0u, 0u, 0u);
             if (blk >= 0 && blk < nb) {
@@ -310,7 +313,7 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
     // 2. radix select of the K-th largest key over 11 + 11 + 10 bits
     uint32_t prefix = 0, mask = 0;
     int kk = K;
-    bool keep_all = false;
+    bool keep_all = false, exact_bin = false;
     for (int pass = 0; pass < 3; ++pass) {
         const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
         const uint32_t dmask = pass == 2 ? 1023u : 2047u;
@@ -359,20 +362,27 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
         }
         const int excl = __shfl_sync(0xffffffffu, winc - wtot, wid) + inc - c4;
         if (excl < kk && excl + c4 >= kk) {
-            int above = excl, d = 4 * u + 3;
-            if (above + h.w < kk) { above += h.w; d -= 1;
-                if (above + h.z < kk) { above += h.z; d -= 1;
-                    if (above + h.y < kk) { above += h.y; d -= 1; } } }
+            int above = excl, d = 4 * u + 3, nbin = h.w;
+            if (above + h.w < kk) { above += h.w; d -= 1; nbin = h.z;
+                if (above + h.z < kk) { above += h.z; d -= 1; nbin = h.y;
+                    if (above + h.y < kk) { above += h.y; d -= 1; nbin = h.x; } } }
             sh.prefix = prefix | ((uint32_t)d << shift);
             sh.kk = kk - above;
+            sh.nbin = nbin;
         }
         __syncthreads();
         prefix = sh.prefix;
         kk = sh.kk;
         mask |= dmask << shift;
+        if (kk == sh.nbin && pass < 2) {  // the whole threshold bin is kept: keys >= prefix
+            exact_bin = true;
+            break;
+        }
     }
-    const uint32_t T = keep_all ? 0u : prefix;
-    if (keep_all) kk = 0;
+    // keep_all: every live key (> 0); exact_bin: every key >= prefix (> 0 then), that is
+    // > prefix - 1 with no tie kept; otherwise keys > prefix and the first kk equal to it
+    const uint32_t T = keep_all ? 0u : exact_bin ? prefix - 1u : prefix;
+    if (keep_all || exact_bin) kk = 0;
 
     // 3. each thread owns a contiguous run of the slice: one packed scan of its gt and eq
     // counts gives the slice totals (published to the peers) and the in-slice offsets
@@ -406,7 +416,7 @@ topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int
             const int pos = out_base + gb + min(ebf, eq_keep);
             if (pos < K) {
                 const int64_t c = c0 + i;
-                out[pos] = (int32_t)((int64_t)__ldg(lst + (c >> 6)) * kBlock + (c & 63));
+                out[pos] = (int32_t)((int64_t)slist[(c >> 6) - e0] * kBlock + (c & 63));
             }
         }
         gb += gt;
@@ -646,7 +656,10 @@ topk_row_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t
     for (int k = written + tid; k < K; k += kTrThreads) out[k] = -1;
 }
 
-static size_t topk_cluster_smem(const spin_config& cfg) { return (size_t)kTkSliceKeys(cfg) * 4; }
+// keys of the largest slice, then its list entries (a slice spans at most MB / 8 + 2)
+static size_t topk_cluster_smem(const spin_config& cfg) {
+    return (size_t)kTkSliceKeys(cfg) * 4 + (size_t)(dims_of(cfg).MB / kTkCluster + 2) * 4;
+}
 
 cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32_t* list,
                         const int32_t* n_list, const int32_t* n_slots, int rows, int32_t* topk_idx,
