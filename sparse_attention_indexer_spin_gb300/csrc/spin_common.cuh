@@ -126,6 +126,42 @@ __device__ __forceinline__ int block_excl_scan(int v, int* smem, int* total) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Programmatic dependent launch (PTX ISA: griddepcontrol).  Every kernel of the library is
+// launched with programmatic stream serialization allowed and begins with pdl_begin():
+// the next kernel on the stream may be scheduled at once (its CTAs take free SM slots
+// while this grid runs), and this grid waits, before any other instruction, until the
+// previous grid on the stream has completed and its writes are visible.  So no memory
+// access of a kernel overlaps its predecessor; only launch latency is hidden.  A kernel
+// launched without the attribute passes both instructions at once.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Host side: launch `k` with programmatic stream serialization allowed, plus any extra
+// launch attributes (a cluster shape).
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              const cudaLaunchAttribute* extra, int n_extra, A&&... args) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = grid;
+    lc.blockDim = block;
+    lc.dynamicSmemBytes = smem;
+    lc.stream = s;
+    cudaLaunchAttribute at[4];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    for (int i = 0; i < n_extra && i < 3; ++i) at[1 + i] = extra[i];
+    lc.attrs = at;
+    lc.numAttrs = 1 + (n_extra < 3 ? n_extra : 3);
+    return [&](P... coerced) {
+        void* pa[] = {const_cast<void*>(static_cast<const void*>(&coerced))...};
+        return cudaLaunchKernelExC(&lc, reinterpret_cast<const void*>(k), pa);
+    }(static_cast<A&&>(args)...);
+}
+
+// ---------------------------------------------------------------------------------------
 // mbarrier and bulk-copy primitives (PTX ISA: mbarrier, cp.async.bulk).  Every wait is
 // bounded: after kWaitLimitNs of global time it reports failure instead of spinning on.
 // ---------------------------------------------------------------------------------------

@@ -27,6 +27,7 @@ constexpr int kEmaThreads = 256;
 constexpr int kEmaMapBlocks = kEmaSpan / kBlock + 2;
 
 __global__ void __launch_bounds__(kEmaThreads) ema_replay_kernel(spin_config cfg, EmaArgs a) {
+    pdl_begin();
     extern __shared__ float zs[];  // [(a+1)][span]
     __shared__ int pos[kEmaMapBlocks];
     const Dims dm = dims_of(cfg);
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(kEmaThreads) ema_replay_kernel(spin_config cfg
 constexpr int kEmaListEntries = 16;  // per CTA of 8 warps
 
 __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs a) {
+    pdl_begin();
     const Dims dm = dims_of(cfg);
     const int req = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int64_t n = a.n_slots[req], q = a.q_pos[req], cnt = a.n_list[req];
@@ -217,14 +219,12 @@ cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s)
     const Dims dm = dims_of(cfg);
     if (a.accepted == nullptr && a.rows == 1) {
         dim3 grid((dm.MB + kEmaListEntries - 1) / kEmaListEntries, dm.R);
-        ema_list_kernel<<<grid, 256, 0, s>>>(cfg, a);
-        return cudaGetLastError();
+        return launch_pdl(ema_list_kernel, grid, dim3(256), 0, s, nullptr, 0, cfg, a);
     }
     const int gx = (dm.max_slots + kEmaSpan - 1) / kEmaSpan;
     dim3 grid(gx > 0 ? gx : 1, dm.R);
     const size_t smem = sizeof(float) * (size_t)a.rows * (kEmaSpan + a.rows);
-    ema_replay_kernel<<<grid, kEmaThreads, smem, s>>>(cfg, a);
-    return cudaGetLastError();
+    return launch_pdl(ema_replay_kernel, grid, dim3(kEmaThreads), smem, s, nullptr, 0, cfg, a);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -232,6 +232,7 @@ cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s)
 // ---------------------------------------------------------------------------------------
 __global__ void init_state_kernel(spin_config cfg, float* V, float* D, float* Vmax, int32_t* warm, int req0,
                                   int nreq) {
+    pdl_begin();
     const Dims dm = dims_of(cfg);
     const int64_t nv = (int64_t)nreq * dm.max_slots, nd = (int64_t)nreq * dm.DL, nm = (int64_t)nreq * dm.MB;
     float* V0 = V + (int64_t)req0 * dm.max_slots;
@@ -251,8 +252,8 @@ cudaError_t launch_init_state(const spin_config& cfg, float* V, float* D, float*
     const int req0 = req < 0 ? 0 : req;
     const int nreq = req < 0 ? cfg.n_req : 1;
     const int grid = device_sm_count() * 4;
-    init_state_kernel<<<grid, 256, 0, s>>>(cfg, V, D, Vmax, warm, req0, nreq);
-    return cudaGetLastError();
+    return launch_pdl(init_state_kernel, dim3(grid), dim3(256), 0, s, nullptr, 0, cfg, V, D, Vmax, warm, req0,
+                      nreq);
 }
 
 }  // namespace spin

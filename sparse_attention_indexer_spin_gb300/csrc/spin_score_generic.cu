@@ -30,6 +30,7 @@ __device__ __forceinline__ float load_k(const void* k, int dtype, int64_t idx) {
 }
 
 __global__ void __launch_bounds__(256) score_generic_kernel(spin_config cfg, ScoreArgs a) {
+    pdl_begin();
     const Dims dm = dims_of(cfg);
     const int req = blockIdx.y;
     const int k = blockIdx.x;
@@ -78,8 +79,7 @@ __global__ void __launch_bounds__(256) score_generic_kernel(spin_config cfg, Sco
 cudaError_t launch_score_generic(const spin_config& cfg, const ScoreArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
     dim3 grid(dm.MB, dm.R);
-    score_generic_kernel<<<grid, 256, 0, s>>>(cfg, a);
-    return cudaGetLastError();
+    return launch_pdl(score_generic_kernel, grid, dim3(256), 0, s, nullptr, 0, cfg, a);
 }
 
 }  // namespace spin

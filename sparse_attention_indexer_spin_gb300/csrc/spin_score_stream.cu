@@ -108,6 +108,7 @@ struct StreamSmemHeader {
 template <class K, int NH, int D, int W, int MAXR>
 __global__ void __launch_bounds__(StreamCfg<K, NH, D, W, MAXR>::kThreads)
 score_stream_kernel(spin_config cfg, ScoreArgs a) {
+    pdl_begin();
     using C = StreamCfg<K, NH, D, W, MAXR>;
     extern __shared__ __align__(128) unsigned char smem[];
     const Dims dm = dims_of(cfg);
@@ -327,8 +328,7 @@ static cudaError_t launch_stream_inst(const spin_config& cfg, const ScoreArgs& a
     int64_t grid = (int64_t)device_sm_count() * per_sm;
     if (grid > max_chunks) grid = max_chunks;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, C::kThreads, smem, s>>>(cfg, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(C::kThreads), smem, s, nullptr, 0, cfg, a);
 }
 
 bool score_stream_supported(const spin_config& cfg, int rows) {

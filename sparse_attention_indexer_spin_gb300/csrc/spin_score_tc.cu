@@ -276,6 +276,7 @@ template <bool FP8>
 __global__ void __launch_bounds__(kTcThreads, 1)
 score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMap kmap,
                 const __grid_constant__ CUtensorMap qmap) {
+    pdl_begin();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const Dims dm = dims_of(cfg);
@@ -784,13 +785,14 @@ cudaError_t launch_score_tc(const spin_config& cfg, const ScoreArgs& a, cudaStre
     if (fp8) {
         e = cudaFuncSetAttribute(score_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
         if (e != cudaSuccess) return e;
-        score_tc_kernel<true><<<(unsigned)grid, kTcThreads, L.total, s>>>(cfg, a, kmap, qmap);
+        return launch_pdl(score_tc_kernel<true>, dim3((unsigned)grid), dim3(kTcThreads), L.total, s, nullptr, 0,
+                          cfg, a, kmap, qmap);
     } else {
         e = cudaFuncSetAttribute(score_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
         if (e != cudaSuccess) return e;
-        score_tc_kernel<false><<<(unsigned)grid, kTcThreads, L.total, s>>>(cfg, a, kmap, qmap);
+        return launch_pdl(score_tc_kernel<false>, dim3((unsigned)grid), dim3(kTcThreads), L.total, s, nullptr, 0,
+                          cfg, a, kmap, qmap);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace spin

@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
                                                           const int32_t* __restrict__ rho_override,
                                                           uint64_t seed, uint64_t step, int layer,
                                                           float* __restrict__ S, uint32_t* __restrict__ X) {
+    pdl_begin();
     const Dims dm = dims_of(cfg);
     const int rr = blockIdx.y;
     const int req = rr / rows, r = rr - req * rows;
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
     const int32_t* __restrict__ q_pos, int rows, const int32_t* __restrict__ rho_override, uint64_t step,
     int layer, const float* __restrict__ S, int32_t* __restrict__ blocks, int32_t* __restrict__ n_blocks,
     int32_t* __restrict__ union_blocks, int32_t* __restrict__ n_union, uint32_t* status) {
+    pdl_begin();
     extern __shared__ __align__(16) unsigned char sel_smem[];
     __shared__ SelShared sh;
     const Dims dm = dims_of(cfg);
@@ -447,6 +449,7 @@ __global__ void __launch_bounds__(kSrThreads, 1) select_reg_kernel(
     int layer, const float* __restrict__ S, const uint32_t* __restrict__ X, int32_t* __restrict__ blocks,
     int32_t* __restrict__ n_blocks, int32_t* __restrict__ union_blocks, int32_t* __restrict__ n_union,
     uint32_t* status) {
+    pdl_begin();
     __shared__ SrShared sh;
     const Dims dm = dims_of(cfg);
     const int MB = dm.MB;
@@ -581,9 +584,8 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
     float* S = a.block_scores;
     uint32_t* X = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.block_scores) +
                                               select_array_bytes(cfg, a.rows));
-    block_score_kernel<<<g1, 256, 0, s>>>(cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,
-                                          a.rho_override, cfg.seed, a.step, a.layer, S, X);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(block_score_kernel, g1, dim3(256), 0, s, nullptr, 0, cfg, a.V, a.D, a.Vmax, a.warm,
+                               a.n_slots, a.q_pos, a.rows, a.rho_override, cfg.seed, a.step, a.layer, S, X);
     if (e != cudaSuccess) return e;
     if (dm.MB <= kSrMaxBlocks && a.rows >= 1 && a.rows <= 8) {
         const int kpt = dm.MB <= kSrThreads ? 1 : dm.MB <= 2 * kSrThreads ? 2 : dm.MB <= 4 * kSrThreads ? 4
@@ -592,31 +594,23 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
                      int, const float*, const uint32_t*, int32_t*, int32_t*, int32_t*, int32_t*, uint32_t*) =
             kpt == 1 ? select_reg_kernel<1> : kpt == 2 ? select_reg_kernel<2> : kpt == 4 ? select_reg_kernel<4>
             : kpt == 8 ? select_reg_kernel<8> : select_reg_kernel<16>;
-        cudaLaunchConfig_t lc = {};
-        lc.gridDim = dim3((unsigned)(dm.R * a.rows));
-        lc.blockDim = dim3(kSrThreads);
-        lc.dynamicSmemBytes = 0;
-        lc.stream = s;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
         at[0].val.clusterDim.x = (unsigned)a.rows;
         at[0].val.clusterDim.y = 1;
         at[0].val.clusterDim.z = 1;
-        lc.attrs = at;
-        lc.numAttrs = 1;
-        return cudaLaunchKernelEx(&lc, kern, cfg, a.warm, a.n_slots, a.q_pos, a.rows, a.rho_override, a.step,
-                                  a.layer, (const float*)S, (const uint32_t*)X, a.blocks, a.n_blocks,
-                                  a.union_blocks, a.n_union, a.status);
+        return launch_pdl(kern, dim3((unsigned)(dm.R * a.rows)), dim3(kSrThreads), 0, s, at, 1, cfg, a.warm,
+                          a.n_slots, a.q_pos, a.rows, a.rho_override, a.step, a.layer, (const float*)S,
+                          (const uint32_t*)X, a.blocks, a.n_blocks, a.union_blocks, a.n_union, a.status);
     }
     const size_t smem = ((size_t)dm.MB * 6 + 15) & ~(size_t)15;
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    select_kernel<<<dm.R, kSelThreads, smem, s>>>(cfg, a.warm, a.n_slots, a.q_pos, a.rows, a.rho_override,
-                                                  a.step, a.layer, a.block_scores, a.blocks, a.n_blocks,
-                                                  a.union_blocks, a.n_union, a.status);
-    return cudaGetLastError();
+    return launch_pdl(select_kernel, dim3(dm.R), dim3(kSelThreads), smem, s, nullptr, 0, cfg, a.warm, a.n_slots,
+                      a.q_pos, a.rows, a.rho_override, a.step, a.layer, (const float*)a.block_scores, a.blocks,
+                      a.n_blocks, a.union_blocks, a.n_union, a.status);
 }
 
 }  // namespace spin

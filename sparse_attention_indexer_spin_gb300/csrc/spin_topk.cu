@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 topk_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __restrict__ list,
             const int32_t* __restrict__ n_list, const int32_t* __restrict__ n_slots, int rows,
             int32_t* __restrict__ topk_idx, uint32_t* status) {
+    pdl_begin();
     __shared__ TopkShared sh;
     const Dims dm = dims_of(cfg);
     const int rr = blockIdx.x, req = rr / rows;
@@ -253,6 +254,7 @@ __global__ void __cluster_dims__(kTkCluster, 1, 1) __launch_bounds__(kTopkThread
 topk_cluster_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __restrict__ list,
                     const int32_t* __restrict__ n_list, const int32_t* __restrict__ n_slots, int rows,
                     int32_t* __restrict__ topk_idx, uint32_t* status) {
+    pdl_begin();
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ __align__(16) uint32_t keys[];
@@ -486,6 +488,7 @@ __global__ void __launch_bounds__(kTrThreads, 1)
 topk_row_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __restrict__ list,
                 const int32_t* __restrict__ n_list, const int32_t* __restrict__ n_slots, int rows,
                 int32_t* __restrict__ topk_idx, uint32_t* status) {
+    pdl_begin();
     extern __shared__ __align__(16) unsigned char tr_smem[];
     TrShared& sh = *reinterpret_cast<TrShared*>(tr_smem);
     int* slist = reinterpret_cast<int*>(tr_smem + sizeof(TrShared));  // the row's list entries
@@ -672,21 +675,18 @@ cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32
     if ((int64_t)cfg.n_req * rows >= 32 && row_smem <= 200 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)row_smem);
         if (e != cudaSuccess) return e;
-        topk_row_kernel<<<cfg.n_req * rows, kTrThreads, row_smem, s>>>(cfg, scores, list, n_list, n_slots, rows,
-                                                                       topk_idx, status);
-        return cudaGetLastError();
+        return launch_pdl(topk_row_kernel, dim3(cfg.n_req * rows), dim3(kTrThreads), row_smem, s, nullptr, 0, cfg,
+                          scores, list, n_list, n_slots, rows, topk_idx, status);
     }
     const size_t smem = topk_cluster_smem(cfg);
     if (smem + sizeof(TkClusterShared) <= 200 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        topk_cluster_kernel<<<dim3(kTkCluster, cfg.n_req * rows), kTopkThreads, smem, s>>>(
-            cfg, scores, list, n_list, n_slots, rows, topk_idx, status);
-        return cudaGetLastError();
+        return launch_pdl(topk_cluster_kernel, dim3(kTkCluster, cfg.n_req * rows), dim3(kTopkThreads), smem, s,
+                          nullptr, 0, cfg, scores, list, n_list, n_slots, rows, topk_idx, status);
     }
-    topk_kernel<<<cfg.n_req * rows, kTopkThreads, 0, s>>>(cfg, scores, list, n_list, n_slots, rows, topk_idx,
-                                                          status);
-    return cudaGetLastError();
+    return launch_pdl(topk_kernel, dim3(cfg.n_req * rows), dim3(kTopkThreads), 0, s, nullptr, 0, cfg, scores, list,
+                      n_list, n_slots, rows, topk_idx, status);
 }
 
 }  // namespace spin

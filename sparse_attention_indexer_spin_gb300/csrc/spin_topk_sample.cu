@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
 topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __restrict__ list,
                    const int32_t* __restrict__ n_list, const int32_t* __restrict__ n_slots, int rows,
                    int32_t* __restrict__ topk_idx, uint32_t* status) {
+    pdl_begin();
     extern __shared__ __align__(16) unsigned char ts_smem[];
     TsShared& sh = *reinterpret_cast<TsShared*>(ts_smem);
     const Dims dm = dims_of(cfg);
@@ -552,9 +553,8 @@ cudaError_t launch_topk_sample(const spin_config& cfg, const float* scores, cons
     const size_t smem = ts_smem_bytes(cfg);
     cudaError_t e = cudaFuncSetAttribute(topk_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    topk_sample_kernel<<<cfg.n_req * rows, kTsThreads, smem, s>>>(cfg, scores, list, n_list, n_slots, rows,
-                                                                   topk_idx, status);
-    return cudaGetLastError();
+    return launch_pdl(topk_sample_kernel, dim3(cfg.n_req * rows), dim3(kTsThreads), smem, s, nullptr, 0, cfg,
+                      scores, list, n_list, n_slots, rows, topk_idx, status);
 }
 
 }  // namespace spin
