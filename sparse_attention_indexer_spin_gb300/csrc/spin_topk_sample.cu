@@ -9,13 +9,15 @@
 //   1. a fixed sample of 1024 candidates (one per thread) brackets the K-th largest key:
 //      two order statistics of the sample, K*1024/C -/+ four standard deviations, found by
 //      8-bit radix passes over the sample in registers;
-//      (the collected keys share the leading bytes of the bracket's ends, so their radix
-//      passes start at the first byte where the ends differ)
-//   2. one pass over every candidate (a warp reads 128 consecutive scores per float4 load)
-//      writes the keys above the bracket straight into a bitmap of the candidates (ballot
-//      and shuffle, no atomics) and collects the keys inside the bracket (typically 1-5 % of
-//      the candidates) into shared memory; the comparisons are made on the scores, and the
-//      number of live candidates comes from the list;
+//      (the collected keys share the leading bytes of the bracket's lower end and their
+//      maximum, so their radix passes start at the first byte where those differ, and stop
+//      once the threshold bin is kept whole)
+//   2. one pass over every candidate (a warp reads 128 consecutive scores per float4 load,
+//      several loads in flight per thread) writes the keys above the bracket straight into a
+//      bitmap of the candidates (shuffles, no atomics) and collects the keys inside the
+//      bracket (typically 1-5 % of the candidates) into per-warp segments of shared memory
+//      (ballot offsets, no atomics); the comparisons are made on the scores, and the number
+//      of live candidates comes from the list;
 //   3. if the K-th key is inside the bracket, radix passes over the collected keys give
 //      the exact threshold T and the number of keys equal to T to keep; otherwise (a
 //      sample that missed, or a bracket holding too many keys, e.g. when all scores tie)
@@ -31,27 +33,24 @@ namespace spin {
 constexpr int kTsThreads = 1024;
 constexpr int kTsWarps = kTsThreads / 32;
 constexpr int kTsSample = kTsThreads;  // one sampled candidate per thread
-constexpr int kTsMid = 8192;           // capacity of the collected in-bracket keys
+constexpr int kTsMid = 16384;          // capacity of the collected in-bracket keys
 constexpr int kTsMidKpt = kTsMid / kTsThreads;
-constexpr int kTsNst = 4;                     // score ring stages
-constexpr int kTsStageFloats = 32 * 32 * 4;   // a stage = 32 chunks of 128 candidates (16 KB)
-constexpr int kTsStageBytes = kTsStageFloats * 4;
+constexpr int kTsRun = 64;                     // entries a warp claims at least at a time
+constexpr int kTsLoads = 4;                    // float4 loads in flight per thread
 
 struct TsShared {
     __align__(16) int hist[6][256];  // radix histograms: 3 rotating buffers x 2 targets
-    int red[kTsWarps][4];  // block sums, one slot per use (no barrier needed between uses)
+    int red[kTsWarps][5];  // block sums, one slot per use (no barrier needed between uses)
+    uint32_t redu[kTsWarps];  // block maximum
+    int npool;                // entries of the collection claimed by the warps' runs
     int scan[33];
-    int nmid;
     int bad_list;
-    int abort_flag;
-    uint64_t full[kTsNst], empty[kTsNst];
 };
 
 __host__ __device__ inline size_t ts_smem_bytes(const spin_config& cfg) {
     const int64_t MB = ((int64_t)cfg.max_slots + kBlock - 1) / kBlock;
-    // TsShared | list[MB] | bitmap[2 MB] | eqmap[2 MB] | midkey[kTsMid] | midpos[kTsMid] | ring
-    const size_t b = ((sizeof(TsShared) + 15) & ~(size_t)15) + (size_t)MB * 4 + (size_t)MB * 8 * 2 + (size_t)kTsMid * 8;
-    return ((b + 127) & ~(size_t)127) + (size_t)kTsNst * kTsStageBytes;
+    // TsShared | list[MB] | bitmap[2 MB] | eqmap[2 MB] | midkey[kTsMid] | midpos[kTsMid]
+    return ((sizeof(TsShared) + 15) & ~(size_t)15) + (size_t)MB * 4 + (size_t)MB * 8 * 2 + (size_t)kTsMid * 8;
 }
 
 // The float whose order key is `key` (inverse of order_key for keys of finite floats).
@@ -112,7 +111,9 @@ __device__ __forceinline__ void ts_clear_ahead(TsShared& sh, int pass) {
 // its value T[t] and the number of eligible keys above it.  All threads call it; on entry
 // the buffers of passes `pass` and `pass + 1` are zero, and so are they on return.
 // The first `d0` bytes of every eligible key are known to equal those of `common`; those
-// digit passes are skipped.
+// digit passes are skipped.  With one target and all four digits asked for, the passes stop
+// once the threshold bin is taken whole: T is then one below the bin's lowest key, with
+// every eligible key above it counted and none equal to it.
 // Only the key slots i < nslot (CTA-uniform) are looked at, and only the digits d0 .. d1-1;
 // with d1 < 4 the results are the order statistics' leading 8*d1 bits (the rest zero) and
 // `above` counts the eligible keys in higher 8*d1-bit bins.
@@ -139,15 +140,23 @@ __device__ void ts_kth_regs(const uint32_t (&key)[KPT], uint32_t elig, const int
             if (NT == 2 && !shared_prefix) ts_hist_add(h1, e && (key[i] & mask) == prefix[NT - 1] ? dg : -1);
         }
         __syncthreads();
+        int nbin0 = 0;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             int dg, ab, nb;
             ts_digit(t == 0 || shared_prefix ? h0 : h1, kk[t], dg, ab, nb);
             prefix[t] |= (uint32_t)dg << shift;
             kk[t] -= ab;
+            if (t == 0) nbin0 = nb;
         }
         ts_clear_ahead(sh, pass);
         mask |= 0xFFu << shift;
+        if (NT == 1 && d1 == 4 && d < 3 && kk[0] == nbin0 && prefix[0] != 0u) {
+            ++pass;
+            T[0] = prefix[0] - 1u;
+            above[0] = k[0];
+            return;
+        }
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) { T[t] = prefix[t]; above[t] = k[t] - kk[t]; }
@@ -215,6 +224,115 @@ __device__ __forceinline__ int ts_block_sum(int v, TsShared& sh, int slot) {
     return s;
 }
 
+// One warp's appends to the collection: keys collected, its current run [fill, end) (all
+// warp-uniform) and the largest key this thread collected.
+struct TsCollect {
+    int wcnt, wfill, wend;
+    uint32_t kmax;
+};
+
+// Step 2, the pass over every candidate.  Each warp takes 32 consecutive float4 (128
+// candidates) per step, with kTsLoads steps' loads in flight per thread, and appends its
+// in-bracket keys to a run of the collection that it claimed (at least kTsRun entries, one
+// shared atomic per claim) at offsets from ballots.  A run given up for a new one has its
+// unused entries set to key 0, which no live candidate has, so the collection is the
+// claimed prefix with holes of key 0.  HI: the bracket has an upper end, and the keys
+// above it are written to the bitmap here; without one nothing is above the bracket.
+// Returns this thread's count of keys above the bracket.
+template <bool HI>
+__device__ __forceinline__ int ts_main_pass(const TsCands& cs, float z_lo, float z_hi, int Cw, uint32_t* bitmap,
+                                            uint32_t* midkey, int* midpos, TsShared& sh, TsCollect& col) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const int C4 = cs.C4;
+    int gt = 0;
+    for (int base = 0; base < C4; base += kTsThreads * kTsLoads) {
+        float4 zv[kTsLoads];
+#pragma unroll
+        for (int u = 0; u < kTsLoads; ++u) {
+            const int f4 = base + u * kTsThreads + tid;
+            zv[u] = f4 < C4 ? __ldg(cs.sc4 + f4) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < kTsLoads; ++u) {
+            const int f4 = base + u * kTsThreads + tid;
+            const int ch = f4 >> 5;  // the warp's chunk of 32 float4 (warp-uniform)
+            if (32 * ch >= C4) continue;
+            // live candidates of this float4: slot < N in a valid block
+            int lim = 0;
+            if (f4 < C4) {
+                const int c = 4 * f4;
+                const int blk = cs.slist[c >> 6];
+                if (blk >= 0 && blk < cs.nb) {
+                    const int64_t room = cs.n - (int64_t)blk * kBlock - (c & 63);
+                    lim = room >= 4 ? 4 : (int)max(room, (int64_t)0);
+                }
+            }
+            const float zz[4] = {zv[u].x, zv[u].y, zv[u].z, zv[u].w};
+            uint32_t in = 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                in |= (uint32_t)(e < lim && zz[e] >= z_lo && (!HI || zz[e] <= z_hi)) << e;
+            if (HI) {
+                uint32_t nib = 0u;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) nib |= (uint32_t)(e < lim && zz[e] > z_hi) << e;
+                gt += __popc(nib);
+                uint32_t wbits = nib << (4 * (lane & 7));
+                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 1);
+                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 2);
+                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 4);
+                if ((lane & 7) == 0 && ch * 4 + (lane >> 3) < Cw) bitmap[ch * 4 + (lane >> 3)] = wbits;
+            }
+            if (__any_sync(0xffffffffu, in != 0u)) {
+                unsigned bal[4];
+                int t = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    bal[e] = __ballot_sync(0xffffffffu, (in >> e) & 1u);
+                    t += __popc(bal[e]);
+                }
+                if (col.wfill + t > col.wend) {
+                    for (int q = col.wfill + lane; q < min(col.wend, kTsMid); q += 32) midkey[q] = 0u;
+                    const int claim = max(kTsRun, (t + 31) & ~31);
+                    int b0 = 0;
+                    if (lane == 0) b0 = atomicAdd(&sh.npool, claim);
+                    col.wfill = __shfl_sync(0xffffffffu, b0, 0);
+                    col.wend = col.wfill + claim;
+                }
+                int off = col.wfill;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if ((in >> e) & 1u) {
+                        const int p = off + __popc(bal[e] & lt);
+                        const uint32_t kx = order_key(zz[e]);
+                        col.kmax = max(col.kmax, kx);
+                        if (p < kTsMid) { midkey[p] = kx; midpos[p] = 4 * f4 + e; }
+                    }
+                    off += __popc(bal[e]);
+                }
+                col.wfill = off;
+                col.wcnt += t;
+            }
+        }
+    }
+    for (int q = col.wfill + lane; q < min(col.wend, kTsMid); q += 32) midkey[q] = 0u;
+    return gt;
+}
+
+// Maximum of v over the CTA (all threads call it).
+__device__ __forceinline__ uint32_t ts_block_max(uint32_t v, TsShared& sh) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (lane == 0) sh.redu[wid] = v;
+    __syncthreads();
+    uint32_t m = sh.redu[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return m;
+}
+
 __global__ void __launch_bounds__(kTsThreads, 1)
 topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __restrict__ list,
                    const int32_t* __restrict__ n_list, const int32_t* __restrict__ n_slots, int rows,
@@ -229,11 +347,9 @@ topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int3
     uint32_t* eqmap = bitmap + 2 * (size_t)MB;
     uint32_t* midkey = eqmap + 2 * (size_t)MB;
     int* midpos = reinterpret_cast<int*>(midkey + kTsMid);
-    float4* ring = reinterpret_cast<float4*>(
-        ts_smem + ((((unsigned char*)(midpos + kTsMid) - ts_smem) + 127) & ~(size_t)127));
 
     const int rr = blockIdx.x, req = rr / rows;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int K = cfg.top_k;
     int32_t* out = topk_idx + (int64_t)rr * K;
     const int64_t n = n_slots[req];
@@ -249,21 +365,6 @@ topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int3
     const int Cw = C / 32;
     TsCands cs{reinterpret_cast<const float4*>(sc), slist, n, (n + kBlock - 1) / kBlock, C / 4};
 
-    // the scores stream through a ring of kTsNst stages by the bulk-copy engine; thread 0
-    // starts it now, so the copies run during the sampling below
-    const int nstage = (C + kTsStageFloats - 1) / kTsStageFloats;
-    auto stage_bytes = [&](int it) { return (uint32_t)(min(C - it * kTsStageFloats, kTsStageFloats) * 4); };
-    if (tid == 0) {
-        for (int st = 0; st < kTsNst; ++st) { mbar_init(&sh.full[st], 1); mbar_init(&sh.empty[st], kTsWarps); }
-        sh.abort_flag = 0;
-        fence_barrier_init();
-        for (int it = 0; it < nstage && it < kTsNst; ++it) {
-            mbar_arrive_expect_tx(&sh.full[it], stage_bytes(it));
-            bulk_g2s(ring + (size_t)it * (kTsStageFloats / 4), sc + (size_t)it * kTsStageFloats, stage_bytes(it),
-                     &sh.full[it]);
-        }
-    }
-
     // sampled candidate of this thread (read straight from global memory while the list is
     // being staged)
     uint32_t skey = 0u;
@@ -277,7 +378,7 @@ topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int3
     for (int i = tid; i < cnt; i += kTsThreads) slist[i] = lst[i];
     if (tid < 512) (&sh.hist[0][0])[tid] = 0;
     if (tid < 1024) (&sh.hist[0][0])[512 + tid] = 0;
-    if (tid == 0) { sh.nmid = 0; sh.bad_list = 0; }
+    if (tid == 0) { sh.bad_list = 0; sh.npool = 0; }
     int pass = 0;
 
     // 1. the bracket [key_lo, key_hi] of the K-th largest key
@@ -307,87 +408,16 @@ topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int3
     // (keys at or beyond those of +inf and -inf mean no bound on that side)
     const float z_hi = key_hi >= 0xFF800000u ? __int_as_float(0x7f800000) : key_to_float(key_hi);
     const float z_lo = key_lo <= 0x007FFFFFu ? __int_as_float(0xff800000) : key_to_float(key_lo);
-    int gt = 0;
-    {
-        const int nch = (cs.C4 + 31) / 32;  // chunks of 32 float4 = 128 candidates
-        int issued = min(nstage, kTsNst);  // (thread 0's count of stages whose copy was issued)
-        for (int it = 0; it < nstage; ++it) {
-            const int st = it % kTsNst;
-            const uint32_t ph = (uint32_t)(it / kTsNst) & 1u;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&sh.full[st], ph, &sh.abort_flag) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) {
-                if (lane == 0) {
-                    sh.abort_flag = 1;
-                    set_status(status, SPIN_STATUS_TIMEOUT);
-                }
-                break;
-            }
-            const int ch = it * 32 + wid;
-            if (ch < nch) {
-                const int f4 = ch * 32 + lane;
-                const float4 zv = ring[(size_t)st * (kTsStageFloats / 4) + wid * 32 + lane];
-                // live candidates of this float4: slot < N in a valid block
-                int lim = 0;
-                if (f4 < cs.C4) {
-                    const int c = 4 * f4;
-                    const int blk = slist[c >> 6];
-                    if (blk >= 0 && blk < cs.nb) {
-                        const int64_t room = cs.n - (int64_t)blk * kBlock - (c & 63);
-                        lim = room >= 4 ? 4 : (int)max(room, (int64_t)0);
-                    }
-                }
-                const float zz[4] = {zv.x, zv.y, zv.z, zv.w};
-                uint32_t nib = 0u, in = 0u;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const bool lv = e < lim;
-                    nib |= (uint32_t)(lv && zz[e] > z_hi) << e;
-                    in |= (uint32_t)(lv && zz[e] >= z_lo && zz[e] <= z_hi) << e;
-                }
-                gt += __popc(nib);
-                uint32_t wbits = nib << (4 * (lane & 7));
-                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 1);
-                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 2);
-                wbits |= __shfl_xor_sync(0xffffffffu, wbits, 4);
-                if ((lane & 7) == 0 && ch * 4 + (lane >> 3) < Cw) bitmap[ch * 4 + (lane >> 3)] = wbits;
-                if (in) {
-                    int p = atomicAdd(&sh.nmid, __popc(in));
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if ((in >> e) & 1u) {
-                            if (p < kTsMid) { midkey[p] = order_key(zz[e]); midpos[p] = 4 * f4 + e; }
-                            ++p;
-                        }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[st]);
-            // thread 0 refills the stage once every warp is done with it
-            if (tid == 0 && it + kTsNst < nstage) {
-                if (!mbar_wait(&sh.empty[st], ph, &sh.abort_flag)) {
-                    sh.abort_flag = 1;
-                    set_status(status, SPIN_STATUS_TIMEOUT);
-                } else {
-                    const int nx = it + kTsNst;
-                    mbar_arrive_expect_tx(&sh.full[st], stage_bytes(nx));
-                    bulk_g2s(ring + (size_t)st * (kTsStageFloats / 4), sc + (size_t)nx * kTsStageFloats,
-                             stage_bytes(nx), &sh.full[st]);
-                    ++issued;
-                }
-            }
-        }
-        // after a timeout: no copy may still be landing when the shared memory is reused.  A
-        // stage's earlier copies completed before its later one was issued, so waiting for
-        // the last copy issued into each stage covers them all.
-        if (tid == 0 && sh.abort_flag) {
-            for (int st = 0; st < kTsNst && st < issued; ++st) {
-                const int last = st + kTsNst * ((issued - 1 - st) / kTsNst);
-                (void)mbar_wait(&sh.full[st], (uint32_t)(last / kTsNst) & 1u, nullptr);
-            }
-        }
+    TsCollect col{0, 0, 0, 0u};
+    int gt;
+    if (key_hi >= 0xFF800000u) {  // no upper end: nothing is above the bracket
+        for (int w = tid; w < Cw; w += kTsThreads) bitmap[w] = 0u;
+        gt = ts_main_pass<false>(cs, z_lo, z_hi, Cw, bitmap, midkey, midpos, sh, col);
+    } else {
+        gt = ts_main_pass<true>(cs, z_lo, z_hi, Cw, bitmap, midkey, midpos, sh, col);
     }
+    const int wcnt = col.wcnt;
+    const uint32_t kmax = col.kmax;
     // live candidates, from the list alone (a listed block outside the context is an error)
     int live = 0;
     bool bad_list = false;
@@ -397,9 +427,10 @@ topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int3
         else bad_list = true;
     }
     if (bad_list) sh.bad_list = 1;
-    gt = ts_block_sum(gt, sh, 1);
+    gt = ts_block_sum(gt, sh, 1);  // (its barrier also publishes the collection)
     const int nvalid = ts_block_sum(live, sh, 2);
-    const int nmid = sh.nmid;
+    const int nmid = ts_block_sum(lane == 0 ? wcnt : 0, sh, 4);
+    const int npool = sh.npool;
     if (tid == 0 && sh.bad_list && rr % rows == 0) set_status(status, SPIN_STATUS_BAD_LIST);
 
     // 3. the exact threshold: keys > T are kept and the first `take_eq` keys == T
@@ -416,22 +447,23 @@ topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int3
             }
             bitmap[w] = bits;
         }
-    } else if (gt < K && gt + nmid >= K && nmid <= kTsMid) {
+    } else if (gt < K && gt + nmid >= K && npool <= kTsMid) {
         uint32_t mk[kTsMidKpt];
         uint32_t elig = 0;
 #pragma unroll
         for (int i = 0; i < kTsMidKpt; ++i) {
             const int p = i * kTsThreads + tid;
-            mk[i] = p < nmid ? midkey[p] : 0u;
-            elig |= (uint32_t)(p < nmid) << i;
+            mk[i] = p < npool ? midkey[p] : 0u;
+            elig |= (uint32_t)(mk[i] != 0u) << i;
         }
         const int k1[1] = {K - gt};
         uint32_t T1[1];
         int ab1[1];
-        // every collected key lies in [key_lo, key_hi]: their common leading bytes are known
-        const uint32_t diff = key_lo ^ key_hi;
+        // every collected key lies in [key_lo, max]: their common leading bytes are known
+        const uint32_t kmx = ts_block_max(kmax, sh);
+        const uint32_t diff = key_lo ^ kmx;
         const int d0 = diff == 0u ? 3 : min(3, __clz(diff) / 8);
-        ts_kth_regs<kTsMidKpt, 1>(mk, elig, k1, T1, ab1, sh, pass, d0, key_hi, (nmid + kTsThreads - 1) / kTsThreads);
+        ts_kth_regs<kTsMidKpt, 1>(mk, elig, k1, T1, ab1, sh, pass, d0, kmx, (npool + kTsThreads - 1) / kTsThreads);
         const uint32_t T = T1[0];
         const int take_eq = K - gt - ab1[0];
         int neq = 0;
@@ -445,8 +477,7 @@ topk_sample_kernel(spin_config cfg, const float* __restrict__ scores, const int3
 #pragma unroll
         for (int i = 0; i < kTsMidKpt; ++i) {
             if (!((elig >> i) & 1u)) continue;
-            const int p = i * kTsThreads + tid;
-            const int c = midpos[p];
+            const int c = midpos[i * kTsThreads + tid];
             if (mk[i] > T || (mk[i] == T && !eq_cut)) atomicOr(&bitmap[c >> 5], 1u << (c & 31));
             else if (mk[i] == T) atomicOr(&eqmap[c >> 5], 1u << (c & 31));
         }
