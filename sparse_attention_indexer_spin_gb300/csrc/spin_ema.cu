@@ -151,10 +151,11 @@ __global__ void __launch_bounds__(kEmaThreads) ema_replay_kernel(spin_config cfg
 // ---------------------------------------------------------------------------------------
 // One-row update (a = 0): each listed slot i is updated once and its offset q - i is
 // distinct, so the work splits by list entry with no ordering between threads.  A warp
-// owns two list entries (128 slots), issues all their loads together, and refreshes the
-// two blocks' Vmax with a warp max.
+// takes two list entries (128 slots) per step, issues all their loads together, and
+// refreshes the two blocks' Vmax with a warp max; the warps of a request's CTAs stride
+// over its list, each reading the next step's list entries before this step's slots.
 // ---------------------------------------------------------------------------------------
-constexpr int kEmaListEntries = 16;  // per CTA of 8 warps
+constexpr int kEmaListWarps = 8;  // warps per CTA
 
 __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs a) {
     pdl_begin();
@@ -175,50 +176,61 @@ __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs 
     float* Dq = a.D + (int64_t)req * dm.DL;
     const int32_t* lst = a.list + (int64_t)req * dm.MB;
     const float* zq = a.scores + (int64_t)req * dm.MB * kBlock;
-    const int64_t k0 = (int64_t)blockIdx.x * kEmaListEntries + 2 * wid;
-    int64_t blk[2];
-    bool ok[2];
-    float z[2][2], v[2][2], d[2][2];
+    const int64_t stride = 2 * (int64_t)gridDim.x * kEmaListWarps;
+    int64_t k0 = 2 * ((int64_t)blockIdx.x * kEmaListWarps + wid);
+    int64_t nxt[2];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int64_t k = k0 + e;
-        blk[e] = k < cnt ? lst[k] : -1;
-        ok[e] = blk[e] >= 0 && blk[e] < nb;
-        if (k < cnt && !ok[e] && lane == 0) set_status(a.status, SPIN_STATUS_BAD_LIST);
+    for (int e = 0; e < 2; ++e) nxt[e] = k0 + e < cnt ? lst[k0 + e] : -1;
+    for (; k0 < cnt; k0 += stride) {
+        int64_t blk[2];
+        bool ok[2];
+        float z[2][2], v[2][2], d[2][2];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int64_t i = blk[e] * kBlock + lane + 32 * hh;
-            const bool live = ok[e] && i < n;
-            z[e][hh] = live ? zq[k * kBlock + lane + 32 * hh] : 0.0f;
-            v[e][hh] = (ok[e] && i < dm.max_slots) ? Vq[i] : 0.0f;
-            d[e][hh] = live ? Dq[q - i] : 0.0f;
-        }
-    }
+        for (int e = 0; e < 2; ++e) {
+            const int64_t k = k0 + e;
+            blk[e] = nxt[e];
+            ok[e] = blk[e] >= 0 && blk[e] < nb;
+            if (k < cnt && !ok[e] && lane == 0) set_status(a.status, SPIN_STATUS_BAD_LIST);
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        if (!ok[e]) continue;  // warp-uniform
-        float m = -FLT_MAX;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int64_t i = blk[e] * kBlock + lane + 32 * hh;
-            if (i < n) {
-                const float t = __fmul_rn(oma, z[e][hh]);
-                v[e][hh] = __fmaf_rn(alpha, v[e][hh], t);
-                Vq[i] = v[e][hh];
-                Dq[q - i] = __fmaf_rn(alpha, d[e][hh], t);
+            for (int hh = 0; hh < 2; ++hh) {
+                const int64_t i = blk[e] * kBlock + lane + 32 * hh;
+                const bool live = ok[e] && i < n;
+                z[e][hh] = live ? zq[k * kBlock + lane + 32 * hh] : 0.0f;
+                v[e][hh] = (ok[e] && i < dm.max_slots) ? Vq[i] : 0.0f;
+                d[e][hh] = live ? Dq[q - i] : 0.0f;
             }
-            if (i < dm.max_slots) m = fmaxf(m, v[e][hh]);
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) a.Vmax[(int64_t)req * dm.MB + blk[e]] = m;
+        for (int e = 0; e < 2; ++e) nxt[e] = k0 + stride + e < cnt ? lst[k0 + stride + e] : -1;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            if (!ok[e]) continue;  // warp-uniform
+            float m = -FLT_MAX;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int64_t i = blk[e] * kBlock + lane + 32 * hh;
+                if (i < n) {
+                    const float t = __fmul_rn(oma, z[e][hh]);
+                    v[e][hh] = __fmaf_rn(alpha, v[e][hh], t);
+                    Vq[i] = v[e][hh];
+                    Dq[q - i] = __fmaf_rn(alpha, d[e][hh], t);
+                }
+                if (i < dm.max_slots) m = fmaxf(m, v[e][hh]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) a.Vmax[(int64_t)req * dm.MB + blk[e]] = m;
+        }
     }
 }
 
 cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
     if (a.accepted == nullptr && a.rows == 1) {
-        dim3 grid((dm.MB + kEmaListEntries - 1) / kEmaListEntries, dm.R);
+        // about eight CTAs per SM over all requests, at most one step per warp for the longest list
+        const int full = (dm.MB + 2 * kEmaListWarps - 1) / (2 * kEmaListWarps);
+        const int want = (device_sm_count() * 8 + dm.R - 1) / dm.R;
+        dim3 grid(want < full ? (want > 0 ? want : 1) : full, dm.R);
         return launch_pdl(ema_list_kernel, grid, dim3(256), 0, s, nullptr, 0, cfg, a);
     }
     const int gx = (dm.max_slots + kEmaSpan - 1) / kEmaSpan;
