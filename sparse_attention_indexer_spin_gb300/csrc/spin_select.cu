@@ -28,7 +28,6 @@ namespace spin {
 // block equals max(Vmax[j], max_i D[q-i]), so V is read only through its per-block max.
 // The additive reading needs V[i] + D[q-i] slot by slot.
 // ---------------------------------------------------------------------------------------
-constexpr int kBsBlocksPerWarp = 8;
 
 // Block budget m_t (Algorithm 1's budget step) with rho in basis points.
 __device__ __forceinline__ int64_t budget_blocks(int64_t nb, int64_t top_k, int32_t rho_bp) {
@@ -39,6 +38,9 @@ __device__ __forceinline__ int64_t budget_blocks(int64_t nb, int64_t top_k, int3
 }
 
 
+// BPW blocks per warp, all their loads issued before the first use: more loads in flight
+// per warp pay when many request rows keep every SM busy; few rows want more CTAs instead.
+template <int BPW>
 __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const float* __restrict__ V,
                                                           const float* __restrict__ D,
                                                           const float* __restrict__ Vmax,
@@ -66,19 +68,19 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
     float* Sq = S + (int64_t)rr * dm.MB;
     uint32_t* Xq = X + (int64_t)rr * dm.MB;
     const bool sum = cfg.combine == SPIN_COMBINE_SUM;
-    // each warp owns kBsBlocksPerWarp consecutive blocks and issues all their loads first
-    for (int64_t j0 = ((int64_t)blockIdx.x * nw + wid) * kBsBlocksPerWarp; j0 < nb;
-         j0 += (int64_t)gridDim.x * nw * kBsBlocksPerWarp) {
-        float lo[kBsBlocksPerWarp], hi[kBsBlocksPerWarp];
+    // each warp owns BPW consecutive blocks and issues all their loads first
+    for (int64_t j0 = ((int64_t)blockIdx.x * nw + wid) * BPW; j0 < nb;
+         j0 += (int64_t)gridDim.x * nw * BPW) {
+        float lo[BPW], hi[BPW];
 #pragma unroll
-        for (int b = 0; b < kBsBlocksPerWarp; ++b) {
+        for (int b = 0; b < BPW; ++b) {
             const int64_t i0 = (j0 + b) * kBlock + lane, i1 = i0 + 32;
             lo[b] = i0 < n ? (sum ? __fadd_rn(Vq[i0], Dq[qr - i0]) : Dq[qr - i0]) : -FLT_MAX;
             hi[b] = i1 < n ? (sum ? __fadd_rn(Vq[i1], Dq[qr - i1]) : Dq[qr - i1]) : -FLT_MAX;
         }
-        const float vm = (!sum && lane < kBsBlocksPerWarp && j0 + lane < nb) ? Vm[j0 + lane] : -FLT_MAX;
+        const float vm = (!sum && lane < BPW && j0 + lane < nb) ? Vm[j0 + lane] : -FLT_MAX;
 #pragma unroll
-        for (int b = 0; b < kBsBlocksPerWarp; ++b) {
+        for (int b = 0; b < BPW; ++b) {
             // every block of the loop has at least one slot < N, so the max is a real value
             float m = fmaxf(lo[b], hi[b]);
 #pragma unroll
@@ -577,15 +579,17 @@ size_t select_workspace_bytes(const spin_config& cfg, int rows) { return 2 * sel
 
 cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
-    const int per_cta = (256 / 32) * kBsBlocksPerWarp;
+    const bool many_rows = (int64_t)dm.R * a.rows >= 8;
+    const int per_cta = (256 / 32) * (many_rows ? 16 : 8);
     int gx = (dm.MB + per_cta - 1) / per_cta;
     if (gx > 512) gx = 512;
     dim3 g1(gx, dm.R * a.rows);
     float* S = a.block_scores;
     uint32_t* X = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.block_scores) +
                                               select_array_bytes(cfg, a.rows));
-    cudaError_t e = launch_pdl(block_score_kernel, g1, dim3(256), 0, s, nullptr, 0, cfg, a.V, a.D, a.Vmax, a.warm,
-                               a.n_slots, a.q_pos, a.rows, a.rho_override, cfg.seed, a.step, a.layer, S, X);
+    cudaError_t e = launch_pdl(many_rows ? block_score_kernel<16> : block_score_kernel<8>, g1, dim3(256), 0, s,
+                               nullptr, 0, cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,
+                               a.rho_override, cfg.seed, a.step, a.layer, S, X);
     if (e != cudaSuccess) return e;
     if (dm.MB <= kSrMaxBlocks && a.rows >= 1 && a.rows <= 8) {
         const int kpt = dm.MB <= kSrThreads ? 1 : dm.MB <= 2 * kSrThreads ? 2 : dm.MB <= 4 * kSrThreads ? 4
