@@ -79,6 +79,19 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
             hi[b] = i1 < n ? (sum ? __fadd_rn(Vq[i1], Dq[qr - i1]) : Dq[qr - i1]) : -FLT_MAX;
         }
         const float vm = (!sum && lane < BPW && j0 + lane < nb) ? Vm[j0 + lane] : -FLT_MAX;
+        // the exploration draws of these blocks (used only for blocks that end up
+        // unselected), computed while the loads are in flight: lane l < BPW / 8 computes
+        // one Philox output, the draws of the 8 blocks of group j0 / 8 + l
+        if (lane < BPW / 8) {
+            const int64_t g = j0 / 8 + lane;
+            if (g * 8 < nb) {
+                uint32_t k8[8];
+                explore_keys8(seed, layer, step, r, req, g, k8);
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                    if (g * 8 + h < nb) Xq[g * 8 + h] = k8[h];
+            }
+        }
 #pragma unroll
         for (int b = 0; b < BPW; ++b) {
             // every block of the loop has at least one slot < N, so the max is a real value
@@ -88,17 +101,6 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
             const float vmb = __shfl_sync(0xffffffffu, vm, b);
             if (lane == 0 && j0 + b < nb) Sq[j0 + b] = sum ? m : fmaxf(vmb, m);
         }
-    }
-    // the exploration draws (used only for blocks that end up unselected), off the
-    // selection's serial path: a lane computes one Philox output, the draws of 8 blocks
-    // (groups interleaved over the CTAs: a short list needs few of them)
-    for (int64_t g = (int64_t)threadIdx.x * gridDim.x + blockIdx.x; g * 8 < nb;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        uint32_t k8[8];
-        explore_keys8(seed, layer, step, r, req, g, k8);
-#pragma unroll
-        for (int h = 0; h < 8; ++h)
-            if (g * 8 + h < nb) Xq[g * 8 + h] = k8[h];
     }
 }
 
