@@ -280,3 +280,49 @@ def raw_numpy(t: torch.Tensor):
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
     return t.numpy()
+
+
+TOPK_DISTS = ("normal", "ties", "narrow", "equal")
+
+
+def topk_inputs(n_req: int, max_slots: int, rows: int, dist: str, seed: int, fill: float = 0.6):
+    """Seeded inputs of a stand-alone top-K call (host numpy arrays):
+
+    - n_slots: per request a context of max_slots/2 .. max_slots slots;
+    - blist / n_list: an ascending list of a `fill` share of the context's blocks (the first
+      and the last always listed);
+    - scores [n_req][rows][MB*64]: the listed slots in list order, drawn from `dist`:
+      'normal' (N(0, 1)), 'ties' (integers 0..15), 'narrow' (1 + 2^-12 * U[0, 1), many
+      shared leading bits), 'equal' (all 0.5).  Slots at or beyond the context's end and
+      entries past the list get 1e30, which no correct top-K may return.
+    """
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    MB = (max_slots + 63) // 64
+    n_slots = rng.integers(max_slots // 2, max_slots + 1, n_req).astype(np.int32)
+    blist = np.full((n_req, MB), -1, np.int32)
+    n_list = np.zeros(n_req, np.int32)
+    scores = np.full((n_req, rows, MB * 64), 1e30, np.float32)
+    for r in range(n_req):
+        nb = (int(n_slots[r]) + 63) // 64
+        k = max(1, min(nb, int(fill * nb)))
+        pick = set(rng.choice(nb, k, replace=False).tolist()) | {0, nb - 1}
+        lst = np.array(sorted(pick), np.int32)
+        blist[r, : len(lst)] = lst
+        n_list[r] = len(lst)
+        C = len(lst) * 64
+        slot = (lst[:, None].astype(np.int64) * 64 + np.arange(64)[None, :]).ravel()
+        for row in range(rows):
+            if dist == "normal":
+                z = rng.standard_normal(C).astype(np.float32)
+            elif dist == "ties":
+                z = rng.integers(0, 16, C).astype(np.float32)
+            elif dist == "narrow":
+                z = (1.0 + rng.random(C) / 4096.0).astype(np.float32)
+            elif dist == "equal":
+                z = np.full(C, 0.5, np.float32)
+            else:
+                raise ValueError(dist)
+            z[slot >= n_slots[r]] = 1e30
+            scores[r, row, :C] = z
+    return scores, blist, n_list, n_slots
