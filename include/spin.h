@@ -6,8 +6,9 @@
  * Per request, per layer and per decode step the library
  *   1. predicts each 64-slot KV block's importance from two EMAs of past indexer scores
  *      (Eq. 1, Eq. 2) and selects the layer's block budget: forced sink and newest
- *      blocks, the top-ranked blocks and a random exploration share (Algorithm 1 lines
- *      1-5, §3.2 practical details, §3.2.1)               -> spin_select_blocks
+ *      blocks, the top-ranked blocks and a random exploration share (Algorithm 1's
+ *      budget, prediction and selection steps, §3.2 practical details, §3.2.1)
+ *                                                          -> spin_select_blocks
  *   2. runs the indexer z[i] = sum_h w_h ReLU(q_h . k_{i,h}) over the slots of the
  *      selected blocks only, read through a paged block table (§2, Algorithm 1's scoring step)
  *                                                          -> spin_indexer_score
@@ -24,6 +25,10 @@
  *     scratch array of spin_select_blocks_noalloc, see there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream): the host validates the configuration and sizes, then enqueues kernels.
+ *     Kernels are launched with programmatic dependent launch allowed (PTX ISA:
+ *     griddepcontrol): one may be scheduled while the previous kernel on the stream
+ *     still runs, but it reads and writes memory only after that kernel has completed,
+ *     so stream order holds exactly as for plain launches.
  *   - Host-side validation failures return an error code and enqueue nothing; the
  *     message is available from spin_last_error_string() (thread-local).
  *   - Values the host cannot see (N, q, block ids, page ids, accepted counts) are
