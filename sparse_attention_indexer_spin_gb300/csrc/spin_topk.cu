@@ -679,7 +679,8 @@ cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32
                           scores, list, n_list, n_slots, rows, topk_idx, status);
     }
     const size_t smem = topk_cluster_smem(cfg);
-    if (smem + sizeof(TkClusterShared) <= 200 * 1024) {
+    // (a slice's gt and eq counts share one 32-bit scan word: fewer than 2^16 keys each)
+    if (smem + sizeof(TkClusterShared) <= 200 * 1024 && kTkSliceKeys(cfg) < 65536) {
         cudaError_t e = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         return launch_pdl(topk_cluster_kernel, dim3(kTkCluster, cfg.n_req * rows), dim3(kTopkThreads), smem, s,
