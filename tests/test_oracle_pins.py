@@ -203,8 +203,24 @@ def _random_state(o, cfg, rng, warm=1):
     return V, D, np.full(cfg.n_req, warm, dtype=np.int32)
 
 
-def _check_selection(o, cfg, V, D, n, q, sel, rho_bp, row=0):
-    """Invariants of §3.2 / §3.2.1 against an independent numpy ranking."""
+def _numpy_explore_keys(seed, layer, step, row, req, js):
+    """Exploration draws from numpy's own Philox4x64-10: block j takes 32-bit half j % 8
+    (word by word, high half first) of the output for counter (step, row, req, j // 8)
+    under key (seed, layer)."""
+    cache, out = {}, []
+    for j in js:
+        m = int(j) // 8
+        if m not in cache:
+            cache[m] = _numpy_philox([step, row, req, m], [seed, layer])
+        w = cache[m][(int(j) % 8) // 2]
+        out.append((w >> 32) if j % 2 == 0 else (w & 0xFFFFFFFF))
+    return out
+
+
+def _check_selection(o, cfg, V, D, n, q, sel, rho_bp, row=0, explore=None):
+    """Invariants of §3.2 / §3.2.1 against an independent numpy ranking.  With
+    explore = (seed, layer, step, req) the explored blocks must also be the e blocks left
+    outside the forced and top blocks with the smallest draws (lower j on equal draws)."""
     B = -(-n // 64)
     m = o.budget(B, cfg.top_k, rho_bp)
     f = 2 if B > 1 else 1
@@ -221,6 +237,12 @@ def _check_selection(o, cfg, V, D, n, q, sel, rho_bp, row=0):
     explored = set(sel) - top - {0, B - 1}
     assert len(explored) == (e if m > f else 0)
     assert not (explored & top)
+    if explore is not None and m > f:
+        seed, layer, step, req = explore
+        rest = [j for j in free.tolist() if j not in top]
+        keys = _numpy_explore_keys(seed, layer, step, row, req, rest)
+        want = sorted(zip(keys, rest))[:e]
+        assert explored == {j for _, j in want}
     return top, explored
 
 
@@ -238,7 +260,8 @@ def test_selection_invariants(oracle_mod, n, rho):
     assert ok
     for r in range(cfg.n_req):
         sel = blocks[r, 0, : nb[r, 0]]
-        _check_selection(o, cfg, V[r], D[r], int(n_slots[r]), int(q_pos[r]), sel, rho)
+        _check_selection(o, cfg, V[r], D[r], int(n_slots[r]), int(q_pos[r]), sel, rho,
+                         explore=(7, 2, 5, r))
 
 
 def test_rho_zero_and_cold_are_dense(oracle_mod):
@@ -274,7 +297,8 @@ def test_exploration_uniform_chi_square(oracle_mod):
     top = None
     for s in range(steps):
         blocks, nb, _, _, ok = o.select_blocks(cfg, V, D, warm, ns, ns - 1, 1, 5000, s, 0)
-        t, ex = _check_selection(o, cfg, V[0], D[0], n, n - 1, blocks[0, 0, : nb[0, 0]], 5000)
+        t, ex = _check_selection(o, cfg, V[0], D[0], n, n - 1, blocks[0, 0, : nb[0, 0]], 5000,
+                                 explore=(7, 0, s, 0) if s < 50 else None)
         top = t if top is None else top
         assert t == top
         for j in ex:
@@ -300,7 +324,7 @@ def test_union_is_or_of_rows(oracle_mod):
         rows = [set(blocks[r, k, : nb[r, k]].tolist()) for k in range(4)]
         for k in range(4):
             _check_selection(o, cfg, V[r], D[r], int(ns[r]), int(ns[r] - 1),
-                             blocks[r, k, : nb[r, k]], 4000, row=k)
+                             blocks[r, k, : nb[r, k]], 4000, row=k, explore=(7, 1, 3, r))
         assert list(union[r, : nu[r]]) == sorted(set().union(*rows))
         assert nu[r] >= nb[r, 0]
 
