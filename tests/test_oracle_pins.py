@@ -43,11 +43,11 @@ def _numpy_philox(ctr, key):
     """numpy's Philox4x64-10 advances its 256-bit counter before each block; start one
     below the wanted counter."""
     c = list(ctr)
-    i = 0
-    while c[i] == 0:
+    for i in range(4):  # 256-bit decrement (the all-zero counter wraps to all ones)
+        if c[i] != 0:
+            c[i] -= 1
+            break
         c[i] = (1 << 64) - 1
-        i += 1
-    c[i] -= 1
     bg = np.random.Philox(key=np.array(key, dtype=np.uint64))
     st = bg.state
     st["state"]["counter"] = np.array(c, dtype=np.uint64)
