@@ -17,6 +17,8 @@ sparsity.  Where the page leaves a step open, these readings are taken:
     budget rule (10000 - p basis points of sparsity), the forced first and last blocks, then
     the best m - f blocks by predicted block score (equal scores: lower block id).  A larger
     budget selects a superset, so the curve does not increase with p.
+  - A layer's curve over a batch is the mean of its requests' curves (each request weighs
+    the same); a request with no valid dense top-K slot is left out.
   - The allocation first finds the smallest attainable worst miss tau* and gives each layer
     the fewest grid points reaching miss <= tau*; spare points then go one at a time to the
     layer with the largest miss at its current point (equal misses: lower layer index; a
@@ -43,6 +45,19 @@ def miss_curve(S, nb, topk, top_k, n_points):
         missed = sum(1 for i in valid if i // 64 not in chosen)
         out.append(missed / len(valid) if valid else 0.0)
     return out
+
+
+def mean_miss_curve(S_rows, nbs, topks, top_k, n_points):
+    """The batch's curve for one layer: the mean over requests of miss_curve (requests whose
+    dense top-K holds no valid slot are left out; none left gives all zeros)."""
+    acc, used = [0.0] * n_points, 0
+    for S, nb, topk in zip(S_rows, nbs, topks):
+        if not any(int(i) >= 0 for i in topk):
+            continue
+        c = miss_curve(S, int(nb), topk, top_k, n_points)
+        acc = [a + b for a, b in zip(acc, c)]
+        used += 1
+    return [a / used for a in acc] if used else acc
 
 
 def allocate(miss, target_g, g_min):

@@ -91,3 +91,16 @@ def test_miss_curve_forced_only_and_empty():
     assert ob.miss_curve([1.0] * 10, 10, [0, 1, 9 * 64 + 3], 3, 11) == [0.0] * 11
     # no valid top-K slot: defined as no miss
     assert ob.miss_curve([1.0] * 10, 10, [-1, -1], 2, 3) == [0.0] * 3
+
+
+def test_mean_curve_of_identical_requests_and_skips_empty():
+    S = [9.0, 5.0, 1.0, 8.0, 0.5, 9.0]
+    topk = [10, 130, 200, 201]
+    one = ob.miss_curve(S, 6, topk, 4, 3)
+    assert ob.mean_miss_curve([S, S, S], [6, 6, 6], [topk, topk, topk], 4, 3) == one
+    # a request with no valid slot does not count; two different requests average
+    other = ob.miss_curve(S, 6, [10, 11, 12, 13], 4, 3)  # all in forced block 0: no miss
+    assert other == [0.0, 0.0, 0.0]
+    got = ob.mean_miss_curve([S, S, S], [6, 6, 6], [topk, [-1] * 4, [10, 11, 12, 13]], 4, 3)
+    assert got == [(a + b) / 2 for a, b in zip(one, other)]
+    assert ob.mean_miss_curve([S], [6], [[-1] * 4], 4, 3) == [0.0, 0.0, 0.0]
