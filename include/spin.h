@@ -20,7 +20,8 @@
  *   prefix of rows once verification is known (spin_commit_mtp).
  *
  * Conventions (every entry point):
- *   - All pointers except `cfg` and `bytes` are DEVICE pointers owned by the caller; the
+ *   - All pointers except `cfg`, `bytes` and those of the per-layer budget functions
+ *     (host functions on host arrays) are DEVICE pointers owned by the caller; the
  *     library allocates nothing and keeps no state between calls (except the built-in
  *     scratch array of spin_select_blocks_noalloc, see there).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
@@ -209,6 +210,47 @@ spin_status_t spin_commit_mtp(const spin_config* cfg, float* V, float* D, float*
                               const int32_t* union_blocks, const int32_t* n_union,
                               const int32_t* n_slots, const int32_t* q_pos,
                               const int32_t* accepted, uint32_t* status, spin_stream_t stream);
+
+/* Per-layer block budgets ("Sparse Attention Still Has a Dense Problem", section "Per-layer
+ * block budgets", Figures 5-6).  HOST functions on host pointers: they enqueue nothing and
+ * need no GPU.  A dense probe step (sparsity 0) gives each layer's dense top-K; the miss
+ * curve of a layer is the share of those slots that the selection at each budget would skip,
+ * and the budgets minimise the worst layer's miss while the total kept fraction stays at
+ * the target.  Budgets are kept fractions on a grid of n_points points,
+ * p_g = g * 10000 / (n_points - 1) basis points; n_points - 1 must divide 10000.
+ *
+ * spin_miss_curve: one layer's curve over a batch, the mean of its requests' curves.
+ *   S      float [n_req][s_stride]  the probe step's predicted block scores (the selection's
+ *                                   ranking key), entries 0 .. nb[r]-1 used; no NaN
+ *   nb     int32 [n_req]            blocks of each request's context, 1 .. s_stride
+ *   topk   int32 [n_req][top_k]     the dense top-K slot ids of each request (-1 = none)
+ *   miss   float [n_points] out     miss[g] = mean over requests of (dense top-K slots in
+ *                                   blocks not selected at p_g) / (valid slots), where the
+ *                                   selection at p_g is the budget rule's m blocks (sparsity
+ *                                   10000 - p_g basis points): blocks 0 and nb-1, then the
+ *                                   best m - f by S (equal S: lower block id); the random
+ *                                   exploration share is not modelled.  Requests with no valid
+ *                                   slot are left out; none left gives zeros.
+ *   Errors: SPIN_ERR_INVALID_ARG (NULL pointer, bad sizes or grid, NaN score, a top-K id
+ *   outside [-1, 64 * nb)); nothing is written then.
+ *
+ * spin_allocate_budgets: per-layer grid points from the layers' curves.
+ *   miss       float [n_layers][n_points]  the curves (no NaN)
+ *   target_g   the grid point of the global kept fraction: sum_l g_l = n_layers * target_g
+ *   g_min      the lowest grid point a layer may take, 0 <= g_min <= target_g <= n_points - 1
+ *   g_out      int32 [n_layers] out        each layer's grid point
+ *   rho_bp_out int32 [n_layers] out or NULL: each layer's sparsity, 10000 - p_{g_l} (the value
+ *              a device budget table hands to spin_select_blocks as rho_override)
+ *   The worst layer's miss max_l miss[l][g_l] is the smallest any allocation with that total
+ *   attains; each layer takes the fewest points reaching it, and the spare points go one at
+ *   a time to the layer with the largest miss at its current point (equal misses: lower
+ *   layer; a layer at the top of the grid takes none).
+ *   Errors: SPIN_ERR_INVALID_ARG (NULL pointer, bad sizes or grid, NaN). */
+spin_status_t spin_miss_curve(const float* S, int32_t n_req, int64_t s_stride, const int32_t* nb,
+                              const int32_t* topk, int32_t top_k, int32_t n_points, float* miss);
+spin_status_t spin_allocate_budgets(const float* miss, int32_t n_layers, int32_t n_points,
+                                    int32_t target_g, int32_t g_min, int32_t* g_out,
+                                    int32_t* rho_bp_out);
 
 /* Bytes of device workspace spin_select_blocks needs for `rows` rows. */
 spin_status_t spin_workspace_size(const spin_config* cfg, int32_t rows, size_t* bytes);

@@ -8,6 +8,8 @@
 
 #include <mutex>
 
+#include <cmath>
+
 #include "spin_common.cuh"
 #include "spin_internal.h"
 
@@ -269,6 +271,48 @@ spin_status_t spin_commit_mtp(const spin_config* cfg, float* V, float* D, float*
         return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
     EmaArgs a{V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots, q_pos, accepted, status};
     return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_commit_mtp");
+}
+
+spin_status_t spin_miss_curve(const float* S, int32_t n_req, int64_t s_stride, const int32_t* nb,
+                              const int32_t* topk, int32_t top_k, int32_t n_points, float* miss) {
+    if (!S || !nb || !topk || !miss) return fail(SPIN_ERR_INVALID_ARG, "S, nb, topk and miss must be non-NULL");
+    if (n_req < 1) return fail(SPIN_ERR_INVALID_ARG, "n_req %d < 1", n_req);
+    if (top_k < 1) return fail(SPIN_ERR_INVALID_ARG, "top_k %d < 1", top_k);
+    if (n_points < 2 || 10000 % (n_points - 1) != 0)
+        return fail(SPIN_ERR_INVALID_ARG, "n_points %d: n_points - 1 must divide 10000", n_points);
+    for (int32_t r = 0; r < n_req; ++r) {
+        if (nb[r] < 1 || (int64_t)nb[r] > s_stride)
+            return fail(SPIN_ERR_INVALID_ARG, "request %d: nb %d outside [1, s_stride=%lld]", r, nb[r], (long long)s_stride);
+        for (int32_t j = 0; j < nb[r]; ++j)
+            if (std::isnan(S[(int64_t)r * s_stride + j]))
+                return fail(SPIN_ERR_INVALID_ARG, "request %d: block score %d is NaN", r, j);
+        for (int32_t k = 0; k < top_k; ++k) {
+            const int32_t id = topk[(int64_t)r * top_k + k];
+            if (id < -1 || (int64_t)id >= (int64_t)nb[r] * kBlock)
+                return fail(SPIN_ERR_INVALID_ARG, "request %d: top-K id %d outside [-1, %lld)", r, id,
+                            (long long)nb[r] * kBlock);
+        }
+    }
+    spin::mean_miss_curve_host(S, n_req, s_stride, nb, topk, top_k, n_points, miss);
+    return SPIN_OK;
+}
+
+spin_status_t spin_allocate_budgets(const float* miss, int32_t n_layers, int32_t n_points, int32_t target_g,
+                                    int32_t g_min, int32_t* g_out, int32_t* rho_bp_out) {
+    if (!miss || !g_out) return fail(SPIN_ERR_INVALID_ARG, "miss and g_out must be non-NULL");
+    if (n_layers < 1) return fail(SPIN_ERR_INVALID_ARG, "n_layers %d < 1", n_layers);
+    if (n_points < 2 || 10000 % (n_points - 1) != 0)
+        return fail(SPIN_ERR_INVALID_ARG, "n_points %d: n_points - 1 must divide 10000", n_points);
+    if (g_min < 0 || g_min > target_g || target_g > n_points - 1)
+        return fail(SPIN_ERR_INVALID_ARG, "need 0 <= g_min (%d) <= target_g (%d) <= n_points - 1 (%d)", g_min,
+                    target_g, n_points - 1);
+    for (int64_t i = 0; i < (int64_t)n_layers * n_points; ++i)
+        if (std::isnan(miss[i])) return fail(SPIN_ERR_INVALID_ARG, "miss[%lld] is NaN", (long long)i);
+    spin::allocate_budgets_host(miss, n_layers, n_points, target_g, g_min, g_out);
+    if (rho_bp_out)
+        for (int32_t l = 0; l < n_layers; ++l)
+            rho_bp_out[l] = 10000 - (int32_t)((int64_t)g_out[l] * 10000 / (n_points - 1));
+    return SPIN_OK;
 }
 
 const char* spin_version(void) { return "spin-gb300 0.1.0 sm_103a"; }

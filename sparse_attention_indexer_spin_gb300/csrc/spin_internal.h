@@ -81,4 +81,12 @@ cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s)
 
 int device_sm_count();
 
+// Per-layer block budgets (host functions; spin_budget.cu).  Arguments are validated by the
+// C-ABI wrappers.
+int64_t budget_blocks_host(int64_t nb, int64_t top_k, int32_t rho_bp);
+void mean_miss_curve_host(const float* S, int32_t n_req, int64_t s_stride, const int32_t* nb,
+                          const int32_t* topk, int32_t top_k, int32_t n_points, float* miss);
+void allocate_budgets_host(const float* miss, int32_t n_layers, int32_t n_points, int32_t target_g,
+                           int32_t g_min, int32_t* g_out);
+
 }  // namespace spin

@@ -92,6 +92,8 @@ def lib():
             "spin_update_ema": [C, P, P, P, P, P, P, P, P, P, P, P],
             "spin_commit_mtp": [C, P, P, P, P, P, i32, P, P, P, P, P, P, P],
             "spin_workspace_size": [C, i32, ctypes.POINTER(ctypes.c_size_t)],
+            "spin_miss_curve": [P, i32, i64, P, P, i32, i32, P],
+            "spin_allocate_budgets": [P, i32, i32, i32, i32, P, P],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -126,6 +128,40 @@ def _ptr(t: Optional[torch.Tensor]):
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _host(a, dtype):
+    """A C-contiguous numpy array of `dtype` (host functions take host arrays)."""
+    import numpy as np
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, ctypes.c_void_p(a.ctypes.data)
+
+
+def miss_curve(S, nb, topk, n_points=101):
+    """One layer's miss curve over a batch (host arrays): S [n_req][stride] predicted block
+    scores of a dense probe step, nb [n_req] blocks per context, topk [n_req][K] the probe's
+    dense top-K.  Returns float32 [n_points]."""
+    import numpy as np
+    S, pS = _host(S, np.float32)
+    nb, pnb = _host(nb, np.int32)
+    topk, pk = _host(topk, np.int32)
+    out = np.zeros(n_points, np.float32)
+    _check(lib().spin_miss_curve(pS, S.shape[0], S.shape[1], pnb, pk, topk.shape[1], n_points,
+                                 ctypes.c_void_p(out.ctypes.data)))
+    return out
+
+
+def allocate_budgets(miss, target_g, g_min=0):
+    """Per-layer grid points and sparsities (basis points) from the layers' miss curves
+    (host array [n_layers][n_points])."""
+    import numpy as np
+    miss, pm = _host(miss, np.float32)
+    L, n_points = miss.shape
+    g = np.zeros(L, np.int32)
+    rho = np.zeros(L, np.int32)
+    _check(lib().spin_allocate_budgets(pm, L, n_points, int(target_g), int(g_min),
+                                       ctypes.c_void_p(g.ctypes.data), ctypes.c_void_p(rho.ctypes.data)))
+    return g, rho
 
 
 def version() -> str:
