@@ -243,8 +243,8 @@ spin_status_t spin_commit_mtp(const spin_config* cfg, float* V, float* D, float*
  *              a device budget table hands to spin_select_blocks as rho_override)
  *   The worst layer's miss max_l miss[l][g_l] is the smallest any allocation with that total
  *   attains; each layer takes the fewest points reaching it, and the spare points go one at
- *   a time to the layer with the largest miss at its current point (equal misses: lower
- *   layer; a layer at the top of the grid takes none).
+ *   a time to the layer with the largest miss at its current point (equal misses: fewer
+ *   points, then lower layer; a layer at the top of the grid takes none).
  *   Errors: SPIN_ERR_INVALID_ARG (NULL pointer, bad sizes or grid, NaN). */
 spin_status_t spin_miss_curve(const float* S, int32_t n_req, int64_t s_stride, const int32_t* nb,
                               const int32_t* topk, int32_t top_k, int32_t n_points, float* miss);

@@ -21,8 +21,9 @@ sparsity.  Where the page leaves a step open, these readings are taken:
     the same); a request with no valid dense top-K slot is left out.
   - The allocation first finds the smallest attainable worst miss tau* and gives each layer
     the fewest grid points reaching miss <= tau*; spare points then go one at a time to the
-    layer with the largest miss at its current point (equal misses: lower layer index; a
-    layer at the top of the grid takes none).
+    layer with the largest miss at its current point (equal misses: the layer with fewer
+    points, then the lower index, so flat curves keep the uniform budget; a layer at the top
+    of the grid takes none).
 """
 from __future__ import annotations
 
@@ -83,7 +84,9 @@ def allocate(miss, target_g, g_min):
     for _ in range(total - sum(g)):
         best = None
         for l in range(L):
-            if g[l] < G and (best is None or miss[l][g[l]] > miss[best][g[best]]):
+            if g[l] >= G:
+                continue
+            if best is None or (miss[l][g[l]], -g[l]) > (miss[best][g[best]], -g[best]):
                 best = l
         g[best] += 1
     return g

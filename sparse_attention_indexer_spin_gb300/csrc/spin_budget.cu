@@ -18,8 +18,9 @@
 // The allocation finds the smallest attainable worst miss tau* by bisection over the
 // curves' distinct values (a layer's fewest points reaching miss <= tau only falls as tau
 // grows), gives each layer those points, and hands the spare points out one at a time to the
-// layer with the largest miss at its current point (equal misses: lower layer index; a layer
-// at the top of the grid takes none), through a max-heap.
+// layer with the largest miss at its current point (equal misses: the layer with fewer
+// points, then the lower index, so flat curves keep the uniform budget; a layer at the top of
+// the grid takes none), through a max-heap.
 #include <algorithm>
 #include <cmath>
 #include <queue>
@@ -122,18 +123,24 @@ void allocate_budgets_host(const float* miss, int32_t n_layers, int32_t n_points
         g_out[l] = need(l, taus[lo]);
         used += g_out[l];
     }
-    // spare points: largest miss first, lower layer on equal misses
-    auto worse = [](const std::pair<float, int32_t>& a, const std::pair<float, int32_t>& b) {
-        return a.first < b.first || (a.first == b.first && a.second > b.second);
+    // spare points: largest miss first; on equal misses fewer points, then lower layer
+    struct Cand {
+        float miss;
+        int32_t g, l;
     };
-    std::priority_queue<std::pair<float, int32_t>, std::vector<std::pair<float, int32_t>>, decltype(worse)> heap(worse);
+    auto worse = [](const Cand& a, const Cand& b) {
+        if (a.miss != b.miss) return a.miss < b.miss;
+        if (a.g != b.g) return a.g > b.g;
+        return a.l > b.l;
+    };
+    std::priority_queue<Cand, std::vector<Cand>, decltype(worse)> heap(worse);
     for (int32_t l = 0; l < n_layers; ++l)
-        if (g_out[l] < G) heap.push({at(l, g_out[l]), l});
+        if (g_out[l] < G) heap.push({at(l, g_out[l]), g_out[l], l});
     for (int64_t s = used; s < total && !heap.empty(); ++s) {
-        const int32_t l = heap.top().second;
+        const int32_t l = heap.top().l;
         heap.pop();
         ++g_out[l];
-        if (g_out[l] < G) heap.push({at(l, g_out[l]), l});
+        if (g_out[l] < G) heap.push({at(l, g_out[l]), g_out[l], l});
     }
 }
 

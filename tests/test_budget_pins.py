@@ -44,6 +44,13 @@ def test_allocation_hand_example():
     # a layer that never misses takes the floor; the others take the rest
     Z = [0.0] * 5
     assert ob.allocate([Z, A], 2, 1) == [1, 3]
+    # flat curves (no miss anywhere) keep the uniform budget: spare points go round the
+    # layers with the fewest points
+    assert ob.allocate([Z, Z, Z], 2, 0) == [2, 2, 2]
+    assert ob.allocate([Z, Z, Z, Z], 3, 1) == [3, 3, 3, 3]
+    # equal misses at different points: the layer with fewer points first
+    C = [1.0, 0.5, 0.5, 0.5, 0.0]
+    assert ob.allocate([C, C], 1, 0) == [1, 1]
 
 
 def test_rho_of_grid():
