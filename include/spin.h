@@ -133,9 +133,10 @@ spin_status_t spin_init_state(const spin_config* cfg, float* V, float* D, float*
  *   B = ceil(N/64); m = min(B, max(ceil(K/64), ceil((10000 - rho) B / 10000)));
  *   forced F = {0, B-1}; e = min(floor(gamma m / 10000), m - |F|) (0 if m <= |F|);
  *   the m - |F| - e non-forced blocks with the largest S (S desc, j asc), then the e
- *   not-yet-selected blocks with the smallest exploration key, where the key of block j
- *   is the high 32 bits of word 0 of Philox4x64-10(key = {seed, layer},
- *   counter = {step, row, req, j}) (ties: lower j).  A cold request selects every block.
+ *   not-yet-selected blocks with the smallest exploration key (ties: lower j), where the
+ *   output of Philox4x64-10(key = {seed, layer}, counter = {step, row, req, floor(j/8)})
+ *   serves blocks 8 floor(j/8) .. +7: block j takes 32-bit half j % 8 of it, word by word,
+ *   high half first.  A cold request selects every block.
  * rho_override: NULL, or a device int32 read by the kernel in place of cfg->rho_bp (a
  *   per-layer budget table entry that CUDA graphs can replay).
  * union_blocks/n_union: required when rows > 1 (ascending union of the rows), else may
@@ -147,6 +148,21 @@ spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const f
                                  int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks,
                                  int32_t* n_union, void* workspace, size_t workspace_bytes,
                                  uint32_t* status, spin_stream_t stream);
+
+/* spin_select_blocks with the decode step read from device memory: the kernels read the
+ * uint64 *step_dev when they run, in place of `step`.  A CUDA graph that captures a step
+ * once can then replay every later step, the caller advancing *step_dev in stream order
+ * between replays (the other inputs -- V, D, N, q, the budget table -- are already device
+ * memory).  Arguments, outputs and errors are otherwise those of spin_select_blocks;
+ * step_dev must be non-NULL. */
+spin_status_t spin_select_blocks_dstep(const spin_config* cfg, const float* V, const float* D,
+                                       const float* Vmax, const int32_t* warm,
+                                       const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
+                                       const int32_t* rho_override, const uint64_t* step_dev,
+                                       int32_t layer, int32_t* blocks, int32_t* n_blocks,
+                                       int32_t* union_blocks, int32_t* n_union, void* workspace,
+                                       size_t workspace_bytes, uint32_t* status,
+                                       spin_stream_t stream);
 
 /* Allocation-free variant of spin_select_blocks (the paper has no counterpart: this is a
  * deployment convenience).  Some callers cannot allocate device memory for the workspace:

@@ -102,11 +102,11 @@ spin_status_t spin_workspace_size(const spin_config* cfg, int32_t rows, size_t* 
     return SPIN_OK;
 }
 
-spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
+static spin_status_t select_impl(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
                                  const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
-                                 const int32_t* rho_override, uint64_t step, int32_t layer, int32_t* blocks,
-                                 int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union, void* workspace,
-                                 size_t workspace_bytes, uint32_t* status, spin_stream_t stream) {
+                                 const int32_t* rho_override, uint64_t step, const uint64_t* step_dev, int32_t layer,
+                                 int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union,
+                                 void* workspace, size_t workspace_bytes, uint32_t* status, spin_stream_t stream) {
     spin_status_t st = check_cfg(cfg);
     if (st) return st;
     if ((st = check_rows(cfg, rows))) return st;
@@ -124,9 +124,29 @@ spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const f
     if (!workspace || workspace_bytes < need)
         return fail(SPIN_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
     if (((uintptr_t)workspace & 255) != 0) return fail(SPIN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer, blocks, n_blocks,
+    SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, step_dev, layer, blocks, n_blocks,
                  union_blocks, n_union, reinterpret_cast<float*>(workspace), status};
     return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks");
+}
+
+spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
+                                 const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
+                                 const int32_t* rho_override, uint64_t step, int32_t layer, int32_t* blocks,
+                                 int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union, void* workspace,
+                                 size_t workspace_bytes, uint32_t* status, spin_stream_t stream) {
+    return select_impl(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, nullptr, layer, blocks,
+                       n_blocks, union_blocks, n_union, workspace, workspace_bytes, status, stream);
+}
+
+spin_status_t spin_select_blocks_dstep(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
+                                       const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos,
+                                       int32_t rows, const int32_t* rho_override, const uint64_t* step_dev,
+                                       int32_t layer, int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks,
+                                       int32_t* n_union, void* workspace, size_t workspace_bytes, uint32_t* status,
+                                       spin_stream_t stream) {
+    if (!step_dev) return fail(SPIN_ERR_INVALID_ARG, "step_dev is NULL");
+    return select_impl(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, 0, step_dev, layer, blocks,
+                       n_blocks, union_blocks, n_union, workspace, workspace_bytes, status, stream);
 }
 
 }  // extern "C"
@@ -194,7 +214,7 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
         return fail(SPIN_ERR_INVALID_ARG, "union_blocks and n_union go together");
     float* scratch = nullptr;
     if ((st = scratch_of_current_device(&scratch))) return st;
-    SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer, blocks, n_blocks,
+    SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, nullptr, layer, blocks, n_blocks,
                  union_blocks, n_union, scratch, status};
     return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks_noalloc");
 }

@@ -19,6 +19,7 @@ struct SelectArgs {
     int rows;
     const int32_t* rho_override;
     uint64_t step;
+    const uint64_t* step_dev;  // non-NULL: the kernels read the step here instead
     int layer;
     int32_t* blocks;
     int32_t* n_blocks;

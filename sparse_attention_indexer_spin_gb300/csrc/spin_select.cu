@@ -48,9 +48,11 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
                                                           const int32_t* __restrict__ n_slots,
                                                           const int32_t* __restrict__ q_pos, int rows,
                                                           const int32_t* __restrict__ rho_override,
-                                                          uint64_t seed, uint64_t step, int layer,
+                                                          uint64_t seed, uint64_t step,
+                                                          const uint64_t* __restrict__ step_dev, int layer,
                                                           float* __restrict__ S, uint32_t* __restrict__ X) {
     pdl_begin();
+    if (step_dev) step = *step_dev;
     const Dims dm = dims_of(cfg);
     const int rr = blockIdx.y;
     const int req = rr / rows, r = rr - req * rows;
@@ -216,8 +218,10 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
     spin_config cfg, const int32_t* __restrict__ warm, const int32_t* __restrict__ n_slots,
     const int32_t* __restrict__ q_pos, int rows, const int32_t* __restrict__ rho_override, uint64_t step,
     int layer, const float* __restrict__ S, int32_t* __restrict__ blocks, int32_t* __restrict__ n_blocks,
-    int32_t* __restrict__ union_blocks, int32_t* __restrict__ n_union, uint32_t* status) {
+    int32_t* __restrict__ union_blocks, int32_t* __restrict__ n_union, uint32_t* status,
+    const uint64_t* __restrict__ step_dev) {
     pdl_begin();
+    if (step_dev) step = *step_dev;
     extern __shared__ __align__(16) unsigned char sel_smem[];
     __shared__ SelShared sh;
     const Dims dm = dims_of(cfg);
@@ -591,7 +595,7 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
                                               select_array_bytes(cfg, a.rows));
     cudaError_t e = launch_pdl(many_rows ? block_score_kernel<16> : block_score_kernel<8>, g1, dim3(256), 0, s,
                                nullptr, 0, cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,
-                               a.rho_override, cfg.seed, a.step, a.layer, S, X);
+                               a.rho_override, cfg.seed, a.step, a.step_dev, a.layer, S, X);
     if (e != cudaSuccess) return e;
     if (dm.MB <= kSrMaxBlocks && a.rows >= 1 && a.rows <= 8) {
         const int kpt = dm.MB <= kSrThreads ? 1 : dm.MB <= 2 * kSrThreads ? 2 : dm.MB <= 4 * kSrThreads ? 4
@@ -616,7 +620,7 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
     }
     return launch_pdl(select_kernel, dim3(dm.R), dim3(kSelThreads), smem, s, nullptr, 0, cfg, a.warm, a.n_slots,
                       a.q_pos, a.rows, a.rho_override, a.step, a.layer, (const float*)a.block_scores, a.blocks,
-                      a.n_blocks, a.union_blocks, a.n_union, a.status);
+                      a.n_blocks, a.union_blocks, a.n_union, a.status, a.step_dev);
 }
 
 }  // namespace spin

@@ -87,6 +87,8 @@ def lib():
             "spin_select_blocks": [C, P, P, P, P, P, P, i32, P, u64, i32, P, P, P, P, P,
                                    ctypes.c_size_t, P, P],
             "spin_select_blocks_noalloc": [C, P, P, P, P, P, P, i32, P, u64, i32, P, P, P, P, P, P],
+            "spin_select_blocks_dstep": [C, P, P, P, P, P, P, i32, P, P, i32, P, P, P, P, P,
+                                         ctypes.c_size_t, P, P],
             "spin_indexer_score": [C, P, P, P, P, i64, P, i64, P, P, P, i32, P, P, P],
             "spin_topk": [C, P, P, P, P, i32, P, P, P],
             "spin_update_ema": [C, P, P, P, P, P, P, P, P, P, P, P],
@@ -181,12 +183,20 @@ def init_state(cfg, V, D, Vmax, warm, req=-1, stream=None):
 
 def select_blocks(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer, blocks,
                   n_blocks, union_blocks, n_union, workspace, status, stream=None):
+    """`step` is an int, or a one-element int64 device tensor read by the kernels when they run
+    (spin_select_blocks_dstep: a captured graph replays every step)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if isinstance(step, torch.Tensor):
+        assert step.dtype == torch.int64 and step.numel() == 1
+        _check(lib().spin_select_blocks_dstep(
+            ctypes.byref(cfg), _ptr(V), _ptr(D), _ptr(Vmax), _ptr(warm), _ptr(n_slots), _ptr(q_pos),
+            rows, _ptr(rho_override), _ptr(step), int(layer), _ptr(blocks), _ptr(n_blocks),
+            _ptr(union_blocks), _ptr(n_union), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+        return
     _check(lib().spin_select_blocks(
         ctypes.byref(cfg), _ptr(V), _ptr(D), _ptr(Vmax), _ptr(warm), _ptr(n_slots), _ptr(q_pos),
         rows, _ptr(rho_override), int(step), int(layer), _ptr(blocks), _ptr(n_blocks),
-        _ptr(union_blocks), _ptr(n_union), _ptr(workspace),
-        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(status),
-        _stream(stream)))
+        _ptr(union_blocks), _ptr(n_union), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
 
 
 def select_blocks_noalloc(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer,
