@@ -7,12 +7,16 @@
 // drawn at random from those not selected), §3.2.2 (masks of several verifier rows are
 // unioned).
 //
-// Two kernels:
+// Kernels:
 //   block_score_kernel  many CTAs: S[req][row][j] for every block (HBM-bound scan of D
-//                       plus the per-block max of V kept in Vmax)
-//   select_kernel       one CTA per request: for each row, budget, forced blocks, radix
-//                       select of the top blocks, Philox exploration, ordered compaction;
-//                       then the union of the rows.
+//                       plus the per-block max of V kept in Vmax) and the Philox
+//                       exploration draw of every block, computed while the loads fly
+//   select_reg_kernel   up to 8192 blocks: one CTA per (request, row), keys in registers,
+//                       budget, forced blocks, radix select of the top blocks and of the
+//                       smallest draws among the rest, ordered compaction; the rows of a
+//                       request form a cluster whose first CTA writes their union
+//   select_kernel       longer lists: one CTA per request, keys in shared memory, the same
+//                       steps row by row, then the union of the rows.
 #include <float.h>
 
 #include "spin_common.cuh"
