@@ -63,6 +63,10 @@ def test_null_pointers_rejected(spin_lib):
                                 None, 1, None, None, None) == 1
     # rows beyond max_rows
     assert L.spin_topk(ctypes.byref(cfg), None, None, None, None, 2, None, None, None) == 2
+    # the device-step selection needs its step pointer
+    assert L.spin_select_blocks_dstep(ctypes.byref(cfg), *([None] * 6), 1, None, None, 0,
+                                      *([None] * 5), 0, None, None) == 1
+    assert "step_dev" in L.spin_last_error_string().decode()
 
 
 def test_library_refuses_to_run_without_build(tmp_path, monkeypatch):
