@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--impl", choices=["spin", "reference"], default="spin")
     p.add_argument("--config", default="v32", choices=sorted(syn.CONFIGS))
     p.add_argument("--rho", type=int, default=None, help="target sparsity in basis points")
+    p.add_argument("--combine", choices=["max", "sum"], default=None,
+                   help="predicted slot score: max(V, D) (Eq. 1) or V + D")
     p.add_argument("--cpu-steps", type=int, default=8, help="oracle steps of the CPU baseline")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--layers", type=int, default=None, help="fewer layers (small profiling case)")
@@ -410,6 +412,8 @@ def main():
         base = base.replace(n_layers=args.layers)
     if args.n0 is not None:
         base = base.replace(n0=args.n0)
+    if args.combine is not None:
+        base = base.replace(combine=args.combine)
     rho = base.rho_bp if args.rho is None else args.rho
     W, K = max(args.warmup, 3), args.steps
     wk = Workload(base, W + K, rho)
@@ -505,6 +509,7 @@ def main():
                                       wl.k_dtype, wl.top_k, rho / 100, wl.gamma_bp / 100, wl.rows),
                        "l2": "inputs larger than L2 (%.2f GB of keys per layer)"
                              % (wk.inp.k_pool[0].numel() * wk.inp.k_pool[0].element_size() / 1e9),
+                       "combine": wl.combine,
                        "parallelism": "replicas" if world > 1 else "1 GPU"},
             "roofline": {"kernel": "indexer score (%s)" % kernel_file[:-3], "bound": "hbm",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

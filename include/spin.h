@@ -35,7 +35,10 @@
  *   - Values the host cannot see (N, q, block ids, page ids, accepted counts) are
  *     checked by the kernels: a bad value sets a bit in the caller's `*status`
  *     (atomicOr; may be NULL) and the affected request or block is skipped -- no
- *     out-of-range access, no trap, no wait.
+ *     out-of-range access and no trap.  Kernels that stage data through shared memory
+ *     wait on mbarriers; every such wait is bounded (1 s of GPU global time), and a
+ *     wait that runs out sets SPIN_STATUS_TIMEOUT, drains the kernel's own copies in
+ *     flight, frees its tensor memory and returns.
  *
  * Layouts (R = n_req, MB = ceil(max_slots / 64), DL = max_slots + max_rows, rows <= max_rows):
  *   V        float  [R][max_slots]       vertical EMA per absolute slot i
@@ -176,7 +179,10 @@ spin_status_t spin_select_blocks_dstep(const spin_config* cfg, const float* V, c
  *     exploration draw per block and row); larger configurations are rejected with
  *     SPIN_ERR_CAPACITY.
  *   - The first call on a device looks up the array's device address (with that device
- *     current) and caches it; make that first call before any stream capture.
+ *     current) and caches it; make that first call before any stream capture.  The cached
+ *     address belongs to the device's current context: it does not survive
+ *     cudaDeviceReset, after which this entry point must not be called again in the
+ *     process.
  *   - Every call shares the one array, which keeps the last call's contents: calls that
  *     may overlap on the GPU (different streams, or different host threads, on one
  *     device) race on it and must be serialised by the caller.

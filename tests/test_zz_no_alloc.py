@@ -36,9 +36,12 @@ def _warm_workload(wl):
     return inp, cfg, st, buf
 
 
-@pytest.mark.parametrize("name,rows", [("v4flash", 1), ("mtp", 4)])
-def test_noalloc_select_equals_workspace_select(spin_lib, name, rows):
-    wl = syn.CONFIGS[name].replace(n_req=6, n0=9000, steps=4, n_heads=8, head_dim=64,
+@pytest.mark.parametrize("name,rows,n_req,n0", [("v4flash", 1, 6, 9000), ("mtp", 4, 6, 9000),
+                                                 ("v4flash", 1, 1, 9000 * 64)])
+def test_noalloc_select_equals_workspace_select(spin_lib, name, rows, n_req, n0):
+    """The third case has more than 8192 blocks per request, so the selection runs the
+    shared-memory kernel, which reads the scratch array at its largest offsets."""
+    wl = syn.CONFIGS[name].replace(n_req=n_req, n0=n0, steps=4, n_heads=8, head_dim=64,
                                    q_dtype="f32", k_dtype="f32", kv_heads=8, top_k=256,
                                    rows=rows, mean_accept=2.4 if rows > 1 else 0.0)
     inp, cfg, st, buf = _warm_workload(wl)
