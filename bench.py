@@ -48,6 +48,13 @@ def parse():
     p.add_argument("--rho", type=int, default=None, help="target sparsity in basis points")
     p.add_argument("--combine", choices=["max", "sum"], default=None,
                    help="predicted slot score: max(V, D) (Eq. 1) or V + D")
+    p.add_argument("--topk", choices=["hinted", "plain"], default="hinted",
+                   help="temporal top-K seeded by the previous step's threshold, or the plain one")
+    p.add_argument("--schedule", choices=["stacked", "serial"], default="stacked",
+                   help="one selection and one EMA launch per step for all layers, or layer by layer")
+    p.add_argument("--no-configs", action="store_true", help="skip the per-workload measurements")
+    p.add_argument("--configs", default="pr1,v32,v4flash,mtp,serving")
+    p.add_argument("--config-steps", type=int, default=20, help="timed steps per workload measurement")
     p.add_argument("--cpu-steps", type=int, default=8, help="oracle steps of the CPU baseline")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--layers", type=int, default=None, help="fewer layers (small profiling case)")
@@ -142,16 +149,43 @@ def ncu_traffic(workload, kernel_file, alg_bytes):
 
 # ----------------------------------------------------------------------- CUDA workload
 
+class StackedState:
+    """The SPIN state of L layers stacked along a new outermost dimension (one PyTorch
+    allocation per array); layer(l) gives a layer's slices for the single-layer calls."""
+
+    def __init__(self, cfg, L):
+        R, MB = cfg.n_req, cfg.max_blocks
+        self.V = torch.zeros((L, R, cfg.max_slots), dtype=torch.float32, device="cuda")
+        self.D = torch.zeros((L, R, cfg.d_len), dtype=torch.float32, device="cuda")
+        self.Vmax = torch.zeros((L, R, MB), dtype=torch.float32, device="cuda")
+        self.warm = torch.zeros((L, R), dtype=torch.int32, device="cuda")
+
+    def layer(self, l):
+        from sparse_attention_indexer_spin_gb300 import spin
+        st = spin.LayerState.__new__(spin.LayerState)
+        st.V, st.D, st.Vmax, st.warm = self.V[l], self.D[l], self.Vmax[l], self.warm[l]
+        return st
+
+
 class Workload:
-    def __init__(self, wl: syn.Workload, n_steps: int, rho_bp: int, share: "Workload" = None):
+    """One workload's inputs, state and buffers on the GPU, stepped through the C ABI.
+
+    schedule "stacked": per step one selection launch for all layers, then every layer's score
+    and top-K, then one EMA update (or MTP commit) launch for all layers; "serial": every
+    layer's select -> score -> top-K -> EMA in turn.  topk "hinted": the score kernel collects
+    the temporal top-K's candidates; "plain": the top-K reads every score."""
+
+    def __init__(self, wl: syn.Workload, n_steps: int, rho_bp: int, share: "Workload" = None,
+                 topk: str = "hinted", schedule: str = "stacked"):
         from sparse_attention_indexer_spin_gb300 import spin
         self.spin = spin
+        self.topk_mode, self.schedule = topk, schedule
         self.wl = wl = wl.replace(steps=max(wl.steps, n_steps), rho_bp=rho_bp)
         self.cfg = spin.make_config(**wl.config_fields())
         self.rows = wl.rows
         self.n_steps = n_steps
         if share is not None:
-            # same inputs, own configuration and state (used for the dense comparison)
+            # same inputs, own configuration and state (the other sparsities of a sweep)
             for k in ("inp", "L", "q", "w", "n_slots", "q_pos", "accepted"):
                 setattr(self, k, getattr(share, k))
             self._alloc()
@@ -181,52 +215,118 @@ class Workload:
         self._alloc()
 
     def _alloc(self):
-        spin, n_steps, wl = self.spin, self.n_steps, self.wl
-        self.states = [spin.LayerState(self.cfg) for _ in range(self.L)]
-        self.buf = spin.StepBuffers(self.cfg, self.rows)
+        spin, n_steps, wl, L, rows = self.spin, self.n_steps, self.wl, self.L, self.rows
+        self.state = StackedState(self.cfg, L)
+        self.states = [self.state.layer(l) for l in range(L)]
+        self.hints = None
+        if self.topk_mode == "hinted" and self._hint_ok():
+            self.hints = [spin.TopkHint(self.cfg, rows) for _ in range(L)]
+        self.buf = spin.StepBuffers(self.cfg, rows)
         R, MB = wl.n_req, self.cfg.max_blocks
+        self.scores = torch.zeros((L, R, rows, MB * 64), dtype=torch.float32, device="cuda")
+        self.topk = torch.full((L, R, rows, self.cfg.top_k), -1, dtype=torch.int32, device="cuda")
+        ws = spin.workspace_size(self.cfg, rows)
+        self.workspace = torch.zeros(((L * ws + 255) // 256) * 64, dtype=torch.float32, device="cuda")
         # per (step, layer) selections so the scored-slot count can be read back afterwards
-        self.blocks = torch.full((n_steps, self.L, R, self.rows, MB), -1, dtype=torch.int32, device="cuda")
-        self.n_blocks = torch.zeros((n_steps, self.L, R, self.rows), dtype=torch.int32, device="cuda")
-        self.unions = torch.full((n_steps, self.L, R, MB), -1, dtype=torch.int32, device="cuda")
-        self.n_unions = torch.zeros((n_steps, self.L, R), dtype=torch.int32, device="cuda")
+        self.blocks = torch.full((n_steps, L, R, rows, MB), -1, dtype=torch.int32, device="cuda")
+        self.n_blocks = torch.zeros((n_steps, L, R, rows), dtype=torch.int32, device="cuda")
+        self.unions = torch.full((n_steps, L, R, MB), -1, dtype=torch.int32, device="cuda")
+        self.n_unions = torch.zeros((n_steps, L, R), dtype=torch.int32, device="cuda")
         self.reset()
+
+    def _hint_ok(self):
+        try:
+            self.spin.topk_hint_size(self.cfg, self.rows)
+            return True
+        except self.spin.SpinError:
+            return False
 
     def reset(self):
         for st in self.states:
             self.spin.init_state(self.cfg, st.V, st.D, st.Vmax, st.warm)
+        for h in self.hints or []:
+            h.reset()
+
+    def hint_stats(self):
+        if not self.hints:
+            return None
+        tot = {}
+        for h in self.hints:
+            for k, v in h.stats().items():
+                tot[k] = tot.get(k, 0) + v
+        return tot
 
     def launches_per_step(self):
-        return self.L * 5  # block scores, select, score, top-K, EMA
+        if self.schedule == "stacked":
+            return 3 + 2 * self.L      # block scores + selection, L x (score, top-K), EMA
+        return self.L * 5              # L x (block scores, selection, score, top-K, EMA)
+
+    def lists(self, s, layer):
+        if self.rows == 1:
+            return self.blocks[s, layer, :, 0], self.n_blocks[s, layer, :, 0]
+        return self.unions[s, layer], self.n_unions[s, layer]
+
+    def score_topk(self, s, layer, q, w, ev=None):
+        spin, cfg, inp, rows = self.spin, self.cfg, self.inp, self.rows
+        ns = self.n_slots[s]
+        lst, nl = self.lists(s, layer)
+        hint = self.hints[layer] if self.hints else None
+        sc, tk = self.scores[layer], self.topk[layer]
+        if ev is not None:
+            ev[0].record()
+        if hint is None:
+            spin.indexer_score(cfg, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
+                               inp.block_table, lst, nl, ns, rows, sc, self.buf.status)
+        else:
+            spin.indexer_score_ex(cfg, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
+                                  inp.block_table, lst, nl, ns, rows, sc, self.buf.status, hint)
+        if ev is not None:
+            ev[1].record()
+        if hint is None:
+            spin.topk(cfg, sc, lst, nl, ns, rows, tk, self.buf.status)
+        else:
+            spin.topk_hinted(cfg, sc, w, lst, nl, ns, rows, tk, hint, self.buf.status)
 
     def step(self, s, ev_score=None, q_override=None, w_override=None, on_topk=None):
-        spin, cfg, buf, inp = self.spin, self.cfg, self.buf, self.inp
-        rows = self.rows
+        spin, cfg, rows, L = self.spin, self.cfg, self.rows, self.L
         ns, qp = self.n_slots[s], self.q_pos[s]
-        for layer in range(self.L):
-            st = self.states[layer]
-            q = q_override[layer] if q_override is not None else self.q[s % len(self.q)][layer]
-            w = w_override[layer] if w_override is not None else self.w[s % len(self.w)][layer]
-            blocks, nb = self.blocks[s, layer], self.n_blocks[s, layer]
+        st, status = self.state, self.buf.status
+        qs = q_override if q_override is not None else self.q[s % len(self.q)]
+        ws = w_override if w_override is not None else self.w[s % len(self.w)]
+        if self.schedule == "stacked":
+            spin.select_blocks_layers(cfg, L, 0, st.V, st.D, st.Vmax, st.warm, ns, qp, rows, None, s,
+                                      self.blocks[s], self.n_blocks[s],
+                                      self.unions[s] if rows > 1 else None,
+                                      self.n_unions[s] if rows > 1 else None, self.workspace, status)
+            for layer in range(L):
+                ev = None if ev_score is None else (ev_score[0][layer], ev_score[1][layer])
+                self.score_topk(s, layer, qs[layer], ws[layer], ev)
+                if on_topk is not None:
+                    on_topk(layer)
+            if rows == 1:
+                spin.update_ema_layers(cfg, L, st.V, st.D, st.Vmax, st.warm, self.scores,
+                                       self.blocks[s, :, :, 0], self.n_blocks[s, :, :, 0], ns, qp, status)
+            else:
+                spin.commit_mtp_layers(cfg, L, st.V, st.D, st.Vmax, st.warm, self.scores, rows,
+                                       self.unions[s], self.n_unions[s], ns, qp, self.accepted[s], status)
+            return
+        for layer in range(L):
+            lst_st = self.states[layer]
             un, nu = (self.unions[s, layer], self.n_unions[s, layer]) if rows > 1 else (None, None)
-            spin.select_blocks(cfg, st.V, st.D, st.Vmax, st.warm, ns, qp, rows, None, s, layer,
-                               blocks, nb, un, nu, buf.workspace, buf.status)
-            lst, nl = (blocks, nb) if rows == 1 else (un, nu)
-            if ev_score is not None:
-                ev_score[0][layer].record()
-            spin.indexer_score(cfg, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
-                               inp.block_table, lst, nl, ns, rows, buf.scores, buf.status)
-            if ev_score is not None:
-                ev_score[1][layer].record()
-            spin.topk(cfg, buf.scores, lst, nl, ns, rows, buf.topk, buf.status)
+            spin.select_blocks(cfg, lst_st.V, lst_st.D, lst_st.Vmax, lst_st.warm, ns, qp, rows, None, s, layer,
+                               self.blocks[s, layer], self.n_blocks[s, layer], un, nu, self.buf.workspace,
+                               status)
+            ev = None if ev_score is None else (ev_score[0][layer], ev_score[1][layer])
+            self.score_topk(s, layer, qs[layer], ws[layer], ev)
             if on_topk is not None:
                 on_topk(layer)
+            lst, nl = self.lists(s, layer)
             if rows == 1:
-                spin.update_ema(cfg, st.V, st.D, st.Vmax, st.warm, buf.scores, lst, nl, ns, qp,
-                                buf.status)
+                spin.update_ema(cfg, lst_st.V, lst_st.D, lst_st.Vmax, lst_st.warm, self.scores[layer], lst, nl,
+                                ns, qp, status)
             else:
-                spin.commit_mtp(cfg, st.V, st.D, st.Vmax, st.warm, buf.scores, rows, lst, nl, ns, qp,
-                                self.accepted[s], buf.status)
+                spin.commit_mtp(cfg, lst_st.V, lst_st.D, lst_st.Vmax, lst_st.warm, self.scores[layer], rows, lst,
+                                nl, ns, qp, self.accepted[s], status)
 
     def scored_slots(self, steps, unique=False):
         """Slots scored per (step, layer) launch, from the recorded lists: times the query
@@ -244,14 +344,42 @@ class Workload:
                 out.append(tot if unique else tot * self.rows)
         return out
 
+    def realized_sparsity(self, steps):
+        """1 - (blocks scored) / (blocks of the contexts), over the steps, layers and requests."""
+        ns = self.n_slots.cpu().numpy().astype(np.int64)
+        counts = (self.n_blocks[:, :, :, 0] if self.rows == 1 else self.n_unions).cpu().numpy()
+        sel = tot = 0
+        for s in steps:
+            nb = (ns[s] + 63) // 64
+            sel += int(counts[s].sum())
+            tot += int(nb.sum()) * self.L
+        return 1.0 - sel / max(tot, 1)
+
     def key_bytes_per_slot(self):
         wl = self.wl
         elt = {"f32": 4, "bf16": 2, "e4m3": 1}[wl.k_dtype]
         return wl.kv_heads * wl.head_dim * elt + (4 if wl.k_dtype == "e4m3" else 0)
 
+    def step_alg_bytes(self, steps):
+        """Algorithmic HBM bytes of each step: the keys (+ FP8 scales) of every scored slot
+        once, one fp32 score per slot and row written, the EMA update of the scored slots
+        (a score read per row, V and D read and written), and block prediction (Vmax and the
+        256-byte D window of every block under max, V and D of every slot under sum)."""
+        ns = self.n_slots.cpu().numpy().astype(np.int64)
+        uniq = np.array(self.scored_slots(steps, unique=True), np.float64).reshape(len(steps), self.L)
+        pred = 260 if self.wl.combine == "max" else 512
+        out = []
+        for i, s in enumerate(steps):
+            nb = float(((ns[s] + 63) // 64).sum()) * self.L * self.rows
+            slots = uniq[i].sum()
+            out.append(slots * (self.key_bytes_per_slot() + 4 * self.rows + 4 * self.rows + 16) + nb * pred)
+        return out
+
 
 def time_steps(wk, steps, with_score_events=False):
-    """Run `steps` (list of step indices) and return (elapsed ms, per-score-launch ms list)."""
+    """Run `steps` (list of step indices); returns (elapsed ms, per-score-launch ms list).
+    With score events the score launches are bracketed by CUDA events on the stream (which
+    also cuts the launch chaining at them): used for the score kernel's own time only."""
     ev_pairs = []
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -278,13 +406,13 @@ def time_e2e(wk, steps):
     host_ns = wk.n_slots.cpu().pin_memory()
     dev_q = [torch.empty_like(q) for q in wk.q[0]]
     dev_w = [torch.empty_like(w) for w in wk.w[0]]
-    host_topk = torch.empty((L,) + tuple(wk.buf.topk.shape), dtype=torch.int32).pin_memory()
+    host_topk = torch.empty(tuple(wk.topk.shape), dtype=torch.int32).pin_memory()
     h2d = sum(q.numel() * q.element_size() for q in host_q[0]) + \
         sum(w.numel() * w.element_size() for w in host_w[0]) + host_ns[0].numel() * 4
     d2h = host_topk.numel() * 4
 
     def read_back(layer):
-        host_topk[layer].copy_(wk.buf.topk, non_blocking=True)
+        host_topk[layer].copy_(wk.topk[layer], non_blocking=True)
 
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -299,6 +427,40 @@ def time_e2e(wk, steps):
     t1.record()
     torch.cuda.synchronize()
     return t0.elapsed_time(t1), h2d, d2h
+
+
+def miss_rate(wk, steps):
+    """Share of each step's dense top-K (every block scored with the same queries) that lies
+    in blocks the step did not score, over the layers, requests and rows (not timed).  Runs
+    the steps (which must follow the ones already run) and scores densely before each."""
+    spin, cfg, rows, inp = wk.spin, wk.cfg, wk.rows, wk.inp
+    R, MB = wk.wl.n_req, cfg.max_blocks
+    full = torch.arange(MB, dtype=torch.int32, device="cuda").repeat(R, 1).contiguous()
+    sc = torch.zeros((R, rows, MB * 64), dtype=torch.float32, device="cuda")
+    tk = torch.full((R, rows, cfg.top_k), -1, dtype=torch.int32, device="cuda")
+    missed = total = 0
+    for s in steps:
+        ns = wk.n_slots[s]
+        nfull = ((ns.long() + 63) // 64).to(torch.int32)
+        dense = []
+        for layer in range(wk.L):
+            q, w = wk.q[s % len(wk.q)][layer], wk.w[s % len(wk.w)][layer]
+            spin.indexer_score(cfg, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages, inp.block_table,
+                               full, nfull, ns, rows, sc, wk.buf.status)
+            spin.topk(cfg, sc, full, nfull, ns, rows, tk, wk.buf.status)
+            dense.append(tk.cpu().numpy().copy())
+        wk.step(s)
+        for layer in range(wk.L):
+            lst, nl = wk.lists(s, layer)
+            lst, nl = lst.cpu().numpy(), nl.cpu().numpy()
+            for r in range(R):
+                chosen = np.zeros(MB + 1, bool)
+                chosen[lst[r, : nl[r]]] = True
+                ids = dense[layer][r].ravel()
+                ids = ids[ids >= 0]
+                missed += int((~chosen[ids // 64]).sum())
+                total += len(ids)
+    return missed / max(total, 1)
 
 
 def reduce_over_ranks(ms, slots, dist, device):
@@ -390,6 +552,89 @@ def run_reference(args):
 
 # ------------------------------------------------------------------------------- main
 
+def host_cpu():
+    """Host core count and CPU model (the oracle's baseline runs on one of these cores)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                model = line.split(":", 1)[1].strip()
+                if line.startswith("Model name"):
+                    break
+    except Exception:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+def measure_workload(base, rho, W, K, topk, schedule, share=None, score_events=True):
+    """W warm-up steps then K timed steps at sparsity rho (basis points).  Returns the
+    workload and a record of the timed region."""
+    wk = Workload(base, W + K, rho, share=share, topk=topk, schedule=schedule)
+    wk.reset()
+    time_steps(wk, range(W))
+    ms, _ = time_steps(wk, range(W, W + K))
+    rec = {"rho_bp": rho, "ms_per_step": ms / K, "step_us_per_layer": 1000.0 * ms / K / wk.L}
+    slots = wk.scored_slots(range(W, W + K))
+    rec["slots_per_s"] = sum(slots) / (ms / 1000.0)
+    rec["realized_sparsity"] = wk.realized_sparsity(range(W, W + K))
+    peak, _ = measured_peaks()
+    step_bytes = float(np.mean(wk.step_alg_bytes(range(W, W + K))))
+    rec["step_hbm_frac"] = step_bytes / (ms / K / 1000.0) / 1e9 / peak
+    rec["step_alg_bytes"] = step_bytes
+    if score_events:
+        # the score kernel's own launches, timed separately (events cut the launch chaining)
+        wk.reset()
+        time_steps(wk, range(W))
+        _, score_ms = time_steps(wk, range(W, W + K), with_score_events=True)
+        avg = float(np.mean(score_ms))
+        unique = wk.scored_slots(range(W, W + K), unique=True)
+        alg = float(np.mean(unique)) * (wk.key_bytes_per_slot() + 4 * wk.rows)
+        rec["score_us"] = 1000.0 * avg
+        rec["score_alg_bytes"] = alg
+        rec["score_frac"] = alg / (avg / 1000.0) / 1e9 / peak
+    rec["topk_hint"] = wk.hint_stats()
+    return wk, rec
+
+
+def run_config(name, W, K, topk, schedule, extra=()):
+    """Every measurement of one workload: its sparsity sweep (or its target and 0), the dense
+    ratio, realized sparsity and miss rate at its target.  Returns a per_config entry."""
+    base = syn.CONFIGS[name]
+    points = sorted(set(base.sweep or ()) | {base.rho_bp, 0})
+    out = {"workload": name, "layers": base.n_layers, "n_req": base.n_req, "rows": base.rows,
+           "k_dtype": base.k_dtype, "kv_heads": base.kv_heads, "top_k": base.top_k,
+           "target_rho_bp": base.rho_bp, "combine": base.combine, "schedule": schedule, "topk": topk}
+    first, recs = None, {}
+    for rho in [base.rho_bp] + [p for p in points if p != base.rho_bp]:
+        wk, rec = measure_workload(base, rho, W, K, topk, schedule, share=first, score_events=(rho in (base.rho_bp, 0)))
+        if first is None:
+            first = wk
+            # miss rate of the target sparsity against the dense top-K of the same queries
+            wm = Workload(base, W + 4, rho, share=wk, topk=topk, schedule=schedule)
+            wm.reset()
+            time_steps(wm, range(W))
+            rec["miss_rate"] = miss_rate(wm, range(W, W + 4))
+            del wm
+        elif wk is not first:
+            del wk
+        recs[rho] = rec
+    tgt, dense = recs[base.rho_bp], recs[0]
+    out["target"] = tgt
+    out["dense"] = dense
+    out["dense_ratio"] = tgt["ms_per_step"] / dense["ms_per_step"]
+    out["sweep_us_per_step"] = {str(p): 1000.0 * recs[p]["ms_per_step"] for p in points}
+    for label, kw in extra:
+        b2 = base.replace(**kw)
+        _, r1 = measure_workload(b2, base.rho_bp, W, K, topk, schedule, share=None, score_events=False)
+        _, r0 = measure_workload(b2, 0, W, K, topk, schedule, share=None, score_events=False)
+        out[label] = {"target_ms_per_step": r1["ms_per_step"], "dense_ms_per_step": r0["ms_per_step"],
+                      "dense_ratio": r1["ms_per_step"] / r0["ms_per_step"], **kw}
+    del first
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -416,7 +661,7 @@ def main():
         base = base.replace(combine=args.combine)
     rho = base.rho_bp if args.rho is None else args.rho
     W, K = max(args.warmup, 3), args.steps
-    wk = Workload(base, W + K, rho)
+    wk = Workload(base, W + K, rho, topk=args.topk, schedule=args.schedule)
     wl = wk.wl
 
     def barrier():
@@ -426,26 +671,32 @@ def main():
 
     # ---------------------------------------------------------------- device-resident
     wk.reset()
-    time_steps(wk, range(W))
-    barrier()
     clocks = ClockSampler()
     clocks.start()
-    ms, score_ms = time_steps(wk, range(W, W + K), with_score_events=True)
-    clk = clocks.stop()
+    time_steps(wk, range(W))
     barrier()
+    ms, _ = time_steps(wk, range(W, W + K))
+    barrier()
+    clk = clocks.stop()
     slots_per_launch = wk.scored_slots(range(W, W + K))
     slots_total = sum(slots_per_launch)
     ms_max, slots_all = reduce_over_ranks(ms, slots_total, dist, "cuda")
     value = slots_all / (ms_max / 1000.0)
     ms_per_step = ms_max / K
+    hint_stats = wk.hint_stats()
+    realized = wk.realized_sparsity(range(W, W + K))
+    peak, peak_kind = measured_peaks()
+    step_bytes = float(np.mean(wk.step_alg_bytes(range(W, W + K))))
 
-    # dominant kernel: the indexer score
+    # dominant kernel: the indexer score, its launches bracketed by events on the stream
+    wk.reset()
+    time_steps(wk, range(W))
+    _, score_ms = time_steps(wk, range(W, W + K), with_score_events=True)
     avg_score_ms = float(np.mean(score_ms))
     kbytes = wk.key_bytes_per_slot()
     unique_per_launch = wk.scored_slots(range(W, W + K), unique=True)
     # keys (+ FP8 scale) of every scored slot once, plus one fp32 score per slot and row
     alg_bytes = float(np.mean(unique_per_launch)) * (kbytes + 4 * wk.rows)
-    peak, peak_kind = measured_peaks()
     achieved = alg_bytes / (avg_score_ms / 1000.0) / 1e9
     kernel_file = "spin_score_stream.cu" if wl.kv_heads > 1 else "spin_score_tc.cu"
     traffic = ncu_traffic(wl.name, kernel_file, alg_bytes)
@@ -453,10 +704,11 @@ def main():
     # ---------------------------------------------------------------- dense comparison
     dense = None
     if not args.no_dense and rho != 0:
-        wd = Workload(base, W + K, 0, share=wk)
+        wd = Workload(base, W + K, 0, share=wk, topk=args.topk, schedule=args.schedule)
         time_steps(wd, range(W))
         msd, _ = time_steps(wd, range(W, W + K))
-        dense = {"rho": 0.0, "ms_per_step": msd / K, "latency_ratio": (ms / K) / (msd / K)}
+        dense = {"rho": 0.0, "ms_per_step": msd / K, "latency_ratio": (ms / K) / (msd / K),
+                 "topk_hint": wd.hint_stats()}
         del wd
         torch.cuda.empty_cache()
 
@@ -483,11 +735,33 @@ def main():
         bps = 256
         rate, secs, _ = oracle_sample(wl, (pool, scale, bt, q_list, w_list, ns, qp), state,
                                       args.cpu_steps, bps, W + K)
-        cpu = {"kind": "oracle", "value": rate, "unit": "slots/s", "cores": 1,
+        cpu = {"kind": "oracle", "value": rate, "unit": "slots/s", "cores": 1, **host_cpu(),
                "sample": "%d steps of request 0, layer 0: selection over the full context, then "
                          "score/top-K/EMA over the first %d selected blocks (%.1f s)" % (args.cpu_steps, bps, secs)}
-
     status = int(wk.buf.status.item())
+    launches = wk.launches_per_step() * K
+    del wk
+    torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- every workload
+    per_config = None
+    if not args.no_configs and rank == 0:
+        per_config = {}
+        Kc = max(3, min(K, args.config_steps))
+        clocks2 = ClockSampler()
+        clocks2.start()
+        for name in args.configs.split(","):
+            extra = (("sum_combiner", {"combine": "sum"}),) if name == "v32" else ()
+            per_config[name] = run_config(name, W, Kc, args.topk, args.schedule, extra)
+        if "v32" in per_config:
+            # the one-layer-at-a-time schedule and the plain top-K, for comparison
+            _, r_serial = measure_workload(syn.CONFIGS["v32"], 4000, W, Kc, args.topk, "serial", score_events=False)
+            _, r_plain = measure_workload(syn.CONFIGS["v32"], 4000, W, Kc, "plain", args.schedule, score_events=False)
+            per_config["v32"]["serial_schedule_ms_per_step"] = r_serial["ms_per_step"]
+            per_config["v32"]["plain_topk_ms_per_step"] = r_plain["ms_per_step"]
+            torch.cuda.empty_cache()
+        per_config["clocks"] = clocks2.stop()
+
     if rank == 0:
         line = {
             "metric": "scored slots/s (SPIN indexer step)",
@@ -497,7 +771,7 @@ def main():
             "steps": K,
             "warmup": W,
             "ms_per_step": ms_per_step,
-            "latency_us_per_layer_step": 1000.0 * ms_per_step / wk.L,
+            "latency_us_per_layer_step": 1000.0 * ms_per_step / base.n_layers,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
@@ -505,21 +779,27 @@ def main():
             "data": "synthetic",
             "config": {"workload": "%s: %d req x %d layers, %d slots, %d heads x %d, kv_heads %d, %s keys, "
                                    "K=%d, rho=%.0f%%, gamma=%.0f%%, rows=%d"
-                                   % (wl.name, wl.n_req, wk.L, base.n0, wl.n_heads, wl.head_dim, wl.kv_heads,
-                                      wl.k_dtype, wl.top_k, rho / 100, wl.gamma_bp / 100, wl.rows),
-                       "l2": "inputs larger than L2 (%.2f GB of keys per layer)"
-                             % (wk.inp.k_pool[0].numel() * wk.inp.k_pool[0].element_size() / 1e9),
-                       "combine": wl.combine,
+                                   % (wl.name, wl.n_req, base.n_layers, base.n0, wl.n_heads, wl.head_dim,
+                                      wl.kv_heads, wl.k_dtype, wl.top_k, rho / 100, wl.gamma_bp / 100, wl.rows),
+                       "l2": "inputs larger than L2 (keys of every layer in their own pool, %.2f GB each)"
+                             % (base.n_req * base.max_blocks * 64 * (wl.kv_heads * wl.head_dim *
+                                {"f32": 4, "bf16": 2, "e4m3": 1}[wl.k_dtype]) / 1e9),
+                       "combine": wl.combine, "schedule": args.schedule, "topk": args.topk,
                        "parallelism": "replicas" if world > 1 else "1 GPU"},
             "roofline": {"kernel": "indexer score (%s)" % kernel_file[:-3], "bound": "hbm",
                          "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_kind": peak_kind, "traffic": traffic,
                          "alg_bytes_per_launch": alg_bytes, "avg_launch_us": 1000.0 * avg_score_ms},
+            "step_hbm": {"alg_bytes_per_step": step_bytes,
+                         "frac": step_bytes / (ms_per_step / 1000.0) / 1e9 / peak, "peak": peak},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "slots/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": wk.launches_per_step() * K,
+            "gpu_launches": launches,
             "clocks": clk,
             "dense": dense,
+            "realized_sparsity": realized,
+            "topk": {"mode": args.topk, "hint": hint_stats},
+            "per_config": per_config,
             "status": status,
         }
         print(json.dumps(line))

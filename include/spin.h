@@ -167,6 +167,45 @@ spin_status_t spin_select_blocks_dstep(const spin_config* cfg, const float* V, c
                                        size_t workspace_bytes, uint32_t* status,
                                        spin_stream_t stream);
 
+/* Layer stacks.  A model runs the indexer step in every layer, and a layer's selection for
+ * decode step t needs only that layer's state after step t-1 -- not the layer's query -- so
+ * the selections of all layers can be computed together at the start of a step
+ * (§3.2: block prediction and the EMA update can be scheduled asynchronously, overlapped
+ * with the forward pass of other layers).  The _layers calls take n_layers layers whose
+ * arrays are stacked along a new outermost dimension -- V [L][R][max_slots], D [L][R][DL],
+ * Vmax [L][R][MB], warm [L][R], blocks [L][R][rows][MB], n_blocks [L][R][rows], union
+ * [L][R][MB], n_union [L][R], scores [L][R][rows][MB*64], list [L][R][MB], n_list [L][R]
+ * -- and do in one launch what n_layers single-layer calls on the slices l = 0 .. L-1
+ * would do, with identical results.  n_slots, q_pos and accepted are per request, shared by
+ * the layers.  1 <= n_layers <= 1024.
+ *
+ * spin_select_blocks_layers: layer l of the stack is model layer layer0 + l (the Philox
+ *   key); rho_override is NULL or a device table of n_layers sparsities (a per-layer budget
+ *   table); step_dev, if non-NULL, is read in place of `step` (as spin_select_blocks_dstep);
+ *   workspace: n_layers * spin_workspace_size(cfg, rows) bytes, 256-byte aligned. */
+spin_status_t spin_select_blocks_layers(const spin_config* cfg, int32_t n_layers, int32_t layer0,
+                                        const float* V, const float* D, const float* Vmax,
+                                        const int32_t* warm, const int32_t* n_slots,
+                                        const int32_t* q_pos, int32_t rows,
+                                        const int32_t* rho_override, uint64_t step,
+                                        const uint64_t* step_dev, int32_t* blocks,
+                                        int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union,
+                                        void* workspace, size_t workspace_bytes, uint32_t* status,
+                                        spin_stream_t stream);
+/* spin_update_ema of every layer of a stack (row-0 scores [L][R][1][MB*64]). */
+spin_status_t spin_update_ema_layers(const spin_config* cfg, int32_t n_layers, float* V, float* D,
+                                     float* Vmax, int32_t* warm, const float* scores,
+                                     const int32_t* list, const int32_t* n_list,
+                                     const int32_t* n_slots, const int32_t* q_pos, uint32_t* status,
+                                     spin_stream_t stream);
+/* spin_commit_mtp of every layer of a stack (scores [L][R][rows][MB*64], unions [L][R][MB]). */
+spin_status_t spin_commit_mtp_layers(const spin_config* cfg, int32_t n_layers, float* V, float* D,
+                                     float* Vmax, int32_t* warm, const float* scores, int32_t rows,
+                                     const int32_t* union_blocks, const int32_t* n_union,
+                                     const int32_t* n_slots, const int32_t* q_pos,
+                                     const int32_t* accepted, uint32_t* status,
+                                     spin_stream_t stream);
+
 /* Allocation-free variant of spin_select_blocks (the paper has no counterpart: this is a
  * deployment convenience).  Some callers cannot allocate device memory for the workspace:
  * serving engines that reserve all device memory up front in their own pool and forbid
@@ -207,12 +246,64 @@ spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const fl
                                  const int32_t* n_slots, int32_t rows, float* scores,
                                  uint32_t* status, spin_stream_t stream);
 
+/* Optional work fused into spin_indexer_score_ex (zero-initialise, then set what is wanted). */
+typedef struct spin_score_extras {
+    /* Temporal top-K (see spin_topk_hinted): a hint buffer of at least topk_hint_bytes bytes
+     * (spin_topk_hint_size).  The score kernel compares every fresh score with its row's
+     * guess and appends the live slots at or above it to the hint; the next
+     * spin_topk_hinted call on the same rows consumes them.  NULL: nothing is collected. */
+    void* topk_hint;
+    size_t topk_hint_bytes;
+} spin_score_extras;
+
+/* spin_indexer_score with the work of `extras` (may be NULL) fused into its kernel.  Errors
+ * as spin_indexer_score, plus SPIN_ERR_UNSUPPORTED when a hint is given for a shape without
+ * a hinted top-K and SPIN_ERR_INVALID_ARG for a hint that is too small or not 256-byte
+ * aligned. */
+spin_status_t spin_indexer_score_ex(const spin_config* cfg, const void* q, const float* w,
+                                    const void* k_pool, const float* k_scale, int64_t n_pages,
+                                    const int32_t* block_table, int64_t bt_stride,
+                                    const int32_t* list, const int32_t* n_list,
+                                    const int32_t* n_slots, int32_t rows, float* scores,
+                                    const spin_score_extras* extras, uint32_t* status,
+                                    spin_stream_t stream);
+
 /* Post-indexer top-K (Algorithm 1's top-K step) of every row over the scored slots i < N of
  * the list: the K largest z, equal z ordered by the lower slot id (-0 == +0); written
  * as ascending slot ids and padded with -1 when fewer than K slots were scored. */
 spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32_t* list,
                         const int32_t* n_list, const int32_t* n_slots, int32_t rows,
                         int32_t* topk_idx, uint32_t* status, spin_stream_t stream);
+
+/* Temporal top-K ("SPIN: Shadow Predictive Indexer for Sparse Attention", §5: the
+ * Guess-Verify-Refine top-K exploits the correlation of consecutive decode steps).  The
+ * result is exactly spin_topk's (same ties, same padding); the hint only makes it cheaper.
+ *   - hint: caller-owned device memory of spin_topk_hint_size bytes, 256-byte aligned,
+ *     holding per (request, row) a 64-byte record -- guess key, candidate count, rank margin,
+ *     and counters of hit / miss / overflow / cold / exact steps as uint32 words 0..8 -- and
+ *     then the candidate arrays.  Zero the records with spin_init_topk_hint before the first
+ *     step and whenever spin_init_state resets a request.
+ *   - A step is spin_indexer_score_ex with extras->topk_hint = hint, then spin_topk_hinted
+ *     on the same scores, head weights w ([R][rows][n_heads], those the scores were computed
+ *     with), list and rows with the same hint.  The score kernel collects the live slots
+ *     whose score is >= the row's threshold: the guess times this step's sum_h |w_h|.  If K
+ *     to cap of them were found (cap = 4 K rounded up to a power of two, at least 4096), the
+ *     top-K is selected among them; otherwise (no guess yet, too few, too many) the row is
+ *     recomputed from its scores.  The score at rank K + margin divided by sum_h |w_h|
+ *     becomes the next step's guess; the margin (initially sqrt(K cap) - K, within
+ *     [K/8, cap/2 - K]) doubles after a miss and halves after an overflow.
+ *   - Calling spin_indexer_score_ex twice with one hint without a spin_topk_hinted in
+ *     between mixes two steps' candidates; the count then usually exceeds cap and the row is
+ *     recomputed (still exact), unless fewer than cap were collected in total -- so do not.
+ *   - Supported for top_k <= 2048 and at most 8192 blocks (ceil(max_slots/64)); other
+ *     shapes get SPIN_ERR_UNSUPPORTED from all three calls. */
+spin_status_t spin_topk_hint_size(const spin_config* cfg, int32_t rows, size_t* bytes);
+spin_status_t spin_init_topk_hint(const spin_config* cfg, int32_t rows, void* hint,
+                                  size_t hint_bytes, int32_t req, spin_stream_t stream);
+spin_status_t spin_topk_hinted(const spin_config* cfg, const float* scores, const float* w,
+                               const int32_t* list, const int32_t* n_list,
+                               const int32_t* n_slots, int32_t rows, int32_t* topk_idx, void* hint,
+                               size_t hint_bytes, uint32_t* status, spin_stream_t stream);
 
 /* EMA update (Algorithm 1's EMA update) from the row-0 scores of the list:
  *   t = fl((1 - alpha) z[i]);  V[i] = fma(alpha, V[i], t);  D[q-i] = fma(alpha, D[q-i], t)

@@ -102,14 +102,21 @@ spin_status_t spin_workspace_size(const spin_config* cfg, int32_t rows, size_t* 
     return SPIN_OK;
 }
 
+static spin_status_t check_layers(int32_t n_layers) {
+    if (n_layers < 1 || n_layers > 1024) return fail(SPIN_ERR_INVALID_ARG, "n_layers %d outside [1, 1024]", n_layers);
+    return SPIN_OK;
+}
+
 static spin_status_t select_impl(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
                                  const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
                                  const int32_t* rho_override, uint64_t step, const uint64_t* step_dev, int32_t layer,
                                  int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union,
-                                 void* workspace, size_t workspace_bytes, uint32_t* status, spin_stream_t stream) {
+                                 void* workspace, size_t workspace_bytes, uint32_t* status, spin_stream_t stream,
+                                 int32_t n_layers = 1) {
     spin_status_t st = check_cfg(cfg);
     if (st) return st;
     if ((st = check_rows(cfg, rows))) return st;
+    if ((st = check_layers(n_layers))) return st;
     const Dims dm = dims_of(*cfg);
     if (dm.MB > kSelectMaxBlocks)
         return fail(SPIN_ERR_CAPACITY, "max_slots %d needs %d blocks; selection supports %d", cfg->max_slots, dm.MB,
@@ -120,12 +127,12 @@ static spin_status_t select_impl(const spin_config* cfg, const float* V, const f
         return fail(SPIN_ERR_INVALID_ARG, "rows > 1 needs union_blocks and n_union");
     if ((union_blocks == nullptr) != (n_union == nullptr))
         return fail(SPIN_ERR_INVALID_ARG, "union_blocks and n_union go together");
-    const size_t need = select_workspace_bytes(*cfg, rows);
+    const size_t need = (size_t)n_layers * select_workspace_bytes(*cfg, rows);
     if (!workspace || workspace_bytes < need)
         return fail(SPIN_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
     if (((uintptr_t)workspace & 255) != 0) return fail(SPIN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, step_dev, layer, blocks, n_blocks,
-                 union_blocks, n_union, reinterpret_cast<float*>(workspace), status};
+                 union_blocks, n_union, reinterpret_cast<float*>(workspace), status, n_layers};
     return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks");
 }
 
@@ -136,6 +143,17 @@ spin_status_t spin_select_blocks(const spin_config* cfg, const float* V, const f
                                  size_t workspace_bytes, uint32_t* status, spin_stream_t stream) {
     return select_impl(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, nullptr, layer, blocks,
                        n_blocks, union_blocks, n_union, workspace, workspace_bytes, status, stream);
+}
+
+spin_status_t spin_select_blocks_layers(const spin_config* cfg, int32_t n_layers, int32_t layer0, const float* V,
+                                        const float* D, const float* Vmax, const int32_t* warm,
+                                        const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
+                                        const int32_t* rho_override, uint64_t step, const uint64_t* step_dev,
+                                        int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union,
+                                        void* workspace, size_t workspace_bytes, uint32_t* status,
+                                        spin_stream_t stream) {
+    return select_impl(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, step_dev, layer0, blocks,
+                       n_blocks, union_blocks, n_union, workspace, workspace_bytes, status, stream, n_layers);
 }
 
 spin_status_t spin_select_blocks_dstep(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
@@ -219,13 +237,29 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
     return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks_noalloc");
 }
 
-spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const float* w, const void* k_pool,
-                                 const float* k_scale, int64_t n_pages, const int32_t* block_table, int64_t bt_stride,
-                                 const int32_t* list, const int32_t* n_list, const int32_t* n_slots, int32_t rows,
-                                 float* scores, uint32_t* status, spin_stream_t stream) {
+static spin_status_t check_hint(const spin_config* cfg, int32_t rows, const void* hint, size_t hint_bytes) {
+    if (!topk_hint_supported(*cfg))
+        return fail(SPIN_ERR_UNSUPPORTED, "no hinted top-K for top_k %d with %d blocks (needs top_k <= 2048 and "
+                    "at most 8192 blocks)", cfg->top_k, dims_of(*cfg).MB);
+    if (!hint) return fail(SPIN_ERR_INVALID_ARG, "hint is NULL");
+    if (((uintptr_t)hint & 255) != 0) return fail(SPIN_ERR_INVALID_ARG, "hint must be 256-byte aligned");
+    const size_t need = topk_hint_bytes(*cfg, rows);
+    if (hint_bytes < need) return fail(SPIN_ERR_INVALID_ARG, "hint of %zu bytes needed (got %zu)", need, hint_bytes);
+    return SPIN_OK;
+}
+
+static spin_status_t score_impl(const spin_config* cfg, const void* q, const float* w, const void* k_pool,
+                                const float* k_scale, int64_t n_pages, const int32_t* block_table, int64_t bt_stride,
+                                const int32_t* list, const int32_t* n_list, const int32_t* n_slots, int32_t rows,
+                                float* scores, const spin_score_extras* ex, uint32_t* status, spin_stream_t stream) {
     spin_status_t st = check_cfg(cfg);
     if (st) return st;
     if ((st = check_rows(cfg, rows))) return st;
+    HintArgs hint{nullptr, nullptr, 0};
+    if (ex && ex->topk_hint) {
+        if ((st = check_hint(cfg, rows, ex->topk_hint, ex->topk_hint_bytes))) return st;
+        hint = topk_hint_args(*cfg, rows, ex->topk_hint);
+    }
     const Dims dm = dims_of(*cfg);
     if (!q || !w || !k_pool || !block_table || !list || !n_list || !n_slots || !scores)
         return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
@@ -235,7 +269,7 @@ spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const fl
     if (((uintptr_t)k_pool & 15) != 0 || (k_scale && ((uintptr_t)k_scale & 15) != 0))
         return fail(SPIN_ERR_INVALID_ARG, "k_pool and k_scale must be 16-byte aligned");
     ScoreArgs a{q, w, k_pool, cfg->k_dtype == SPIN_DTYPE_E4M3 ? k_scale : nullptr, n_pages, block_table, bt_stride,
-                list, n_list, n_slots, rows, scores, status};
+                list, n_list, n_slots, rows, scores, status, hint};
     int path = cfg->score_path;
     if (path == SPIN_SCORE_AUTO) {
         if (score_tc_supported(*cfg, rows)) path = SPIN_SCORE_TCGEN05;
@@ -258,6 +292,63 @@ spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const fl
     return fail(SPIN_ERR_INVALID_ARG, "score_path");
 }
 
+spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const float* w, const void* k_pool,
+                                 const float* k_scale, int64_t n_pages, const int32_t* block_table, int64_t bt_stride,
+                                 const int32_t* list, const int32_t* n_list, const int32_t* n_slots, int32_t rows,
+                                 float* scores, uint32_t* status, spin_stream_t stream) {
+    return score_impl(cfg, q, w, k_pool, k_scale, n_pages, block_table, bt_stride, list, n_list, n_slots, rows,
+                      scores, nullptr, status, stream);
+}
+
+spin_status_t spin_indexer_score_ex(const spin_config* cfg, const void* q, const float* w, const void* k_pool,
+                                    const float* k_scale, int64_t n_pages, const int32_t* block_table,
+                                    int64_t bt_stride, const int32_t* list, const int32_t* n_list,
+                                    const int32_t* n_slots, int32_t rows, float* scores,
+                                    const spin_score_extras* extras, uint32_t* status, spin_stream_t stream) {
+    return score_impl(cfg, q, w, k_pool, k_scale, n_pages, block_table, bt_stride, list, n_list, n_slots, rows,
+                      scores, extras, status, stream);
+}
+
+spin_status_t spin_topk_hint_size(const spin_config* cfg, int32_t rows, size_t* bytes) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    if (!bytes) return fail(SPIN_ERR_INVALID_ARG, "bytes is NULL");
+    if (!topk_hint_supported(*cfg))
+        return fail(SPIN_ERR_UNSUPPORTED, "no hinted top-K for top_k %d with %d blocks (needs top_k <= 2048 and "
+                    "at most 8192 blocks)", cfg->top_k, dims_of(*cfg).MB);
+    *bytes = topk_hint_bytes(*cfg, rows);
+    return SPIN_OK;
+}
+
+spin_status_t spin_init_topk_hint(const spin_config* cfg, int32_t rows, void* hint, size_t hint_bytes, int32_t req,
+                                  spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    if ((st = check_hint(cfg, rows, hint, hint_bytes))) return st;
+    if (req >= cfg->n_req) return fail(SPIN_ERR_INVALID_ARG, "req %d >= n_req %d", req, cfg->n_req);
+    const size_t rec = (size_t)kHintWords * 4;
+    unsigned char* base = reinterpret_cast<unsigned char*>(hint);
+    const size_t off = req < 0 ? 0 : (size_t)req * rows * rec;
+    const size_t len = (req < 0 ? (size_t)cfg->n_req : 1u) * rows * rec;
+    return launched(cudaMemsetAsync(base + off, 0, len, (cudaStream_t)stream), "spin_init_topk_hint");
+}
+
+spin_status_t spin_topk_hinted(const spin_config* cfg, const float* scores, const float* w, const int32_t* list,
+                               const int32_t* n_list, const int32_t* n_slots, int32_t rows, int32_t* topk_idx,
+                               void* hint, size_t hint_bytes, uint32_t* status, spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    if (!scores || !w || !list || !n_list || !n_slots || !topk_idx)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if ((st = check_hint(cfg, rows, hint, hint_bytes))) return st;
+    return launched(launch_topk_hint(*cfg, scores, w, list, n_list, n_slots, rows, topk_idx,
+                                     topk_hint_args(*cfg, rows, hint), status, (cudaStream_t)stream),
+                    "spin_topk_hinted");
+}
+
 spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32_t* list, const int32_t* n_list,
                         const int32_t* n_slots, int32_t rows, int32_t* topk_idx, uint32_t* status,
                         spin_stream_t stream) {
@@ -269,28 +360,59 @@ spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32
                     "spin_topk");
 }
 
+static spin_status_t update_impl(const spin_config* cfg, int32_t n_layers, float* V, float* D, float* Vmax,
+                                 int32_t* warm, const float* scores, const int32_t* list, const int32_t* n_list,
+                                 const int32_t* n_slots, const int32_t* q_pos, uint32_t* status, spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_layers(n_layers))) return st;
+    if (!V || !D || !Vmax || !warm || !scores || !list || !n_list || !n_slots || !q_pos)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    EmaArgs a{V, D, Vmax, warm, scores, 1, list, n_list, n_slots, q_pos, nullptr, status, n_layers};
+    return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_update_ema");
+}
+
+static spin_status_t commit_impl(const spin_config* cfg, int32_t n_layers, float* V, float* D, float* Vmax,
+                                 int32_t* warm, const float* scores, int32_t rows, const int32_t* union_blocks,
+                                 const int32_t* n_union, const int32_t* n_slots, const int32_t* q_pos,
+                                 const int32_t* accepted, uint32_t* status, spin_stream_t stream) {
+    spin_status_t st = check_cfg(cfg);
+    if (st) return st;
+    if ((st = check_rows(cfg, rows))) return st;
+    if ((st = check_layers(n_layers))) return st;
+    if (!V || !D || !Vmax || !warm || !scores || !union_blocks || !n_union || !n_slots || !q_pos || !accepted)
+        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    EmaArgs a{V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots, q_pos, accepted, status, n_layers};
+    return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_commit_mtp");
+}
+
 spin_status_t spin_update_ema(const spin_config* cfg, float* V, float* D, float* Vmax, int32_t* warm,
                               const float* scores, const int32_t* list, const int32_t* n_list, const int32_t* n_slots,
                               const int32_t* q_pos, uint32_t* status, spin_stream_t stream) {
-    spin_status_t st = check_cfg(cfg);
-    if (st) return st;
-    if (!V || !D || !Vmax || !warm || !scores || !list || !n_list || !n_slots || !q_pos)
-        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
-    EmaArgs a{V, D, Vmax, warm, scores, 1, list, n_list, n_slots, q_pos, nullptr, status};
-    return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_update_ema");
+    return update_impl(cfg, 1, V, D, Vmax, warm, scores, list, n_list, n_slots, q_pos, status, stream);
+}
+
+spin_status_t spin_update_ema_layers(const spin_config* cfg, int32_t n_layers, float* V, float* D, float* Vmax,
+                                     int32_t* warm, const float* scores, const int32_t* list, const int32_t* n_list,
+                                     const int32_t* n_slots, const int32_t* q_pos, uint32_t* status,
+                                     spin_stream_t stream) {
+    return update_impl(cfg, n_layers, V, D, Vmax, warm, scores, list, n_list, n_slots, q_pos, status, stream);
 }
 
 spin_status_t spin_commit_mtp(const spin_config* cfg, float* V, float* D, float* Vmax, int32_t* warm,
                               const float* scores, int32_t rows, const int32_t* union_blocks, const int32_t* n_union,
                               const int32_t* n_slots, const int32_t* q_pos, const int32_t* accepted, uint32_t* status,
                               spin_stream_t stream) {
-    spin_status_t st = check_cfg(cfg);
-    if (st) return st;
-    if ((st = check_rows(cfg, rows))) return st;
-    if (!V || !D || !Vmax || !warm || !scores || !union_blocks || !n_union || !n_slots || !q_pos || !accepted)
-        return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
-    EmaArgs a{V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots, q_pos, accepted, status};
-    return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_commit_mtp");
+    return commit_impl(cfg, 1, V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots, q_pos, accepted,
+                       status, stream);
+}
+
+spin_status_t spin_commit_mtp_layers(const spin_config* cfg, int32_t n_layers, float* V, float* D, float* Vmax,
+                                     int32_t* warm, const float* scores, int32_t rows, const int32_t* union_blocks,
+                                     const int32_t* n_union, const int32_t* n_slots, const int32_t* q_pos,
+                                     const int32_t* accepted, uint32_t* status, spin_stream_t stream) {
+    return commit_impl(cfg, n_layers, V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots, q_pos,
+                       accepted, status, stream);
 }
 
 spin_status_t spin_miss_curve(const float* S, int32_t n_req, int64_t s_stride, const int32_t* nb,

@@ -53,6 +53,80 @@ __device__ __forceinline__ uint32_t order_key(float x) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Temporal top-K hint (spin_topk_hint.cu).  Per (request, row) a record of kHintWords words:
+// the guess (order key at or below the coming step's K-th score; 0 = none), the number of
+// candidates the score kernel found at or above it, the rank margin of the next guess and
+// counters of how the hinted top-K resolved its steps.  The candidates follow the records:
+// cap entries per (request, row), each the slot's key in the high word and the complement
+// of its list position (list entry * 64 + slot of the block) in the low word, so that the
+// K largest entries are the top-K with equal keys taken in ascending position order.
+// ---------------------------------------------------------------------------------------
+constexpr int kHintWords = 16;
+enum HintWord {
+    kHwGuess = 0,    // order key of the normalised guess g (0: none, the next top-K takes the
+                     // cold path); the score kernel's threshold is g * sum_h |w_h| of its step
+    kHwCount = 1,    // candidates found by the score kernel (may exceed cap)
+    kHwExtra = 2,    // ranks beyond K at which the next guess is taken (0: K / 2)
+    kHwHit = 3,      // steps resolved from the candidates
+    kHwMiss = 4,     // steps whose guess found fewer than K candidates
+    kHwOver = 5,     // steps whose guess found more candidates than fit
+    kHwCold = 6,     // steps without a guess
+    kHwGlobal = 7,   // cold steps whose boundary bin did not fit: exact passes over the scores
+    kHwLast = 8      // the last step's candidate count
+};
+
+struct HintArgs {
+    uint32_t* rec;              // [R * rows][kHintWords], NULL: no hint
+    unsigned long long* cand;   // [R * rows][cap]
+    int cap;
+};
+
+// Inverse of order_key (the float of a key; key 0x80000000 is +0).
+__device__ __forceinline__ float key_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// sum_h |w_h| of one row's n head weights (in head order).
+__device__ __forceinline__ float row_wsum(const float* w, int n) {
+    float s = 0.0f;
+    for (int h = 0; h < n; ++h) s = __fadd_rn(s, fabsf(w[h]));
+    return s;
+}
+
+// Threshold key of a row for this step: the normalised guess times the step's sum of |w_h|
+// (the head weights move the scale of every score of a step together), 0 without a guess.
+__device__ __forceinline__ uint32_t hint_threshold(uint32_t guess_word, float wsum) {
+    if (guess_word == 0u) return 0u;
+    const uint32_t k = order_key(__fmul_rn(key_float(guess_word), wsum));
+    return k == 0u ? 1u : k;
+}
+
+__device__ __forceinline__ unsigned long long hint_entry(uint32_t key, uint32_t pos) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(~pos);
+}
+
+// Append one candidate with its own atomic (a few per cent of the slots reach the guess).
+__device__ __forceinline__ void hint_push(const HintArgs& h, int64_t rr, uint32_t key, uint32_t pos) {
+    const uint32_t at = atomicAdd(h.rec + rr * kHintWords + kHwCount, 1u);
+    if (at < (uint32_t)h.cap) h.cand[rr * h.cap + at] = hint_entry(key, pos);
+}
+
+// The same for a full warp whose lanes belong to one (request, row): one atomic per warp.
+__device__ __forceinline__ void hint_push_warp(const HintArgs& h, int64_t rr, bool take, uint32_t key,
+                                               uint32_t pos) {
+    const unsigned m = __ballot_sync(0xffffffffu, take);
+    if (m == 0u) return;
+    const int lane = threadIdx.x & 31, lead = __ffs(m) - 1;
+    uint32_t base = 0;
+    if (lane == lead) base = atomicAdd(h.rec + rr * kHintWords + kHwCount, (uint32_t)__popc(m));
+    base = __shfl_sync(0xffffffffu, base, lead);
+    if (take) {
+        const uint32_t at = base + (uint32_t)__popc(m & ((1u << lane) - 1u));
+        if (at < (uint32_t)h.cap) h.cand[rr * h.cap + at] = hint_entry(key, pos);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2,
 // 3", SC'11): ten rounds; each multiplies counter words 0 and 2 by the round multipliers,
 // xors the high halves into words 1 and 3 together with the round key, and the key is

@@ -26,11 +26,25 @@ constexpr int kEmaSpan = 1024;
 constexpr int kEmaThreads = 256;
 constexpr int kEmaMapBlocks = kEmaSpan / kBlock + 2;
 
+// Layer blockIdx.z of a stack of layers: its arrays start l layer-sizes after layer 0's.
+__device__ __forceinline__ void ema_layer_offsets(const Dims& dm, EmaArgs& a) {
+    const int64_t l = blockIdx.z;
+    if (l == 0) return;
+    a.V += l * dm.R * dm.max_slots;
+    a.D += l * dm.R * dm.DL;
+    a.Vmax += l * dm.R * dm.MB;
+    a.warm += l * dm.R;
+    a.scores += l * dm.R * a.rows * dm.MB * kBlock;
+    a.list += l * dm.R * dm.MB;
+    a.n_list += l * dm.R;
+}
+
 __global__ void __launch_bounds__(kEmaThreads) ema_replay_kernel(spin_config cfg, EmaArgs a) {
     pdl_begin();
     extern __shared__ float zs[];  // [(a+1)][span]
     __shared__ int pos[kEmaMapBlocks];
     const Dims dm = dims_of(cfg);
+    ema_layer_offsets(dm, a);
     const int req = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     const int rows = a.rows;
     const int64_t n = a.n_slots[req], q = a.q_pos[req], cnt = a.n_list[req];
@@ -160,6 +174,7 @@ constexpr int kEmaListWarps = 8;  // warps per CTA
 __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs a) {
     pdl_begin();
     const Dims dm = dims_of(cfg);
+    ema_layer_offsets(dm, a);
     const int req = blockIdx.y, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int64_t n = a.n_slots[req], q = a.q_pos[req], cnt = a.n_list[req];
     uint32_t bad = request_check(n, q, 1, dm);
@@ -226,15 +241,16 @@ __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs 
 
 cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
+    const int L = a.n_layers > 1 ? a.n_layers : 1;
     if (a.accepted == nullptr && a.rows == 1) {
         // about eight CTAs per SM over all requests, at most one step per warp for the longest list
         const int full = (dm.MB + 2 * kEmaListWarps - 1) / (2 * kEmaListWarps);
-        const int want = (device_sm_count() * 8 + dm.R - 1) / dm.R;
-        dim3 grid(want < full ? (want > 0 ? want : 1) : full, dm.R);
+        const int want = (device_sm_count() * 8 + dm.R * L - 1) / (dm.R * L);
+        dim3 grid(want < full ? (want > 0 ? want : 1) : full, dm.R, L);
         return launch_pdl(ema_list_kernel, grid, dim3(256), 0, s, nullptr, 0, cfg, a);
     }
     const int gx = (dm.max_slots + kEmaSpan - 1) / kEmaSpan;
-    dim3 grid(gx > 0 ? gx : 1, dm.R);
+    dim3 grid(gx > 0 ? gx : 1, dm.R, L);
     const size_t smem = sizeof(float) * (size_t)a.rows * (kEmaSpan + a.rows);
     return launch_pdl(ema_replay_kernel, grid, dim3(kEmaThreads), smem, s, nullptr, 0, cfg, a);
 }

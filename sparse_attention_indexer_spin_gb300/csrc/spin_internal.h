@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "../../include/spin.h"
+#include "spin_common.cuh"
 
 namespace spin {
 
@@ -27,6 +28,7 @@ struct SelectArgs {
     int32_t* n_union;
     float* block_scores;  // workspace: S [R][rows][MB] fp32, then exploration draws [R][rows][MB] u32
     uint32_t* status;
+    int n_layers;         // layers stacked along the outermost dimension of every array (0 or 1: one)
 };
 
 struct ScoreArgs {
@@ -43,6 +45,7 @@ struct ScoreArgs {
     int rows;
     float* scores;
     uint32_t* status;
+    HintArgs hint;  // rec == NULL: no candidate collection for the hinted top-K
 };
 
 struct EmaArgs {
@@ -58,6 +61,7 @@ struct EmaArgs {
     const int32_t* q_pos;
     const int32_t* accepted;  // NULL: a = 0
     uint32_t* status;
+    int n_layers;             // layers stacked along the outermost dimension (0 or 1: one)
 };
 
 size_t select_workspace_bytes(const spin_config& cfg, int rows);
@@ -79,6 +83,15 @@ cudaError_t launch_topk(const spin_config& cfg, const float* scores, const int32
                         const int32_t* n_list, const int32_t* n_slots, int rows,
                         int32_t* topk_idx, uint32_t* status, cudaStream_t s);
 cudaError_t launch_ema(const spin_config& cfg, const EmaArgs& a, cudaStream_t s);
+
+// Temporal top-K (spin_topk_hint.cu).
+bool topk_hint_supported(const spin_config& cfg);
+int topk_hint_cap(const spin_config& cfg);
+size_t topk_hint_bytes(const spin_config& cfg, int rows);
+HintArgs topk_hint_args(const spin_config& cfg, int rows, void* hint);
+cudaError_t launch_topk_hint(const spin_config& cfg, const float* scores, const float* w, const int32_t* list,
+                             const int32_t* n_list, const int32_t* n_slots, int rows, int32_t* topk_idx,
+                             const HintArgs& h, uint32_t* status, cudaStream_t s);
 
 int device_sm_count();
 

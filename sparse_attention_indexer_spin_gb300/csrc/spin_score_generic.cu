@@ -73,6 +73,13 @@ __global__ void __launch_bounds__(256) score_generic_kernel(spin_config cfg, Sco
             if (z == 0.0f) z = 0.0f;  // no -0 in the output
         }
         a.scores[(((int64_t)req * rows + r) * dm.MB + k) * kBlock + s] = z;
+        // hinted top-K: a live slot (valid block, i < N) at or above its row's threshold
+        if (a.hint.rec && !bad_list && i < n) {
+            const int64_t rr = (int64_t)req * rows + r;
+            const uint32_t thr = hint_threshold(a.hint.rec[rr * kHintWords + kHwGuess], row_wsum(a.w + rr * H, H));
+            const uint32_t key = order_key(z);
+            if (thr != 0u && key >= thr) hint_push(a.hint, rr, key, (uint32_t)(k * kBlock + s));
+        }
     }
 }
 

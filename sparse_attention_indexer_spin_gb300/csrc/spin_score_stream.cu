@@ -216,6 +216,8 @@ score_stream_kernel(spin_config cfg, ScoreArgs a) {
         float qreg[MAXR][C::kU][C::kEPC];
         float wreg[MAXR][C::kU];
         int cur_req = -1;
+        int h_req = -1;        // hinted top-K: request of the cached threshold of this thread's row
+        uint32_t h_thr = 0u;
         for (int ch = c0, it = 0; ch < c1; ++ch, ++it) {
             const int st = it % C::kNST;
             const uint32_t ph = (uint32_t)(it / C::kNST) & 1u;
@@ -304,6 +306,16 @@ score_stream_kernel(spin_config cfg, ScoreArgs a) {
                 const int64_t i = blk * kBlock + (int64_t)g * C::kS + s;
                 if (i >= n || z == 0.0f) z = 0.0f;
                 a.scores[(((int64_t)req * rows + r) * dm.MB + k) * kBlock + g * C::kS + s] = z;
+                // hinted top-K: a live slot (valid block, i < N) at or above its row's threshold
+                if (a.hint.rec && blk >= 0 && blk * kBlock < n && i < n) {
+                    const int64_t rr = (int64_t)req * rows + r;
+                    if (req != h_req) {  // this thread's row r of a new request
+                        h_req = req;
+                        h_thr = hint_threshold(a.hint.rec[rr * kHintWords + kHwGuess], row_wsum(a.w + rr * NH, NH));
+                    }
+                    const uint32_t key = order_key(z);
+                    if (h_thr != 0u && key >= h_thr) hint_push(a.hint, rr, key, (uint32_t)(k * kBlock + g * C::kS + s));
+                }
             }
             if (fail) break;
         }

@@ -58,6 +58,17 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
     pdl_begin();
     if (step_dev) step = *step_dev;
     const Dims dm = dims_of(cfg);
+    {   // layer blockIdx.z of a stack of layers (0 for a one-layer call)
+        const int64_t l = blockIdx.z;
+        V += l * dm.R * dm.max_slots;
+        D += l * dm.R * dm.DL;
+        Vmax += l * dm.R * dm.MB;
+        warm += l * dm.R;
+        if (rho_override) rho_override += l;
+        S += l * dm.R * rows * dm.MB;
+        X += l * dm.R * rows * dm.MB;
+        layer += (int)l;
+    }
     const int rr = blockIdx.y;
     const int req = rr / rows, r = rr - req * rows;
     const int64_t n = n_slots[req], q = q_pos[req];
@@ -230,6 +241,17 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
     __shared__ SelShared sh;
     const Dims dm = dims_of(cfg);
     const int MB = dm.MB;
+    {   // layer blockIdx.y of a stack of layers (0 for a one-layer call)
+        const int64_t l = blockIdx.y;
+        warm += l * dm.R;
+        if (rho_override) rho_override += l;
+        S += l * dm.R * rows * MB;
+        blocks += l * dm.R * rows * MB;
+        n_blocks += l * dm.R * rows;
+        if (union_blocks) union_blocks += l * dm.R * MB;
+        if (n_union) n_union += l * dm.R;
+        layer += (int)l;
+    }
     uint32_t* keys = reinterpret_cast<uint32_t*>(sel_smem);
     uint8_t* flag = sel_smem + (size_t)MB * 4;
     uint8_t* uflag = flag + MB;
@@ -465,6 +487,18 @@ __global__ void __launch_bounds__(kSrThreads, 1) select_reg_kernel(
     __shared__ SrShared sh;
     const Dims dm = dims_of(cfg);
     const int MB = dm.MB;
+    {   // layer blockIdx.y of a stack of layers (0 for a one-layer call)
+        const int64_t l = blockIdx.y;
+        warm += l * dm.R;
+        if (rho_override) rho_override += l;
+        S += l * dm.R * rows * MB;
+        X += l * dm.R * rows * MB;
+        blocks += l * dm.R * rows * MB;
+        n_blocks += l * dm.R * rows;
+        if (union_blocks) union_blocks += l * dm.R * MB;
+        if (n_union) n_union += l * dm.R;
+        layer += (int)l;
+    }
     const int tid = threadIdx.x;
     const int req = blockIdx.x / rows, r = blockIdx.x % rows;  // a cluster = the rows of a request
     const int64_t rr = (int64_t)req * rows + r;
@@ -587,16 +621,19 @@ static size_t select_array_bytes(const spin_config& cfg, int rows) {
 
 size_t select_workspace_bytes(const spin_config& cfg, int rows) { return 2 * select_array_bytes(cfg, rows); }
 
+// Layer stacks: every array of layer l starts l layer-sizes after layer 0's; the workspace
+// holds the n_layers block-score arrays, then the n_layers exploration-draw arrays.
 cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStream_t s) {
     const Dims dm = dims_of(cfg);
-    const bool many_rows = (int64_t)dm.R * a.rows >= 8;
+    const int L = a.n_layers > 1 ? a.n_layers : 1;
+    const bool many_rows = (int64_t)dm.R * a.rows * L >= 8;
     const int per_cta = (256 / 32) * (many_rows ? 16 : 8);
     int gx = (dm.MB + per_cta - 1) / per_cta;
     if (gx > 512) gx = 512;
-    dim3 g1(gx, dm.R * a.rows);
+    dim3 g1(gx, dm.R * a.rows, L);
     float* S = a.block_scores;
     uint32_t* X = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(a.block_scores) +
-                                              select_array_bytes(cfg, a.rows));
+                                              (size_t)L * select_array_bytes(cfg, a.rows));
     cudaError_t e = launch_pdl(many_rows ? block_score_kernel<16> : block_score_kernel<8>, g1, dim3(256), 0, s,
                                nullptr, 0, cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,
                                a.rho_override, cfg.seed, a.step, a.step_dev, a.layer, S, X);
@@ -613,7 +650,7 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
         at[0].val.clusterDim.x = (unsigned)a.rows;
         at[0].val.clusterDim.y = 1;
         at[0].val.clusterDim.z = 1;
-        return launch_pdl(kern, dim3((unsigned)(dm.R * a.rows)), dim3(kSrThreads), 0, s, at, 1, cfg, a.warm,
+        return launch_pdl(kern, dim3((unsigned)(dm.R * a.rows), (unsigned)L), dim3(kSrThreads), 0, s, at, 1, cfg, a.warm,
                           a.n_slots, a.q_pos, a.rows, a.rho_override, a.step, a.layer, (const float*)S,
                           (const uint32_t*)X, a.blocks, a.n_blocks, a.union_blocks, a.n_union, a.status);
     }
@@ -622,7 +659,7 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
         e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(select_kernel, dim3(dm.R), dim3(kSelThreads), smem, s, nullptr, 0, cfg, a.warm, a.n_slots,
+    return launch_pdl(select_kernel, dim3(dm.R, L), dim3(kSelThreads), smem, s, nullptr, 0, cfg, a.warm, a.n_slots,
                       a.q_pos, a.rows, a.rho_override, a.step, a.layer, (const float*)a.block_scores, a.blocks,
                       a.n_blocks, a.union_blocks, a.n_union, a.status, a.step_dev);
 }

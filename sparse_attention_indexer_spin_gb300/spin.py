@@ -37,6 +37,10 @@ class SpinError(RuntimeError):
         self.code = code
 
 
+class SpinScoreExtras(ctypes.Structure):
+    _fields_ = [("topk_hint", ctypes.c_void_p), ("topk_hint_bytes", ctypes.c_size_t)]
+
+
 class SpinConfig(ctypes.Structure):
     _fields_ = [
         ("n_req", ctypes.c_int32), ("max_slots", ctypes.c_int32), ("max_rows", ctypes.c_int32),
@@ -89,7 +93,16 @@ def lib():
             "spin_select_blocks_noalloc": [C, P, P, P, P, P, P, i32, P, u64, i32, P, P, P, P, P, P],
             "spin_select_blocks_dstep": [C, P, P, P, P, P, P, i32, P, P, i32, P, P, P, P, P,
                                          ctypes.c_size_t, P, P],
+            "spin_select_blocks_layers": [C, i32, i32, P, P, P, P, P, P, i32, P, u64, P, P, P, P, P,
+                                          P, ctypes.c_size_t, P, P],
+            "spin_update_ema_layers": [C, i32, P, P, P, P, P, P, P, P, P, P, P],
+            "spin_commit_mtp_layers": [C, i32, P, P, P, P, P, i32, P, P, P, P, P, P, P],
             "spin_indexer_score": [C, P, P, P, P, i64, P, i64, P, P, P, i32, P, P, P],
+            "spin_indexer_score_ex": [C, P, P, P, P, i64, P, i64, P, P, P, i32, P,
+                                      ctypes.POINTER(SpinScoreExtras), P, P],
+            "spin_topk_hint_size": [C, i32, ctypes.POINTER(ctypes.c_size_t)],
+            "spin_init_topk_hint": [C, i32, P, ctypes.c_size_t, i32, P],
+            "spin_topk_hinted": [C, P, P, P, P, P, i32, P, P, ctypes.c_size_t, P, P],
             "spin_topk": [C, P, P, P, P, i32, P, P, P],
             "spin_update_ema": [C, P, P, P, P, P, P, P, P, P, P, P],
             "spin_commit_mtp": [C, P, P, P, P, P, i32, P, P, P, P, P, P, P],
@@ -199,6 +212,34 @@ def select_blocks(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, ste
         _ptr(union_blocks), _ptr(n_union), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
 
 
+def select_blocks_layers(cfg, n_layers, layer0, V, D, Vmax, warm, n_slots, q_pos, rows, rho_table,
+                         step, blocks, n_blocks, union_blocks, n_union, workspace, status, stream=None):
+    """Selections of n_layers stacked layers (arrays [L][...]) in one launch.  `step` is an int
+    or a one-element int64 device tensor read when the kernels run."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    step_dev = step if isinstance(step, torch.Tensor) else None
+    _check(lib().spin_select_blocks_layers(
+        ctypes.byref(cfg), int(n_layers), int(layer0), _ptr(V), _ptr(D), _ptr(Vmax), _ptr(warm),
+        _ptr(n_slots), _ptr(q_pos), rows, _ptr(rho_table), 0 if step_dev is not None else int(step),
+        _ptr(step_dev), _ptr(blocks), _ptr(n_blocks), _ptr(union_blocks), _ptr(n_union),
+        _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+
+
+def update_ema_layers(cfg, n_layers, V, D, Vmax, warm, scores, list_, n_list, n_slots, q_pos, status,
+                      stream=None):
+    _check(lib().spin_update_ema_layers(ctypes.byref(cfg), int(n_layers), _ptr(V), _ptr(D), _ptr(Vmax),
+                                        _ptr(warm), _ptr(scores), _ptr(list_), _ptr(n_list),
+                                        _ptr(n_slots), _ptr(q_pos), _ptr(status), _stream(stream)))
+
+
+def commit_mtp_layers(cfg, n_layers, V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots,
+                      q_pos, accepted, status, stream=None):
+    _check(lib().spin_commit_mtp_layers(ctypes.byref(cfg), int(n_layers), _ptr(V), _ptr(D), _ptr(Vmax),
+                                        _ptr(warm), _ptr(scores), rows, _ptr(union_blocks),
+                                        _ptr(n_union), _ptr(n_slots), _ptr(q_pos), _ptr(accepted),
+                                        _ptr(status), _stream(stream)))
+
+
 def select_blocks_noalloc(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer,
                           blocks, n_blocks, union_blocks, n_union, status, stream=None):
     """spin_select_blocks without a workspace: for callers that cannot allocate device
@@ -215,6 +256,65 @@ def indexer_score(cfg, q, w, k_pool, k_scale, n_pages, block_table, list_, n_lis
         ctypes.byref(cfg), _ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), int(n_pages),
         _ptr(block_table), block_table.shape[-1], _ptr(list_), _ptr(n_list), _ptr(n_slots), rows,
         _ptr(scores), _ptr(status), _stream(stream)))
+
+
+def indexer_score_ex(cfg, q, w, k_pool, k_scale, n_pages, block_table, list_, n_list, n_slots, rows,
+                     scores, status, topk_hint=None, stream=None):
+    """spin_indexer_score_ex: the score kernel also collects the hinted top-K's candidates
+    into `topk_hint` (a TopkHint)."""
+    ex = SpinScoreExtras()
+    if topk_hint is not None:
+        ex.topk_hint = topk_hint.buf.data_ptr()
+        ex.topk_hint_bytes = topk_hint.nbytes
+    _check(lib().spin_indexer_score_ex(
+        ctypes.byref(cfg), _ptr(q), _ptr(w), _ptr(k_pool), _ptr(k_scale), int(n_pages),
+        _ptr(block_table), block_table.shape[-1], _ptr(list_), _ptr(n_list), _ptr(n_slots), rows,
+        _ptr(scores), ctypes.byref(ex), _ptr(status), _stream(stream)))
+
+
+def topk_hint_size(cfg: SpinConfig, rows: int = 1) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().spin_topk_hint_size(ctypes.byref(cfg), rows, ctypes.byref(out)))
+    return int(out.value)
+
+
+def init_topk_hint(cfg, rows, hint, req=-1, stream=None):
+    _check(lib().spin_init_topk_hint(ctypes.byref(cfg), rows, _ptr(hint.buf), hint.nbytes, int(req),
+                                     _stream(stream)))
+
+
+def topk_hinted(cfg, scores, w, list_, n_list, n_slots, rows, topk_idx, hint, status, stream=None):
+    _check(lib().spin_topk_hinted(ctypes.byref(cfg), _ptr(scores), _ptr(w), _ptr(list_), _ptr(n_list),
+                                  _ptr(n_slots), rows, _ptr(topk_idx), _ptr(hint.buf), hint.nbytes,
+                                  _ptr(status), _stream(stream)))
+
+
+HINT_WORDS = 16
+HINT_FIELDS = ("guess", "count", "extra", "hit", "miss", "overflow", "cold", "exact", "last")
+
+
+class TopkHint:
+    """Device buffer of the temporal top-K hint (allocated by PyTorch), zeroed on creation."""
+
+    def __init__(self, cfg: SpinConfig, rows: int = 1, device="cuda"):
+        self.cfg, self.rows = cfg, rows
+        self.nbytes = topk_hint_size(cfg, rows)
+        self.buf = torch.zeros(((self.nbytes + 255) // 256) * 256, dtype=torch.uint8, device=device)
+        assert self.buf.data_ptr() % 256 == 0
+
+    def reset(self, req=-1, stream=None):
+        init_topk_hint(self.cfg, self.rows, self, req, stream)
+
+    def records(self):
+        """uint32 [n_req * rows][HINT_WORDS] copy of the records (synchronises)."""
+        n = self.cfg.n_req * self.rows * HINT_WORDS
+        return self.buf[: 4 * n].view(torch.int32).view(-1, HINT_WORDS).cpu().numpy().view("uint32")
+
+    def stats(self):
+        """Totals over all rows of the hit / miss / overflow / cold / exact counters."""
+        r = self.records().astype("int64")
+        return {f: int(r[:, i].sum()) for i, f in enumerate(HINT_FIELDS) if f in
+                ("hit", "miss", "overflow", "cold", "exact")}
 
 
 def topk(cfg, scores, list_, n_list, n_slots, rows, topk_idx, status, stream=None):
@@ -276,9 +376,11 @@ class StepBuffers:
 
 def run_step(cfg, state: LayerState, buf: StepBuffers, q, w, k_pool, k_scale, n_pages,
              block_table, n_slots, q_pos, step=0, layer=0, rho_override=None, accepted=None,
-             stream=None):
+             stream=None, hint: Optional[TopkHint] = None):
     """One decode step of one layer through the C ABI: select -> score -> top-K -> EMA
-    (or, with rows > 1, select -> union -> score -> top-K -> deferred commit)."""
+    (or, with rows > 1, select -> union -> score -> top-K -> deferred commit).  With a
+    TopkHint the score kernel collects the temporal top-K's candidates and the hinted top-K
+    replaces the plain one."""
     rows = buf.rows
     union = buf.union if rows > 1 else None
     n_union = buf.n_union if rows > 1 else None
@@ -290,9 +392,14 @@ def run_step(cfg, state: LayerState, buf: StepBuffers, q, w, k_pool, k_scale, n_
         nlist = buf.n_blocks
     else:
         blist, nlist = buf.union, buf.n_union
-    indexer_score(cfg, q, w, k_pool, k_scale, n_pages, block_table, blist, nlist, n_slots, rows,
-                  buf.scores, buf.status, stream)
-    topk(cfg, buf.scores, blist, nlist, n_slots, rows, buf.topk, buf.status, stream)
+    if hint is None:
+        indexer_score(cfg, q, w, k_pool, k_scale, n_pages, block_table, blist, nlist, n_slots, rows,
+                      buf.scores, buf.status, stream)
+        topk(cfg, buf.scores, blist, nlist, n_slots, rows, buf.topk, buf.status, stream)
+    else:
+        indexer_score_ex(cfg, q, w, k_pool, k_scale, n_pages, block_table, blist, nlist, n_slots,
+                         rows, buf.scores, buf.status, hint, stream)
+        topk_hinted(cfg, buf.scores, w, blist, nlist, n_slots, rows, buf.topk, hint, buf.status, stream)
     if rows == 1:
         update_ema(cfg, state.V, state.D, state.Vmax, state.warm, buf.scores, blist, nlist,
                    n_slots, q_pos, buf.status, stream)

@@ -38,7 +38,7 @@ class Harness:
         self.tol = TOL[wl.k_dtype]
 
     def step(self, step, layer, q, w, qp, rho_override=None, accepted=None, check=True,
-             score_requests=None):
+             score_requests=None, hint=None):
         wl, cfg, st, buf, inp = self.wl, self.cfg, self.states[layer], self.buf, self.inp
         rows = wl.rows
         pre = dict(V=np_(st.V).copy(), D=np_(st.D).copy(), warm=np_(st.warm).copy())
@@ -46,7 +46,8 @@ class Harness:
         qpn = np_(qp).copy()
         buf.status.zero_()
         spin.run_step(cfg, st, buf, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
-                      inp.block_table, inp.n_slots, qp, step, layer, rho_override, accepted)
+                      inp.block_table, inp.n_slots, qp, step, layer, rho_override, accepted,
+                      hint=hint)
         torch.cuda.synchronize()
         if not check:
             return None
