@@ -48,8 +48,9 @@ def parse():
     p.add_argument("--rho", type=int, default=None, help="target sparsity in basis points")
     p.add_argument("--combine", choices=["max", "sum"], default=None,
                    help="predicted slot score: max(V, D) (Eq. 1) or V + D")
-    p.add_argument("--topk", choices=["hinted", "plain"], default="hinted",
-                   help="temporal top-K seeded by the previous step's threshold, or the plain one")
+    p.add_argument("--topk", choices=["auto", "hinted", "plain"], default="auto",
+                   help="temporal top-K seeded by the previous step's threshold, the plain one, or "
+                        "auto: the temporal one for one query row, the plain one for several")
     p.add_argument("--schedule", choices=["stacked", "serial"], default="stacked",
                    help="one selection and one EMA launch per step for all layers, or layer by layer")
     p.add_argument("--no-configs", action="store_true", help="skip the per-workload measurements")
@@ -179,6 +180,8 @@ class Workload:
                  topk: str = "hinted", schedule: str = "stacked"):
         from sparse_attention_indexer_spin_gb300 import spin
         self.spin = spin
+        if topk == "auto":
+            topk = "hinted" if wl.rows == 1 else "plain"
         self.topk_mode, self.schedule = topk, schedule
         self.wl = wl = wl.replace(steps=max(wl.steps, n_steps), rho_bp=rho_bp)
         self.cfg = spin.make_config(**wl.config_fields())
@@ -286,6 +289,8 @@ class Workload:
             spin.topk(cfg, sc, lst, nl, ns, rows, tk, self.buf.status)
         else:
             spin.topk_hinted(cfg, sc, w, lst, nl, ns, rows, tk, hint, self.buf.status)
+        if ev is not None:
+            ev[2].record()
 
     def step(self, s, ev_score=None, q_override=None, w_override=None, on_topk=None):
         spin, cfg, rows, L = self.spin, self.cfg, self.rows, self.L
@@ -299,7 +304,7 @@ class Workload:
                                       self.unions[s] if rows > 1 else None,
                                       self.n_unions[s] if rows > 1 else None, self.workspace, status)
             for layer in range(L):
-                ev = None if ev_score is None else (ev_score[0][layer], ev_score[1][layer])
+                ev = None if ev_score is None else (ev_score[0][layer], ev_score[1][layer], ev_score[2][layer])
                 self.score_topk(s, layer, qs[layer], ws[layer], ev)
                 if on_topk is not None:
                     on_topk(layer)
@@ -316,7 +321,7 @@ class Workload:
             spin.select_blocks(cfg, lst_st.V, lst_st.D, lst_st.Vmax, lst_st.warm, ns, qp, rows, None, s, layer,
                                self.blocks[s, layer], self.n_blocks[s, layer], un, nu, self.buf.workspace,
                                status)
-            ev = None if ev_score is None else (ev_score[0][layer], ev_score[1][layer])
+            ev = None if ev_score is None else (ev_score[0][layer], ev_score[1][layer], ev_score[2][layer])
             self.score_topk(s, layer, qs[layer], ws[layer], ev)
             if on_topk is not None:
                 on_topk(layer)
@@ -376,24 +381,26 @@ class Workload:
         return out
 
 
-def time_steps(wk, steps, with_score_events=False):
+def time_steps(wk, steps, with_score_events=False, topk_ms=None):
     """Run `steps` (list of step indices); returns (elapsed ms, per-score-launch ms list).
-    With score events the score launches are bracketed by CUDA events on the stream (which
-    also cuts the launch chaining at them): used for the score kernel's own time only."""
-    ev_pairs = []
+    With score events the score and top-K launches are bracketed by CUDA events on the
+    stream (which also cuts the launch chaining at them): used for those kernels' own times
+    only; the top-K times are appended to `topk_ms` when given."""
+    ev_sets = []
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for s in steps:
         ev = None
         if with_score_events:
-            ev = ([torch.cuda.Event(enable_timing=True) for _ in range(wk.L)],
-                  [torch.cuda.Event(enable_timing=True) for _ in range(wk.L)])
-            ev_pairs.append(ev)
+            ev = tuple([torch.cuda.Event(enable_timing=True) for _ in range(wk.L)] for _ in range(3))
+            ev_sets.append(ev)
         wk.step(s, ev)
     t1.record()
     torch.cuda.synchronize()
-    score_ms = [a.elapsed_time(b) for ev in ev_pairs for a, b in zip(ev[0], ev[1])]
+    score_ms = [a.elapsed_time(b) for ev in ev_sets for a, b in zip(ev[0], ev[1])]
+    if topk_ms is not None:
+        topk_ms.extend(a.elapsed_time(b) for ev in ev_sets for a, b in zip(ev[1], ev[2]))
     return t0.elapsed_time(t1), score_ms
 
 
@@ -586,7 +593,9 @@ def measure_workload(base, rho, W, K, topk, schedule, share=None, score_events=T
         # the score kernel's own launches, timed separately (events cut the launch chaining)
         wk.reset()
         time_steps(wk, range(W))
-        _, score_ms = time_steps(wk, range(W, W + K), with_score_events=True)
+        tk_ms = []
+        _, score_ms = time_steps(wk, range(W, W + K), with_score_events=True, topk_ms=tk_ms)
+        rec["topk_us"] = 1000.0 * float(np.mean(tk_ms))
         avg = float(np.mean(score_ms))
         unique = wk.scored_slots(range(W, W + K), unique=True)
         alg = float(np.mean(unique)) * (wk.key_bytes_per_slot() + 4 * wk.rows)
@@ -691,8 +700,10 @@ def main():
     # dominant kernel: the indexer score, its launches bracketed by events on the stream
     wk.reset()
     time_steps(wk, range(W))
-    _, score_ms = time_steps(wk, range(W, W + K), with_score_events=True)
+    tk_ms = []
+    _, score_ms = time_steps(wk, range(W, W + K), with_score_events=True, topk_ms=tk_ms)
     avg_score_ms = float(np.mean(score_ms))
+    avg_topk_us = 1000.0 * float(np.mean(tk_ms))
     kbytes = wk.key_bytes_per_slot()
     unique_per_launch = wk.scored_slots(range(W, W + K), unique=True)
     # keys (+ FP8 scale) of every scored slot once, plus one fp32 score per slot and row
@@ -798,7 +809,7 @@ def main():
             "clocks": clk,
             "dense": dense,
             "realized_sparsity": realized,
-            "topk": {"mode": args.topk, "hint": hint_stats},
+            "topk": {"mode": args.topk, "hint": hint_stats, "avg_launch_us": avg_topk_us},
             "per_config": per_config,
             "status": status,
         }

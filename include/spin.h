@@ -249,9 +249,10 @@ spin_status_t spin_indexer_score(const spin_config* cfg, const void* q, const fl
 /* Optional work fused into spin_indexer_score_ex (zero-initialise, then set what is wanted). */
 typedef struct spin_score_extras {
     /* Temporal top-K (see spin_topk_hinted): a hint buffer of at least topk_hint_bytes bytes
-     * (spin_topk_hint_size).  The score kernel compares every fresh score with its row's
-     * guess and appends the live slots at or above it to the hint; the next
-     * spin_topk_hinted call on the same rows consumes them.  NULL: nothing is collected. */
+     * (spin_topk_hint_size).  The streaming and generic score kernels then compare every
+     * fresh score with its row's threshold and append the live slots at or above it to the
+     * hint, for the next spin_topk_hinted call on the same rows; the tensor-core kernel
+     * leaves that to spin_topk_hinted.  NULL: nothing is collected. */
     void* topk_hint;
     size_t topk_hint_bytes;
 } spin_score_extras;
@@ -285,9 +286,11 @@ spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32
  *     step and whenever spin_init_state resets a request.
  *   - A step is spin_indexer_score_ex with extras->topk_hint = hint, then spin_topk_hinted
  *     on the same scores, head weights w ([R][rows][n_heads], those the scores were computed
- *     with), list and rows with the same hint.  The score kernel collects the live slots
- *     whose score is >= the row's threshold: the guess times this step's sum_h |w_h|.  If K
- *     to cap of them were found (cap = 4 K rounded up to a power of two, at least 4096), the
+ *     with), list and rows with the same hint.  The live slots whose score is >= the row's
+ *     threshold (the guess times this step's sum_h |w_h|) are the candidates, collected by
+ *     the score kernel or, where it does not, by spin_topk_hinted in one pass.  If K
+ *     to cap of them were found (cap = 8 K rounded up to a power of two, at least 4096, or
+ *     4 K when 8 K candidates would not fit in shared memory beside the list), the
  *     top-K is selected among them; otherwise (no guess yet, too few, too many) the row is
  *     recomputed from its scores.  The score at rank K + margin divided by sum_h |w_h|
  *     becomes the next step's guess; the margin (initially sqrt(K cap) - K, within
@@ -295,7 +298,8 @@ spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32
  *   - Calling spin_indexer_score_ex twice with one hint without a spin_topk_hinted in
  *     between mixes two steps' candidates; the count then usually exceeds cap and the row is
  *     recomputed (still exact), unless fewer than cap were collected in total -- so do not.
- *   - Supported for top_k <= 2048 and at most 8192 blocks (ceil(max_slots/64)); other
+ *   - Supported for top_k <= 2048 and at most 8192 blocks (ceil(max_slots/64)) when the
+ *     candidates, a one-bit-per-slot bitmap and the list fit in 220 KB of shared memory; other
  *     shapes get SPIN_ERR_UNSUPPORTED from all three calls. */
 spin_status_t spin_topk_hint_size(const spin_config* cfg, int32_t rows, size_t* bytes);
 spin_status_t spin_init_topk_hint(const spin_config* cfg, int32_t rows, void* hint,

@@ -72,7 +72,9 @@ enum HintWord {
     kHwOver = 5,     // steps whose guess found more candidates than fit
     kHwCold = 6,     // steps without a guess
     kHwGlobal = 7,   // cold steps whose boundary bin did not fit: exact passes over the scores
-    kHwLast = 8      // the last step's candidate count
+    kHwLast = 8,     // the last step's candidate count
+    kHwFlags = 9     // bit 0: this step's score kernel collected the candidates (else the
+                     // top-K kernel collects them from the scores)
 };
 
 struct HintArgs {
@@ -86,11 +88,20 @@ __device__ __forceinline__ float key_float(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// sum_h |w_h| of one row's n head weights (in head order).
+// sum_h |w_h| of one row's n head weights by one thread: four interleaved partial sums
+// (h mod 4), so the loads of a row are in flight together; a fixed order for a given n.
 __device__ __forceinline__ float row_wsum(const float* w, int n) {
-    float s = 0.0f;
-    for (int h = 0; h < n; ++h) s = __fadd_rn(s, fabsf(w[h]));
-    return s;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    int h = 0;
+#pragma unroll 4
+    for (; h + 4 <= n; h += 4) {
+        s0 = __fadd_rn(s0, fabsf(w[h]));
+        s1 = __fadd_rn(s1, fabsf(w[h + 1]));
+        s2 = __fadd_rn(s2, fabsf(w[h + 2]));
+        s3 = __fadd_rn(s3, fabsf(w[h + 3]));
+    }
+    for (; h < n; ++h) s0 = __fadd_rn(s0, fabsf(w[h]));
+    return __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
 }
 
 // Threshold key of a row for this step: the normalised guess times the step's sum of |w_h|
@@ -109,21 +120,6 @@ __device__ __forceinline__ unsigned long long hint_entry(uint32_t key, uint32_t 
 __device__ __forceinline__ void hint_push(const HintArgs& h, int64_t rr, uint32_t key, uint32_t pos) {
     const uint32_t at = atomicAdd(h.rec + rr * kHintWords + kHwCount, 1u);
     if (at < (uint32_t)h.cap) h.cand[rr * h.cap + at] = hint_entry(key, pos);
-}
-
-// The same for a full warp whose lanes belong to one (request, row): one atomic per warp.
-__device__ __forceinline__ void hint_push_warp(const HintArgs& h, int64_t rr, bool take, uint32_t key,
-                                               uint32_t pos) {
-    const unsigned m = __ballot_sync(0xffffffffu, take);
-    if (m == 0u) return;
-    const int lane = threadIdx.x & 31, lead = __ffs(m) - 1;
-    uint32_t base = 0;
-    if (lane == lead) base = atomicAdd(h.rec + rr * kHintWords + kHwCount, (uint32_t)__popc(m));
-    base = __shfl_sync(0xffffffffu, base, lead);
-    if (take) {
-        const uint32_t at = base + (uint32_t)__popc(m & ((1u << lane) - 1u));
-        if (at < (uint32_t)h.cap) h.cand[rr * h.cap + at] = hint_entry(key, pos);
-    }
 }
 
 // ---------------------------------------------------------------------------------------

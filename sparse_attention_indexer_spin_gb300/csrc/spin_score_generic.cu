@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(256) score_generic_kernel(spin_config cfg, Sco
         if (a.hint.rec && !bad_list && i < n) {
             const int64_t rr = (int64_t)req * rows + r;
             const uint32_t thr = hint_threshold(a.hint.rec[rr * kHintWords + kHwGuess], row_wsum(a.w + rr * H, H));
+            a.hint.rec[rr * kHintWords + kHwFlags] = 1u;  // (every writer stores the same value)
             const uint32_t key = order_key(z);
             if (thr != 0u && key >= thr) hint_push(a.hint, rr, key, (uint32_t)(k * kBlock + s));
         }

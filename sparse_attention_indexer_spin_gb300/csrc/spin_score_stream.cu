@@ -312,6 +312,7 @@ score_stream_kernel(spin_config cfg, ScoreArgs a) {
                     if (req != h_req) {  // this thread's row r of a new request
                         h_req = req;
                         h_thr = hint_threshold(a.hint.rec[rr * kHintWords + kHwGuess], row_wsum(a.w + rr * NH, NH));
+                        a.hint.rec[rr * kHintWords + kHwFlags] = 1u;  // (every writer stores the same value)
                     }
                     const uint32_t key = order_key(z);
                     if (h_thr != 0u && key >= h_thr) hint_push(a.hint, rr, key, (uint32_t)(k * kBlock + g * C::kS + s));

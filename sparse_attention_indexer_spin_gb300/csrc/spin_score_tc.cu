@@ -626,7 +626,6 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         const int m = quarter * 32 + lane;      // slot row of the tile = TMEM lane
         const int h = m >> 6, s = m & 63;
         float* wloc = sW + (size_t)(wid - kTcEpiWarp0) * NQ;
-        uint32_t hg0 = 0u, hg1 = 0u, hg2 = 0u, hg3 = 0u;  // the rows' thresholds (hinted top-K)
         int cur_req = -1;
         for (int t = t0 + (split_rows ? 0 : parity), it = split_rows ? 0 : parity; t < t1; t += tstep, it += tstep) {
             // FP8: this slot's scale, from the scale-ring entry the producer filled for tile it
@@ -654,18 +653,6 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                                         (((int64_t)req * rows + r) * kTcNH + hh) * kTcD);
                     }
                     wloc[n] = a.w[(int64_t)req * rows * kTcNH + n] * g;
-                }
-                if (a.hint.rec) {  // lane r: row r's threshold for this step
-                    uint32_t thr = 0u;
-                    if (lane < rows) {
-                        const int64_t rr = (int64_t)req * rows + lane;
-                        thr = hint_threshold(a.hint.rec[rr * kHintWords + kHwGuess], row_wsum(a.w + rr * kTcNH, kTcNH));
-                    }
-                    static_assert(kTcMaxRows == 4, "one register per row");
-                    hg0 = __shfl_sync(0xffffffffu, thr, 0);
-                    hg1 = __shfl_sync(0xffffffffu, thr, 1);
-                    hg2 = __shfl_sync(0xffffffffu, thr, 2);
-                    hg3 = __shfl_sync(0xffffffffu, thr, 3);
                 }
                 __syncwarp();
                 cur_req = req;
@@ -707,12 +694,6 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             };
             auto emit = [&](float z, int r) {
                 if (listed) a.scores[(((int64_t)req * rows + r) * dm.MB + k) * kBlock + s] = z;
-                if (a.hint.rec) {  // hinted top-K: live slots at or above the row's guess (warp-uniform)
-                    const uint32_t gk = r == 0 ? hg0 : r == 1 ? hg1 : r == 2 ? hg2 : hg3;
-                    const uint32_t key = order_key(z);
-                    const bool take = gk != 0u && blk >= 0 && (int64_t)blk * kBlock + s < ti.n && key >= gk;
-                    hint_push_warp(a.hint, (int64_t)req * rows + r, take, key, (uint32_t)(k * kBlock + s));
-                }
             };
             // this warp's rows (paired TMEM loads measured slower)
             const int rstep = split_rows ? 2 : 1;

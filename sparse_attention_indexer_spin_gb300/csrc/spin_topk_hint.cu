@@ -6,11 +6,13 @@
 // decode steps of one request score the same context with a slowly drifting query, so the
 // K-th score moves little from one step to the next.
 //
-//   guess   the score kernel of this step (spin_indexer_score_ex with the hint) already
-//           compared every fresh score with the row's threshold -- the previous step's score
-//           at rank K + extra, divided by that step's sum_h |w_h| and multiplied by this
-//           step's (the head weights of a step scale all its scores together) -- and appended
-//           those at or above it to the row's candidate array (a few per cent of the slots);
+//   guess   every live fresh score is compared with the row's threshold -- the previous
+//           step's score at rank K + extra, divided by that step's sum_h |w_h| and multiplied
+//           by this step's (the head weights of a step scale all its scores together) -- and
+//           those at or above it (a few per cent of the slots) become the candidates.  The
+//           streaming and generic score kernels (spin_indexer_score_ex with the hint) do this
+//           as they write the scores and mark the record; otherwise (the tensor-core kernel,
+//           whose epilogue is its bottleneck) this kernel does it in one pass over the scores;
 //   verify  if at least K and at most cap candidates were found, the top-K lies among them:
 //           the K-th key T is >= the guess because K keys are, so every key > T and every
 //           key == T was collected;
@@ -18,14 +20,18 @@
 //           complement of the list position, all distinct) gives the K largest entries;
 //           they are marked in a bitmap of list positions and written in ascending slot
 //           order.  The score at rank K + extra, normalised, becomes the next step's guess.
+// The candidates' keys all lie between their minimum and maximum, so the radix digits start
+// below the bits those two share; the first digit pass also places rank K + extra, whose
+// bin's lower edge, normalised, becomes the next step's guess.
 // A row without a guess, or whose guess found too few or too many candidates, takes the
-// cold path: one pass over its scores builds a histogram of the top 12 key bits, the bin
-// holding rank K + extra bounds the candidates (refined by the next 12, then the last 8
-// bits while that bin alone overflows the candidate array), a last pass collects them, and
-// the same refine step follows.  The margin `extra` starts at the geometric middle of [K, cap] minus K,
-// doubles after a miss and halves after an overflow.  Only a boundary bin too large for the candidate array (massive ties) falls
-// back to exact radix passes over the scores.  Every path returns exactly the top-K of
-// spin_topk; the hint only decides how fast.
+// cold path: one pass over its scores counts the live keys and finds their minimum and
+// maximum; 12-bit histograms below the shared bits place rank K + extra (refined 12 bits
+// at a time while its bin alone overflows the candidate array); a last pass collects every
+// live key at or above that bin, and the same refine step follows.  The margin `extra`
+// starts at the geometric middle of [K, cap] minus K, doubles after a miss and halves
+// after an overflow.  Only a boundary bin too large for the candidate array (massive ties)
+// falls back to exact radix passes over the scores.  Every path returns exactly the top-K
+// of spin_topk; the hint only decides how fast.
 //
 // One 1024-thread CTA per (request, row).  Shared memory: the candidates (cap 8-byte
 // entries), the position bitmap (2 words per list entry) and the row's list.
@@ -36,24 +42,34 @@
 namespace spin {
 
 constexpr int kThThreads = 1024;
-constexpr int kThMaxK = 2048;        // cap = 4K rounded up to a power of two, <= 8192
+constexpr int kThMaxK = 2048;        // cap <= 16384 candidates (128 KB of shared memory)
 constexpr int kThMaxBlocks = 8192;   // bitmap of the list positions: <= 64 KB
 constexpr int kThBinsA = 4096;       // cold pass: top 12 bits of the key
 constexpr int kThBins = 2048;        // candidate radix: 11-bit digits of the 64-bit entry
+constexpr size_t kThSmemBudget = 220 * 1024;
 
 struct ThShared {
-    int hist[kThBinsA];
+    __align__(16) int hist[kThBinsA];
     int scan[33];
     int ncand;
-    int digit, above, nbin;
-    TopkShared exact;  // the exact fallback's own scratch
+    int digit, above, nbin, gdigit;
+    uint32_t kmin, kmax;  // smallest and largest key of the candidates (or live keys)
+    float wsum;           // sum_h |w_h| of the row
+    TopkShared exact;     // the exact fallback's own scratch
 };
 
 static_assert(kThThreads == kTopkThreads, "the exact fallback runs with the same CTA");
 
+static size_t th_smem_bytes(const spin_config& cfg, int cap) {
+    return ((sizeof(ThShared) + 15) & ~(size_t)15) + (size_t)cap * 8 + (size_t)dims_of(cfg).MB * 12;
+}
+
+// Candidate capacity per row: 8 K rounded up to a power of two (at least 4096), or 4 K when
+// that does not fit in shared memory next to the bitmap and the list.
 int topk_hint_cap(const spin_config& cfg) {
     int c = 4096;
-    while (c < 4 * cfg.top_k) c <<= 1;
+    while (c < 8 * cfg.top_k) c <<= 1;
+    if (th_smem_bytes(cfg, c) > kThSmemBudget && c > 4096 && c / 2 >= 4 * cfg.top_k) c /= 2;
     return c;
 }
 
@@ -65,7 +81,8 @@ __device__ __forceinline__ uint32_t th_default_extra(int K, int cap) {
 }
 
 bool topk_hint_supported(const spin_config& cfg) {
-    return cfg.top_k <= kThMaxK && dims_of(cfg).MB <= kThMaxBlocks;
+    return cfg.top_k <= kThMaxK && dims_of(cfg).MB <= kThMaxBlocks &&
+           th_smem_bytes(cfg, topk_hint_cap(cfg)) <= kThSmemBudget;
 }
 
 static size_t hint_rec_bytes(const spin_config& cfg, int rows) {
@@ -92,46 +109,105 @@ __device__ __forceinline__ int th_block_sum(int v, ThShared& sh) {
     return tot;
 }
 
-// Digit search over `nbins` bins, scanned from the top: the bin d with
-// (# in bins > d) < kk <= (# in bins >= d).  Thread t owns nbins / 1024 consecutive bins in
-// descending order.  Leaves d, the count above it and the bin's own count in sh.
-__device__ __forceinline__ void th_find_digit(const int* hist, int nbins, int kk, ThShared& sh) {
-    const int per = nbins / kThThreads;
-    const int top = nbins - 1 - (int)threadIdx.x * per;
-    int c = 0;
-    for (int b = 0; b < per; ++b) c += hist[top - b];
-    int tot;
-    const int excl = block_excl_scan(c, sh.scan, &tot);
-    if (excl < kk && excl + c >= kk) {
-        int above = excl;
-        for (int b = 0; b < per; ++b) {
+// Digit search over `nbins` bins (a multiple of 128), scanned from the top, by warp 0 alone:
+// the bin d with (# in bins > d) < kk <= (# in bins >= d), for kk and (when kk2 > 0) kk2.
+// Lane l first sums its nbins / 32 consecutive bins (16-byte reads); the lane whose range
+// holds the rank is then scanned by the whole warp, nbins / 1024 bins a lane.  Leaves d, the
+// count above it and the bin's own count in sh (and kk2's digit in sh.gdigit); the caller's
+// barrier publishes them.  1 <= kk, kk2 <= the total.
+__device__ __forceinline__ void th_find_one(const int* hist, int nbins, int inc, int c, int kk, int* digit,
+                                            int* above_out, int* nbin) {
+    const int lane = threadIdx.x & 31;
+    const int per = nbins / 32;
+    const int src = __ffs(__ballot_sync(0xffffffffu, inc >= kk)) - 1;
+    const int above0 = __shfl_sync(0xffffffffu, inc - c, src);
+    const int q = per / 32;
+    const int top = nbins - 1 - src * per - lane * q;
+    int c2 = 0;
+    for (int b = 0; b < q; ++b) c2 += hist[top - b];
+    const int inc2 = above0 + warp_incl_scan(c2);
+    const int src2 = __ffs(__ballot_sync(0xffffffffu, inc2 >= kk)) - 1;
+    if (lane == src2) {
+        int above = inc2 - c2;
+        for (int b = 0; b < q; ++b) {
             const int h = hist[top - b];
             if (above + h >= kk) {
-                sh.digit = top - b;
-                sh.above = above;
-                sh.nbin = h;
+                *digit = top - b;
+                *above_out = above;
+                *nbin = h;
                 break;
             }
             above += h;
         }
     }
+}
+
+__device__ __forceinline__ void th_find_digit_warp(const int* hist, int nbins, int kk, int kk2, ThShared& sh) {
+    const int lane = threadIdx.x & 31;
+    const int per = nbins / 32;
+    const int4* h4 = reinterpret_cast<const int4*>(hist + (nbins - (lane + 1) * per));
+    int c = 0;
+#pragma unroll 4
+    for (int j = 0; j < per / 4; ++j) {
+        const int4 v = h4[j];
+        c += v.x + v.y + v.z + v.w;
+    }
+    const int inc = warp_incl_scan(c);
+    th_find_one(hist, nbins, inc, c, kk, &sh.digit, &sh.above, &sh.nbin);
+    if (kk2 > 0) {
+        int a2, n2;
+        th_find_one(hist, nbins, inc, c, kk2, &sh.gdigit, &a2, &n2);
+    }
+}
+
+// The same over the whole CTA (every thread gets the result; ends with a barrier).
+__device__ __forceinline__ void th_find_digit(const int* hist, int nbins, int kk, ThShared& sh, int kk2 = 0) {
+    if (threadIdx.x < 32) th_find_digit_warp(hist, nbins, kk, kk2, sh);
     __syncthreads();
 }
 
-// Adds this thread's bin (-1: none) to a shared histogram, one atomic per distinct bin of the warp.
+// Adds this thread's bin (-1: none) to a shared histogram: one atomic for the warp when all
+// its lanes share a bin (ties, a narrow score range), else one per lane (the keys of a
+// candidate array, below the bits they share, spread over many bins).
 __device__ __forceinline__ void th_hist_add(int* hist, int bin) {
-    const unsigned same = __match_any_sync(0xffffffffu, bin);
-    if (bin >= 0 && (int)(threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
+    const int b0 = __shfl_sync(0xffffffffu, bin, 0);
+    if (__all_sync(0xffffffffu, bin == b0)) {
+        if ((threadIdx.x & 31) == 0 && b0 >= 0) atomicAdd(&hist[b0], 32);
+    } else if (bin >= 0) {
+        atomicAdd(&hist[bin], 1);
+    }
 }
 
-// Threshold U with exactly k of the n (distinct) entries >= U, 1 <= k <= n: radix select over
-// 11-bit digits from the top, stopping as soon as the bin holding rank k is needed whole.
-__device__ unsigned long long th_kth_entry(const unsigned long long* v, int n, int k, ThShared& sh) {
-    unsigned long long prefix = 0ull, mask = 0ull;
-    int kk = k;
-    for (int pass = 0; pass < 6; ++pass) {
-        const int shift = pass < 5 ? 53 - 11 * pass : 0;
-        const unsigned long long dmask = pass < 5 ? 2047ull : 511ull;
+// Warp-reduced minimum and maximum of a key (0xffffffff / 0 for lanes without one) into sh.
+__device__ __forceinline__ void th_minmax(uint32_t lo, uint32_t hi, ThShared& sh) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicMin(&sh.kmin, lo);
+        atomicMax(&sh.kmax, hi);
+    }
+}
+
+// Threshold U with exactly k of the n (distinct) entries >= U, 1 <= k <= n, whose keys all
+// lie in [sh.kmin, sh.kmax]: radix select over 11-bit digits starting below the key bits the
+// extremes share, stopping as soon as the bin holding rank k is needed whole.  The first
+// pass also places rank kp >= k: *guess is the key of its bin's lower edge (at least kp
+// entries have a key >= it).
+__device__ unsigned long long th_select(const unsigned long long* v, int n, int k, int kp, uint32_t* guess,
+                                        ThShared& sh) {
+    const uint32_t kmin = sh.kmin, kmax = sh.kmax;
+    const int p = kmin == kmax ? 32 : __clz(kmin ^ kmax);  // key bits every entry shares
+    unsigned long long mask = p == 0 ? 0ull : (~0ull << (64 - p));
+    unsigned long long prefix = ((unsigned long long)kmin << 32) & mask;
+    int top = 64 - p, kk = k;
+    bool first = true;
+    while (top > 0) {
+        const int wdt = top < 11 ? top : 11;
+        const int shift = top - wdt;
+        const unsigned long long dmask = (1ull << wdt) - 1ull;
         for (int b = threadIdx.x; b < kThBins; b += kThThreads) sh.hist[b] = 0;
         __syncthreads();
         for (int i0 = 0; i0 < n; i0 += kThThreads) {
@@ -144,10 +220,15 @@ __device__ unsigned long long th_kth_entry(const unsigned long long* v, int n, i
             th_hist_add(sh.hist, bin);
         }
         __syncthreads();
-        th_find_digit(sh.hist, kThBins, kk, sh);
+        th_find_digit(sh.hist, kThBins, kk, sh, first ? kp : 0);
+        if (first) {
+            *guess = (uint32_t)((prefix | ((unsigned long long)sh.gdigit << shift)) >> 32);
+            first = false;
+        }
         prefix |= (unsigned long long)sh.digit << shift;
         mask |= dmask << shift;
         kk -= sh.above;
+        top = shift;
         const bool whole = sh.nbin == kk;
         __syncthreads();
         if (whole) break;  // every entry with this prefix is kept: U = the prefix, low bits 0
@@ -180,7 +261,10 @@ topk_hint_kernel(spin_config cfg, const float* __restrict__ scores, const float*
     uint32_t extra = rec[kHwExtra];
     if (extra == 0u) extra = th_default_extra(K, h.cap);
     extra = extra < kmin ? kmin : extra > kmax ? kmax : extra;
-    __syncthreads();  // every thread has read the record before thread 0 rewrites it
+    // (thread 0 rewrites the record at the end, after many barriers: every thread has read it)
+    float wpart = 0.0f;  // warp 0: its lanes' share of sum_h |w_h|, loaded while the list comes in
+    if (tid < 32)
+        for (int hh = tid; hh < cfg.n_heads; hh += 32) wpart += fabsf(w[(int64_t)rr * cfg.n_heads + hh]);
     if (n < 0 || n > dm.max_slots || cnt < 0 || cnt > dm.MB) {
         if (tid == 0) {
             set_status(status, (n < 0 || n > dm.max_slots) ? SPIN_STATUS_BAD_N : SPIN_STATUS_BAD_LIST);
@@ -194,107 +278,212 @@ topk_hint_kernel(spin_config cfg, const float* __restrict__ scores, const float*
     const int64_t C = cnt * kBlock;
     const int W = (int)((C + 31) / 32);  // bitmap words
 
+    // the whole list array (MB entries) is staged, so its loads need not wait for the count
     bool bad_list = false;
-    for (int64_t k = tid; k < cnt; k += kThThreads) {
+    for (int k = tid; k < dm.MB; k += kThThreads) {
         const int b = list[(int64_t)req * dm.MB + k];
-        if (b < 0 || b >= nb) bad_list = true;
+        if (k < cnt && (b < 0 || b >= nb)) bad_list = true;
         slist[k] = b;
     }
     if (bad_list && rr % rows == 0) set_status(status, SPIN_STATUS_BAD_LIST);
     for (int wd = tid; wd < W; wd += kThThreads) bits[wd] = 0u;
-    if (tid == 0) sh.ncand = 0;
+    if (tid == 0) {
+        sh.ncand = 0;
+        sh.kmin = 0xffffffffu;
+        sh.kmax = 0u;
+    }
+    if (tid < 32) {  // sum_h |w_h| of the row
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wpart += __shfl_xor_sync(0xffffffffu, wpart, o);
+        if (tid == 0) sh.wsum = wpart;
+    }
     __syncthreads();
 
-    const bool hit = guess != 0u && count >= (uint32_t)K && count <= (uint32_t)h.cap;
-    bool take_all = false, exact = false;
-    int nc = 0;
-    if (hit) {
-        nc = (int)count;
-        const unsigned long long* src = h.cand + (int64_t)rr * h.cap;
-        for (int i = tid; i < nc; i += kThThreads) cand[i] = src[i];
-        __syncthreads();
-    } else {
-        // cold path.  Keys of four candidates (0: not a live candidate).
-        const float4* sc4 = reinterpret_cast<const float4*>(scores + (int64_t)rr * dm.MB * kBlock);
-        const int C4 = (int)(C / 4);
-        auto keys4 = [&](int i4, uint32_t* k4) {
-            const int c = 4 * i4;
-            const int blk = slist[c >> 6];
-            const int64_t slot = (int64_t)blk * kBlock + (c & 63);
-            const bool okb = blk >= 0 && blk < nb;
-            const float4 z = sc4[i4];
-            k4[0] = okb && slot + 0 < n ? order_key(z.x) : 0u;
-            k4[1] = okb && slot + 1 < n ? order_key(z.y) : 0u;
-            k4[2] = okb && slot + 2 < n ? order_key(z.z) : 0u;
-            k4[3] = okb && slot + 3 < n ? order_key(z.w) : 0u;
-        };
-        for (int b = tid; b < kThBinsA; b += kThThreads) sh.hist[b] = 0;
-        __syncthreads();
-        int v = 0;
-        const int C4pad = (C4 + 31) & ~31;
-        for (int i4 = tid; i4 < C4pad; i4 += kThThreads) {
-            uint32_t k4[4] = {0u, 0u, 0u, 0u};
-            if (i4 < C4) keys4(i4, k4);
+    // Keys of four candidates (0: not a live candidate).
+    const float4* sc4 = reinterpret_cast<const float4*>(scores + (int64_t)rr * dm.MB * kBlock);
+    const int C4 = (int)(C / 4);
+    const int C4pad = (C4 + 31) & ~31;
+    auto keys4 = [&](int i4, const float4& z, uint32_t* k4) {
+        const int c = 4 * i4;
+        const int blk = i4 < C4 ? slist[c >> 6] : -1;  // (padding lanes read nothing)
+        const int64_t slot = (int64_t)blk * kBlock + (c & 63);
+        const bool okb = blk >= 0 && blk < nb;
+        k4[0] = okb && slot + 0 < n ? order_key(z.x) : 0u;
+        k4[1] = okb && slot + 1 < n ? order_key(z.y) : 0u;
+        k4[2] = okb && slot + 2 < n ? order_key(z.z) : 0u;
+        k4[3] = okb && slot + 3 < n ? order_key(z.w) : 0u;
+    };
+    // body(i4, k4) for every i4 < C4pad (whole warps: C4pad is a multiple of 32; k4 is zero
+    // past C4), four 16-byte loads in flight per thread
+    auto scan_keys = [&](auto&& body) {
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i0 = tid; i0 < C4pad; i0 += 4 * kThThreads) {
+            float4 z[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                th_hist_add(sh.hist, k4[e] ? (int)(k4[e] >> 20) : -1);
-                v += k4[e] != 0u;
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * kThThreads;
+                z[u] = i < C4 ? sc4[i] : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + u * kThThreads;
+                if (i < C4pad) {  // (warp-uniform)
+                    uint32_t k4[4];
+                    keys4(i, z[u], k4);
+                    body(i, k4);
+                }
             }
         }
-        const int nvalid = th_block_sum(v, sh);  // (its barriers also complete the histogram)
+    };
+    // Appends the warp's keys >= tkey (as candidate entries at position 4 i4 + e) to the shared
+    // candidate array.  Each warp fills 32-entry chunks it claims with one atomic (sh.ncand
+    // counts the entries claimed); `seen` counts the keys taken, `lo`/`hi` track their extremes.
+    // Warp-uniform chunk state: base (-1: none yet) and fill.
+    auto collect4 = [&](int i4, const uint32_t* k4, uint32_t tkey, int& cbase, int& cfill, int& seen_w,
+                        uint32_t& lo, uint32_t& hi) {
+        const int lane = tid & 31;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool take = k4[e] != 0u && k4[e] >= tkey;
+            const unsigned m = __ballot_sync(0xffffffffu, take);
+            if (m == 0u) continue;
+            const int nm = __popc(m), rank = __popc(m & ((1u << lane) - 1u));
+            seen_w += nm;
+            const int room = cbase < 0 ? 0 : 32 - cfill;
+            int nbase = cbase;
+            if (nm > room) {  // a new chunk for the rest of the batch
+                int b = 0;
+                if (lane == 0) b = atomicAdd(&sh.ncand, 32);
+                nbase = __shfl_sync(0xffffffffu, b, 0);
+            }
+            if (take) {
+                const int at = rank < room ? cbase + cfill + rank : nbase + (rank - room);
+                if (at < h.cap) {
+                    cand[at] = hint_entry(k4[e], (uint32_t)(4 * i4 + e));
+                    lo = min(lo, k4[e]);
+                    hi = max(hi, k4[e]);
+                }
+            }
+            if (nm > room) {
+                cbase = nbase;
+                cfill = nm - room;
+            } else {
+                cfill += nm;
+            }
+        }
+    };
+    // zero the unfilled tail of the warp's last chunk (entries of key 0 rank below every
+    // candidate, so they are never selected)
+    auto close_chunk = [&](int cbase, int cfill) {
+        const int lane = tid & 31;
+        if (cbase >= 0 && lane >= cfill && cbase + lane < h.cap) cand[cbase + lane] = 0ull;
+    };
+
+    const bool collected = (rec[kHwFlags] & 1u) != 0u;
+    uint32_t seen = count;  // candidates at or above this step's threshold
+    int nc_claimed = (int)count;  // entries of the candidate array in use
+    bool hit = false;
+    if (guess != 0u && collected) {
+        // the score kernel collected them
+        if (count >= (uint32_t)K && count <= (uint32_t)h.cap) {
+            hit = true;
+            const unsigned long long* src = h.cand + (int64_t)rr * h.cap;
+            uint32_t lo = 0xffffffffu, hi = 0u;
+            for (int i = tid; i < (int)count; i += kThThreads) {
+                const unsigned long long x = src[i];
+                cand[i] = x;
+                lo = min(lo, (uint32_t)(x >> 32));
+                hi = max(hi, (uint32_t)(x >> 32));
+            }
+            th_minmax(lo, hi, sh);
+            __syncthreads();
+        }
+    } else if (guess != 0u) {
+        // collect them here: one pass over the scores against this step's threshold
+        const uint32_t thr = hint_threshold(guess, sh.wsum);
+        uint32_t lo = 0xffffffffu, hi = 0u;
+        int cbase = -1, cfill = 0, seen_w = 0;
+        scan_keys([&](int i4, const uint32_t* k4) { collect4(i4, k4, thr, cbase, cfill, seen_w, lo, hi); });
+        close_chunk(cbase, cfill);
+        th_minmax(lo, hi, sh);
+        seen = (uint32_t)th_block_sum((tid & 31) == 0 ? seen_w : 0, sh);
+        // (the claimed chunks, zero tails included, must fit: at most one partial chunk a warp)
+        hit = seen >= (uint32_t)K && sh.ncand <= h.cap;
+        nc_claimed = sh.ncand;
+        __syncthreads();
+        if (!hit && tid == 0) {
+            sh.ncand = 0;
+            sh.kmin = 0xffffffffu;
+            sh.kmax = 0u;
+        }
+        __syncthreads();
+    }
+    bool take_all = false, exact = false;
+    int nc = hit ? nc_claimed : 0;
+    int seen_cold = 0;  // live candidates collected by the cold path
+    if (!hit) {
+        // cold path
+        // pass A: live count, smallest and largest live key
+        int v = 0;
+        uint32_t lo = 0xffffffffu, hi = 0u;
+        scan_keys([&](int, const uint32_t* k4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (k4[e]) {
+                    ++v;
+                    lo = min(lo, k4[e]);
+                    hi = max(hi, k4[e]);
+                }
+        });
+        th_minmax(lo, hi, sh);
+        const int nvalid = th_block_sum(v, sh);  // (its barriers also complete the extremes)
         if (nvalid <= K) {
             take_all = true;
         } else {
+            // the bin holding rank kp, 12 bits at a time below the bits every live key shares,
+            // until the keys at or above it fit the candidate array
             const int kp = (int)min((int64_t)nvalid, (int64_t)K + extra);
-            // the bin holding rank kp, by the top 12 bits of the key; while it holds more
-            // candidates than fit, refine it by the next 12, then the last 8 bits
-            uint32_t tkey = 0u, tmask = 0u;  // collect the live keys >= tkey
-            int above = 0, total = 0;
-            for (int lvl = 0; lvl < 3; ++lvl) {
-                const int shift = lvl == 0 ? 20 : lvl == 1 ? 8 : 0;
-                const uint32_t dmask = lvl < 2 ? 4095u : 255u;
-                if (lvl > 0) {
-                    for (int b = tid; b < kThBinsA; b += kThThreads) sh.hist[b] = 0;
-                    __syncthreads();
-                    for (int i4 = tid; i4 < C4pad; i4 += kThThreads) {
-                        uint32_t k4[4] = {0u, 0u, 0u, 0u};
-                        if (i4 < C4) keys4(i4, k4);
+            const uint32_t kmn = sh.kmin, kmx = sh.kmax;
+            const int pbits = kmn == kmx ? 32 : __clz(kmn ^ kmx);
+            uint32_t tmask = pbits == 0 ? 0u : (0xffffffffu << (32 - pbits));
+            uint32_t tkey = kmn & tmask;  // collect the live keys >= tkey
+            int top = 32 - pbits, above = 0, total = nvalid;
+            const int fit = h.cap - 32 * (kThThreads / 32);  // room left for the warps' chunk tails
+            while (top > 0 && total > fit) {
+                const int wdt = top < 12 ? top : 12;
+                const int shift = top - wdt;
+                const uint32_t dmask = (1u << wdt) - 1u;
+                for (int b = tid; b < kThBinsA; b += kThThreads) sh.hist[b] = 0;
+                __syncthreads();
+                scan_keys([&](int, const uint32_t* k4) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            th_hist_add(sh.hist, k4[e] != 0u && (k4[e] & tmask) == tkey
-                                                     ? (int)((k4[e] >> shift) & dmask) : -1);
-                    }
-                    __syncthreads();
-                }
+                    for (int e = 0; e < 4; ++e)
+                        th_hist_add(sh.hist, k4[e] != 0u && (k4[e] & tmask) == tkey ? (int)((k4[e] >> shift) & dmask) : -1);
+                });
+                __syncthreads();
                 th_find_digit(sh.hist, kThBinsA, kp - above, sh);
                 total = above + sh.above + sh.nbin;
                 above += sh.above;
                 tkey |= (uint32_t)sh.digit << shift;
                 tmask |= dmask << shift;
+                top = shift;
                 __syncthreads();
-                if (total <= h.cap) break;
             }
-            if (total <= h.cap) {
+            if (total <= fit) {
                 // collect every live candidate with key >= tkey (all of rank <= kp)
-                for (int i4 = tid; i4 < C4pad; i4 += kThThreads) {
-                    uint32_t k4[4] = {0u, 0u, 0u, 0u};
-                    if (i4 < C4) keys4(i4, k4);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const bool take = k4[e] != 0u && k4[e] >= tkey;
-                        const unsigned m = __ballot_sync(0xffffffffu, take);
-                        if (m) {
-                            const int lane = tid & 31, lead = __ffs(m) - 1;
-                            int base = 0;
-                            if (lane == lead) base = atomicAdd(&sh.ncand, __popc(m));
-                            base = __shfl_sync(0xffffffffu, base, lead);
-                            if (take) cand[base + __popc(m & ((1u << lane) - 1u))] =
-                                hint_entry(k4[e], (uint32_t)(4 * i4 + e));
-                        }
-                    }
+                if (tid == 0) {
+                    sh.kmin = 0xffffffffu;
+                    sh.kmax = 0u;
                 }
                 __syncthreads();
+                uint32_t clo = 0xffffffffu, chi = 0u;
+                int cbase = -1, cfill = 0, seen_w = 0;
+                scan_keys([&](int i4, const uint32_t* k4) { collect4(i4, k4, tkey, cbase, cfill, seen_w, clo, chi); });
+                close_chunk(cbase, cfill);
+                th_minmax(clo, chi, sh);
+                __syncthreads();
                 nc = sh.ncand;
+                seen_cold = total;
             } else {
                 exact = true;  // a huge boundary bin (massive ties): exact passes over the scores
             }
@@ -321,13 +510,15 @@ topk_hint_kernel(spin_config cfg, const float* __restrict__ scores, const float*
             }
             __syncthreads();
         } else {
-            const unsigned long long U = th_kth_entry(cand, nc, K, sh);
-            const int kp = (int)min((int64_t)nc, (int64_t)K + extra);
+            // (nc may include zero entries of chunk tails; the live candidates number `live`)
+            const int live = hit ? (int)seen : seen_cold;
+            const int kp = (int)min((int64_t)live, (int64_t)K + extra);
+            uint32_t gkey = 0u;
+            const unsigned long long U = th_select(cand, nc, K, kp, &gkey, sh);
             // the next guess: the score at rank K + extra over this step's sum of |w_h|
-            const float t = key_float((uint32_t)(th_kth_entry(cand, nc, kp, sh) >> 32));
-            const float ws = row_wsum(w + (int64_t)rr * cfg.n_heads, cfg.n_heads);
+            const float ws = sh.wsum;
             if (ws > 0.0f) {
-                const float g = __fdiv_rn(t, ws);
+                const float g = __fdiv_rn(key_float(gkey), ws);
                 if (isfinite(g)) next_guess = order_key(g) == 0u ? 1u : order_key(g);
             }
             for (int i = tid; i < nc; i += kThThreads) {
@@ -358,13 +549,14 @@ topk_hint_kernel(spin_config cfg, const float* __restrict__ scores, const float*
 
     if (tid == 0) {
         rec[kHwCount] = 0u;
+        rec[kHwFlags] = 0u;
         rec[kHwGuess] = next_guess;
         uint32_t nx = extra;
         if (hit) {
             rec[kHwHit] += 1u;
         } else if (guess == 0u) {
             rec[kHwCold] += 1u;
-        } else if (count < (uint32_t)K) {
+        } else if (seen < (uint32_t)K) {
             rec[kHwMiss] += 1u;
             nx = extra * 2u;
         } else {
@@ -373,15 +565,14 @@ topk_hint_kernel(spin_config cfg, const float* __restrict__ scores, const float*
         }
         rec[kHwExtra] = nx < kmin ? kmin : nx > kmax ? kmax : nx;
         if (exact) rec[kHwGlobal] += 1u;
-        rec[kHwLast] = count;
+        rec[kHwLast] = seen;
     }
 }
 
 cudaError_t launch_topk_hint(const spin_config& cfg, const float* scores, const float* w, const int32_t* list,
                              const int32_t* n_list, const int32_t* n_slots, int rows, int32_t* topk_idx,
                              const HintArgs& h, uint32_t* status, cudaStream_t s) {
-    const Dims dm = dims_of(cfg);
-    const size_t smem = ((sizeof(ThShared) + 15) & ~(size_t)15) + (size_t)h.cap * 8 + (size_t)dm.MB * 12;
+    const size_t smem = th_smem_bytes(cfg, h.cap);
     cudaError_t e = cudaFuncSetAttribute(topk_hint_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(topk_hint_kernel, dim3((unsigned)(cfg.n_req * rows)), dim3(kThThreads), smem, s, nullptr, 0,

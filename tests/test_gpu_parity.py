@@ -331,17 +331,21 @@ def test_v32_full_size_one_layer():
 
 
 def test_v4flash_full_size_sampled():
-    """32 requests x 131072 slots, FP8 keys with a per-slot scale, shuffled pages:
-    selection, top-K and EMA checked for every request, scores for two requests."""
+    """32 requests x 131072 slots, FP8 keys with a per-slot scale, shuffled pages: a dense
+    first step and four sparse ones; selection, top-K and EMA checked for every request,
+    scores for two requests."""
     h = Harness(syn.CONFIGS["v4flash"])
-    run_steps(h, 2, score_requests=[0, 31])
+    run_steps(h, 5, score_requests=[0, 31])
 
 
 def test_serving_full_size_sampled():
+    """96 requests x 131072 slots, FP8 keys: a dense first step and four sparse ones."""
     h = Harness(syn.CONFIGS["serving"])
-    run_steps(h, 2, score_requests=[0, 95])
+    run_steps(h, 5, score_requests=[0, 95])
 
 
 def test_mtp_full_size_sampled():
+    """16 requests x 262144 slots, 4 verifier rows: a dense first step and four sparse ones
+    with their unions and deferred commits."""
     h = Harness(syn.CONFIGS["mtp"])
-    run_steps(h, 2, score_requests=[0])
+    run_steps(h, 5, score_requests=[0])

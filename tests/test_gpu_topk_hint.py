@@ -24,7 +24,7 @@ from sparse_attention_indexer_spin_gb300 import synthetic as syn
 pytestmark = pytest.mark.gpu
 
 W = spin.HINT_WORDS
-GUESS, COUNT, EXTRA, HIT, MISS, OVER, COLD, EXACT, LAST = range(9)
+GUESS, COUNT, EXTRA, HIT, MISS, OVER, COLD, EXACT, LAST, FLAGS = range(10)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,10 +59,12 @@ def live_positions(blist, n_list, n_slots, r):
     return np.nonzero(slot < n_slots[r])[0]
 
 
-def plant(hint, cfg, rows, scores, blist, n_list, n_slots, guess_rank, rng, extra=0):
+def plant(hint, cfg, rows, scores, blist, n_list, n_slots, guess_rank, rng, extra=0, collected=True):
     """Write each row's record and candidates as a score kernel with this guess would: the
-    guess is the key at `guess_rank` (None: no guess), the candidates every live slot at or
-    above it, in random order.  Returns the counts."""
+    threshold is the key at `guess_rank` (None: no guess), the candidates every live slot at or
+    above it, in random order.  collected=False writes only the guess (the threshold over the
+    weights' sum, exact for a sum of 4) and leaves the collection to the top-K kernel.
+    Returns the counts."""
     R, cap = cfg.n_req, _cap(cfg)
     recs = np.zeros((R * rows, W), np.uint32)
     cands = np.zeros((R * rows, cap), np.uint64)
@@ -81,9 +83,13 @@ def plant(hint, cfg, rows, scores, blist, n_list, n_slots, guess_rank, rng, extr
             ent = (keys[take].astype(np.uint64) << np.uint64(32)) | (~pos[take].astype(np.uint32)).astype(np.uint64)
             rng.shuffle(ent)
             c = len(ent)
-            cands[rr, : min(c, cap)] = ent[:cap]
-            recs[rr, GUESS], recs[rr, COUNT], recs[rr, EXTRA] = g, c, extra
             counts.append(c)
+            recs[rr, EXTRA] = extra
+            if collected:
+                cands[rr, : min(c, cap)] = ent[:cap]
+                recs[rr, GUESS], recs[rr, COUNT], recs[rr, FLAGS] = g, c, 1
+            else:
+                recs[rr, GUESS] = order_keys(np.array([key_float(g) / WSUM], np.float32))[0]
     raw = hint.buf
     rec_bytes = (R * rows * W * 4 + 255) // 256 * 256
     raw[: recs.nbytes].copy_(torch.from_numpy(recs.view(np.uint8).ravel()))
@@ -92,8 +98,9 @@ def plant(hint, cfg, rows, scores, blist, n_list, n_slots, guess_rank, rng, extr
 
 
 def _cap(cfg):
+    """The library's candidate capacity for these shapes (8 K, at least 4096; all fit)."""
     c = 4096
-    while c < 4 * cfg.top_k:
+    while c < 8 * cfg.top_k:
         c *= 2
     return c
 
@@ -130,8 +137,9 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("collected", [True, False], ids=["score-collected", "self-collected"])
 @pytest.mark.parametrize("n_req,max_slots,rows,top_k,dist,mult,branch", CASES)
-def test_topk_hinted_direct(n_req, max_slots, rows, top_k, dist, mult, branch):
+def test_topk_hinted_direct(n_req, max_slots, rows, top_k, dist, mult, branch, collected):
     f = _fields(n_req, max_slots, rows, top_k)
     cfg, ocfg = spin.make_config(**f), o.make_cfg(**f)
     scores, blist, n_list, n_slots = syn.topk_inputs(n_req, max_slots, rows, dist, 100 + n_req)
@@ -140,11 +148,11 @@ def test_topk_hinted_direct(n_req, max_slots, rows, top_k, dist, mult, branch):
     hint = spin.TopkHint(cfg, rows)
     rng = np.random.default_rng(7)
     rank = None if mult is None else max(1, int(mult * top_k))
-    counts = plant(hint, cfg, rows, scores, blist, n_list, n_slots, rank, rng)
+    counts = plant(hint, cfg, rows, scores, blist, n_list, n_slots, rank, rng, collected=collected)
     got = run_hinted(cfg, rows, scores, blist, n_list, n_slots, hint)
     np.testing.assert_array_equal(got, want)
     rec = hint.records()
-    assert (rec[:, COUNT] == 0).all()                     # consumed
+    assert (rec[:, COUNT] == 0).all() and (rec[:, FLAGS] == 0).all()   # consumed
     assert (rec[:, LAST] == np.array(counts, np.uint32)).all()
     if branch is not None:
         col = EXACT if branch == EXACT else branch
@@ -171,12 +179,12 @@ def test_topk_hinted_margin_adapts():
     plant(hint, cfg, 1, scores, blist, n_list, n_slots, 512, rng, extra=300)      # miss
     run_hinted(cfg, 1, scores, blist, n_list, n_slots, hint)
     assert int(hint.records()[0, EXTRA]) == 600
-    plant(hint, cfg, 1, scores, blist, n_list, n_slots, 9000, rng, extra=600)     # overflow (cap 4096)
+    plant(hint, cfg, 1, scores, blist, n_list, n_slots, 9000, rng, extra=600)     # overflow (cap 8192)
     run_hinted(cfg, 1, scores, blist, n_list, n_slots, hint)
     assert int(hint.records()[0, EXTRA]) == 300
-    plant(hint, cfg, 1, scores, blist, n_list, n_slots, 512, rng, extra=1024)     # miss at the top
+    plant(hint, cfg, 1, scores, blist, n_list, n_slots, 512, rng, extra=2000)     # miss at the top
     run_hinted(cfg, 1, scores, blist, n_list, n_slots, hint)
-    assert int(hint.records()[0, EXTRA]) == 4096 // 2 - 1024
+    assert int(hint.records()[0, EXTRA]) == 8192 // 2 - 1024
 
 
 def test_topk_hinted_reset_and_errors():
