@@ -18,6 +18,7 @@ from . import build as _build
 
 DTYPES = {"f32": 0, "bf16": 1, "e4m3": 2}
 COMBINES = {"max": 0, "sum": 1}
+POOLINGS = {"max": 0, "mean": 1, "top4": 2}
 RAW_NP = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}
 
 
@@ -38,6 +39,7 @@ class OracleCfg(ctypes.Structure):
         ("alpha", ctypes.c_float),
         ("combine", ctypes.c_int32),
         ("seed", ctypes.c_uint64),
+        ("pooling", ctypes.c_int32),
     ]
 
 
@@ -79,11 +81,12 @@ def lib():
 
 
 def make_cfg(n_req, max_slots, max_rows, n_heads, head_dim, kv_heads, q_dtype, k_dtype,
-             top_k, rho_bp, gamma_bp, alpha, combine="max", seed=0, block=64, **_ignored):
+             top_k, rho_bp, gamma_bp, alpha, combine="max", seed=0, block=64, pooling="max",
+             **_ignored):
     return OracleCfg(int(n_req), int(max_slots), int(max_rows), int(block), int(n_heads),
                      int(head_dim), int(kv_heads), DTYPES[q_dtype], DTYPES[k_dtype],
                      int(top_k), int(rho_bp), int(gamma_bp), float(alpha),
-                     COMBINES[combine], int(seed) & 0xFFFFFFFFFFFFFFFF)
+                     COMBINES[combine], int(seed) & 0xFFFFFFFFFFFFFFFF, POOLINGS[pooling])
 
 
 def max_blocks(cfg) -> int:

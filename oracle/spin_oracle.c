@@ -20,7 +20,10 @@
  *   oracle_budget ............. hand-derived table of Algorithm 1's budget step (golden file)
  *   oracle_explore_count ...... hand-derived table (golden file) + invariants
  *   oracle_block_scores ....... numpy reductions in the degenerate cases D = -inf and
- *                               V = -inf, and brute force on tiny inputs
+ *                               V = -inf, and brute force on tiny inputs; the MEAN and
+ *                               TOP4 poolings: numpy's mean / sorted top four where the
+ *                               fp32 sums are exact (small integers), constant blocks,
+ *                               one-slot blocks, max >= top-4 mean >= mean
  *   oracle_select_blocks ...... |selection| = budget, forced blocks kept, top set
  *                               dominance, exploration uniformity (chi-square),
  *                               rho = 0 gives the dense selection
@@ -161,6 +164,46 @@ static float predicted_slot_score(const oracle_cfg* cfg, const float* V_req,
     return v > d ? v : d;
 }
 
+/* §4.6 (block-reduction ablation): instead of Eq. 2's max, a block's score is the mean of
+ * its slots' predictions (MEAN) or the mean of the (up to) four largest (TOP4).  The pages
+ * give no precision; the sums are fp32 in a fixed order, the one the GPU kernel uses, so
+ * that both sides rank blocks identically:
+ *   MEAN: slot l and slot l + 32 of the block are added first (a slot at or beyond N adds
+ *         nothing), then the 32 pair sums pairwise at distance 16, 8, 4, 2, 1 (each step
+ *         replaces t[l] by t[l] + t[l ^ d]), and the sum is divided by the count of slots < N;
+ *   TOP4: the largest values t1 >= t2 >= t3 >= t4 are added as (t1 + t2) + (t3 + t4) (with
+ *         fewer slots: t1, t1 + t2, (t1 + t2) + t3) and divided by their count. */
+static float pool_mean(const float* p, const int* valid) {
+    float t[32], u[32];
+    for (int l = 0; l < 32; ++l) t[l] = (valid[l] ? p[l] : 0.0f) + (valid[l + 32] ? p[l + 32] : 0.0f);
+    for (int d = 16; d >= 1; d >>= 1) {
+        for (int l = 0; l < 32; ++l) u[l] = t[l] + t[l ^ d];
+        memcpy(t, u, sizeof t);
+    }
+    int count = 0;
+    for (int l = 0; l < 64; ++l) count += valid[l] != 0;
+    return t[0] / (float)count;
+}
+
+static float pool_top4(const float* p, const int* valid) {
+    float top[4];
+    int c = 0, used[64];
+    for (int l = 0; l < 64; ++l) used[l] = !valid[l];
+    for (; c < 4; ++c) {  /* the largest remaining value, each slot taken once */
+        int best = -1;
+        for (int l = 0; l < 64; ++l)
+            if (!used[l] && (best < 0 || p[l] > p[best])) best = l;
+        if (best < 0) break;
+        used[best] = 1;
+        top[c] = p[best];
+    }
+    float sum = top[0];
+    if (c == 2) sum = top[0] + top[1];
+    if (c == 3) sum = (top[0] + top[1]) + top[2];
+    if (c == 4) sum = (top[0] + top[1]) + (top[2] + top[3]);
+    return sum / (float)c;
+}
+
 void oracle_block_scores(const oracle_cfg* cfg, const float* V_req, const float* D_req,
                          int64_t n_slots, int64_t q, float* S_out) {
     int64_t b = cfg->block;
@@ -168,6 +211,16 @@ void oracle_block_scores(const oracle_cfg* cfg, const float* V_req, const float*
     for (int64_t j = 0; j < nb; ++j) {
         int64_t lo = j * b;
         int64_t hi = (j + 1) * b < n_slots ? (j + 1) * b : n_slots;
+        if (cfg->pooling == ORACLE_POOL_MEAN || cfg->pooling == ORACLE_POOL_TOP4) {
+            float p[64];
+            int valid[64];
+            for (int64_t l = 0; l < 64; ++l) {
+                valid[l] = lo + l < hi;
+                p[l] = valid[l] ? predicted_slot_score(cfg, V_req, D_req, q, lo + l) : 0.0f;
+            }
+            S_out[j] = cfg->pooling == ORACLE_POOL_MEAN ? pool_mean(p, valid) : pool_top4(p, valid);
+            continue;
+        }
         float s = predicted_slot_score(cfg, V_req, D_req, q, lo);
         for (int64_t i = lo + 1; i < hi; ++i) {
             float p = predicted_slot_score(cfg, V_req, D_req, q, i);

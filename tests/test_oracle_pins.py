@@ -617,3 +617,64 @@ def test_rho_zero_step_equals_dense_topk(oracle_mod):
                                       q[r, 0].astype(np.float64)), 0) * w[r, 0]).sum(-1)
             order = np.lexsort((np.arange(N), -z))[:100]
             np.testing.assert_array_equal(out["topk"][r, 0], np.sort(order))
+
+
+# ------------------------------------------------------------- pooling ablations (§4.6)
+
+def _pool_inputs(oracle_mod, pooling, seed, n, combine="max", ints=True):
+    cfg = tiny_cfg(oracle_mod, combine=combine, pooling=pooling)
+    rng = np.random.default_rng(seed)
+    if ints:  # small integers: every fp32 sum below is exact, whatever its order
+        V = rng.integers(-50, 51, cfg.max_slots).astype(np.float32)
+        D = rng.integers(-50, 51, oracle_mod.d_len(cfg)).astype(np.float32)
+    else:
+        V = rng.standard_normal(cfg.max_slots).astype(np.float32)
+        D = rng.standard_normal(oracle_mod.d_len(cfg)).astype(np.float32)
+    q = n + 3
+    pred = np.maximum(V[:n], D[q - np.arange(n)]) if combine == "max" else V[:n] + D[q - np.arange(n)]
+    return cfg, V, D, q, pred
+
+
+@pytest.mark.parametrize("combine", ["max", "sum"])
+@pytest.mark.parametrize("n", [1, 37, 64, 150, 257])
+def test_mean_pooling_is_the_block_mean(oracle_mod, combine, n):
+    """MEAN pooling: with integer predictions the fp32 sum is exact in any order, so the
+    block score is the exact mean rounded once (numpy's float64 mean, then float32)."""
+    cfg, V, D, q, pred = _pool_inputs(oracle_mod, "mean", 40 + n, n, combine)
+    S = oracle_mod.block_scores(cfg, V, D, n, q)
+    want = [np.float32(pred[j * 64: (j + 1) * 64].astype(np.float64).mean()) for j in range(-(-n // 64))]
+    np.testing.assert_array_equal(S, np.array(want, np.float32))
+
+
+@pytest.mark.parametrize("combine", ["max", "sum"])
+@pytest.mark.parametrize("n", [1, 3, 64, 130, 257])
+def test_top4_pooling_is_the_mean_of_the_four_largest(oracle_mod, combine, n):
+    """TOP4 pooling: the mean of the four largest slot predictions of a block (all of them
+    when the block has fewer), exact for integer predictions."""
+    cfg, V, D, q, pred = _pool_inputs(oracle_mod, "top4", 70 + n, n, combine)
+    S = oracle_mod.block_scores(cfg, V, D, n, q)
+    want = []
+    for j in range(-(-n // 64)):
+        blk = np.sort(pred[j * 64: (j + 1) * 64].astype(np.float64))[::-1][:4]
+        want.append(np.float32(blk.mean()))
+    np.testing.assert_array_equal(S, np.array(want, np.float32))
+
+
+@pytest.mark.parametrize("n", [64, 200])
+def test_pooling_invariants_on_real_values(oracle_mod, n):
+    """Non-integer predictions: max >= top-4 mean >= mean (up to rounding of the means), a
+    constant block pools to its constant under every pooling, and a one-slot block to its
+    only value."""
+    cfgs = {p: tiny_cfg(oracle_mod, pooling=p) for p in ("max", "mean", "top4")}
+    _, V, D, q, _ = _pool_inputs(oracle_mod, "max", 5, n, ints=False)
+    S = {p: oracle_mod.block_scores(c, V, D, n, q) for p, c in cfgs.items()}
+    eps = 1e-6
+    assert np.all(S["max"] >= S["top4"] - eps * np.abs(S["max"]))
+    assert np.all(S["top4"] >= S["mean"] - eps * np.abs(S["top4"]))
+    Vc = np.full_like(V, np.float32(0.3))
+    Dc = np.full_like(D, np.float32(-1.0))
+    for p, c in cfgs.items():
+        np.testing.assert_array_equal(oracle_mod.block_scores(c, Vc, Dc, n, q), np.float32(0.3))
+    for p, c in cfgs.items():  # N = 65: the second block holds one slot
+        S1 = oracle_mod.block_scores(c, V, D, 65, 68)
+        assert S1[1] == max(V[64], D[68 - 64])
