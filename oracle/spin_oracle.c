@@ -286,6 +286,28 @@ static int64_t select_row(const oracle_cfg* cfg, const float* V_req, const float
         memset(mask, 1, (size_t)nb);
         return nb;
     }
+    if (cfg->pooling == ORACLE_POOL_SLOTS) {
+        /* §4.6, A0: the K slots with the largest predicted scores (equal scores: lower slot),
+         * then every block holding one of them, with the sink and newest blocks; no
+         * exploration.  A budget of every block still selects every block. */
+        if (oracle_budget(nb, cfg->top_k, b, rho_bp) >= nb) {
+            memset(mask, 1, (size_t)nb);
+            return nb;
+        }
+        score_idx* sl = (score_idx*)malloc(sizeof(score_idx) * (size_t)n_slots);
+        for (int64_t i = 0; i < n_slots; ++i) {
+            sl[i].s = predicted_slot_score(cfg, V_req, D_req, q, i);
+            sl[i].j = i;
+        }
+        qsort(sl, (size_t)n_slots, sizeof(score_idx), cmp_score_desc);
+        mask[0] = 1;
+        mask[nb - 1] = 1;
+        for (int64_t k = 0; k < cfg->top_k && k < n_slots; ++k) mask[sl[k].j / b] = 1;
+        free(sl);
+        int64_t cnt = 0;
+        for (int64_t j = 0; j < nb; ++j) cnt += mask[j];
+        return cnt;
+    }
     float* S = (float*)malloc(sizeof(float) * (size_t)nb);  /* predict and pool */
     oracle_block_scores(cfg, V_req, D_req, n_slots, q, S);
     int64_t m = oracle_budget(nb, cfg->top_k, b, rho_bp);    /* budget */

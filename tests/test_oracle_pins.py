@@ -678,3 +678,43 @@ def test_pooling_invariants_on_real_values(oracle_mod, n):
     for p, c in cfgs.items():  # N = 65: the second block holds one slot
         S1 = oracle_mod.block_scores(c, V, D, 65, 68)
         assert S1[1] == max(V[64], D[68 - 64])
+
+
+# ------------------------------------------------------- A0 block reduction (§4.6)
+
+@pytest.mark.parametrize("combine", ["max", "sum"])
+@pytest.mark.parametrize("n,top_k", [(290, 16), (150, 40), (64, 16), (297, 1)])
+def test_a0_selects_the_blocks_of_the_top_k_predicted_slots(oracle_mod, combine, n, top_k):
+    """A0: numpy brute force -- the K slots with the largest predicted score (ties: lower
+    slot), then every block holding one, plus the sink and newest blocks."""
+    o = oracle_mod
+    cfg = tiny_cfg(o, combine=combine, pooling="slots", top_k=top_k, n_req=1, rho_bp=6000)
+    rng = np.random.default_rng(n + top_k)
+    V = rng.integers(-5, 6, cfg.max_slots).astype(np.float32)   # small integers: many ties
+    D = rng.integers(-5, 6, o.d_len(cfg)).astype(np.float32)
+    q = n + 2
+    warm = np.ones(1, np.int32)
+    blocks, nb_, _, _, ok = o.select_blocks(cfg, V[None], D[None], warm, np.array([n], np.int32),
+                                            np.array([q], np.int32), 1, -1, 0, 0)
+    assert ok
+    i = np.arange(n)
+    pred = np.maximum(V[:n], D[q - i]) if combine == "max" else V[:n] + D[q - i]
+    order = np.lexsort((i, -pred.astype(np.float64)))
+    nblk = -(-n // 64)
+    want = sorted(set((order[:top_k] // 64).tolist()) | {0, nblk - 1})
+    assert blocks[0, 0, : nb_[0, 0]].tolist() == want
+
+
+def test_a0_dense_cases(oracle_mod):
+    """Cold requests, budgets of every block (rho = 0) and K >= N select every block."""
+    o = oracle_mod
+    n = 280
+    for rho, top_k, warm in ((4000, 16, 0), (0, 16, 1), (4000, 300, 1)):
+        cfg = tiny_cfg(o, pooling="slots", top_k=top_k, n_req=1, rho_bp=rho)
+        rng = np.random.default_rng(rho + top_k)
+        V = rng.standard_normal(cfg.max_slots).astype(np.float32)
+        D = rng.standard_normal(o.d_len(cfg)).astype(np.float32)
+        blocks, nb_, _, _, ok = o.select_blocks(cfg, V[None], D[None], np.array([warm], np.int32),
+                                                np.array([n], np.int32), np.array([n + 1], np.int32),
+                                                1, -1, 0, 0)
+        assert ok and blocks[0, 0, : nb_[0, 0]].tolist() == list(range(-(-n // 64)))
