@@ -96,6 +96,14 @@ typedef enum spin_dtype { SPIN_DTYPE_F32 = 0, SPIN_DTYPE_BF16 = 1, SPIN_DTYPE_E4
  * V[i] + D[q-i]. */
 typedef enum spin_combine { SPIN_COMBINE_MAX = 0, SPIN_COMBINE_SUM = 1 } spin_combine_t;
 
+/* Block pooling of the predicted slot scores.  MAX is Eq. 2 (the method).  MEAN and TOP4 are
+ * the pooling ablations of §4.6 ("Block reduction"), for diagnostics: the mean of the block's
+ * slot predictions (slots i < N), or the mean of its (up to) four largest.  Their fp32 sums
+ * have a fixed order -- MEAN: slots l and l + 32 first, then the 32 pair sums pairwise at
+ * distance 16, 8, 4, 2, 1; TOP4: (t1 + t2) + (t3 + t4) in descending order -- divided
+ * (correctly rounded) by the count. */
+typedef enum spin_pooling { SPIN_POOL_MAX = 0, SPIN_POOL_MEAN = 1, SPIN_POOL_TOP4 = 2 } spin_pooling_t;
+
 /* Indexer-score kernel choice.  AUTO takes the tensor-core kernel when the key is shared
  * by all heads (kv_heads == 1) and the shape is supported, the streaming CUDA-core
  * kernel for per-head keys, and the generic kernel otherwise. */
@@ -123,7 +131,7 @@ typedef struct spin_config {
     int32_t combine;     /* spin_combine_t */
     uint64_t seed;       /* exploration key */
     int32_t score_path;  /* spin_score_path_t */
-    int32_t reserved;    /* must be 0 */
+    int32_t pooling;     /* spin_pooling_t: MAX (Eq. 2, the method) or an ablation variant */
 } spin_config;
 
 /* Zero V, D and Vmax and mark the request cold: the reset after prefill and at every
@@ -368,6 +376,17 @@ spin_status_t spin_miss_curve(const float* S, int32_t n_req, int64_t s_stride, c
 spin_status_t spin_allocate_budgets(const float* miss, int32_t n_layers, int32_t n_points,
                                     int32_t target_g, int32_t g_min, int32_t* g_out,
                                     int32_t* rho_bp_out);
+
+/* Self-test of the bounded wait the pipelined kernels use on their shared-memory stage
+ * barriers (no counterpart in the paper: it checks the library's failure handling).  One
+ * CTA waits on an mbarrier with a limit of limit_ns (0 < limit_ns <= 10 s) of GPU global time:
+ *   mode 0: nobody arrives -- the wait must end at the limit;
+ *   mode 1: the kernel's abort flag is raised first -- the wait must end at once;
+ *   mode 2: a second warp arrives -- the wait must succeed.
+ * A wait that gives up sets SPIN_STATUS_TIMEOUT in *status (device); *elapsed_ns (device)
+ * receives the time the wait took. */
+spin_status_t spin_selftest_wait(int32_t mode, uint64_t limit_ns, uint32_t* status,
+                                 uint64_t* elapsed_ns, spin_stream_t stream);
 
 /* Bytes of device workspace spin_select_blocks needs for `rows` rows. */
 spin_status_t spin_workspace_size(const spin_config* cfg, int32_t rows, size_t* bytes);

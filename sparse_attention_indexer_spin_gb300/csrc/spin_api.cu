@@ -63,7 +63,8 @@ static spin_status_t check_cfg(const spin_config* c) {
         return fail(SPIN_ERR_INVALID_ARG, "combine %d unknown", c->combine);
     if (c->score_path < SPIN_SCORE_AUTO || c->score_path > SPIN_SCORE_TCGEN05)
         return fail(SPIN_ERR_INVALID_ARG, "score_path %d unknown", c->score_path);
-    if (c->reserved != 0) return fail(SPIN_ERR_INVALID_ARG, "reserved must be 0");
+    if (c->pooling < SPIN_POOL_MAX || c->pooling > SPIN_POOL_TOP4)
+        return fail(SPIN_ERR_INVALID_ARG, "pooling %d unknown", c->pooling);
     return SPIN_OK;
 }
 
@@ -455,6 +456,18 @@ spin_status_t spin_allocate_budgets(const float* miss, int32_t n_layers, int32_t
         for (int32_t l = 0; l < n_layers; ++l)
             rho_bp_out[l] = 10000 - (int32_t)((int64_t)g_out[l] * 10000 / (n_points - 1));
     return SPIN_OK;
+}
+
+spin_status_t spin_selftest_wait(int32_t mode, uint64_t limit_ns, uint32_t* status, uint64_t* elapsed_ns,
+                                spin_stream_t stream) {
+    g_err[0] = 0;
+    if (mode < 0 || mode > 2) return fail(SPIN_ERR_INVALID_ARG, "mode %d outside [0, 2]", mode);
+    if (!status || !elapsed_ns) return fail(SPIN_ERR_INVALID_ARG, "status and elapsed_ns must be non-NULL");
+    if (limit_ns == 0 || limit_ns > 10ull * 1000ull * 1000ull * 1000ull)
+        return fail(SPIN_ERR_INVALID_ARG, "limit_ns outside (0, 10 s]");
+    return launched(launch_wait_selftest(mode, limit_ns, status, reinterpret_cast<unsigned long long*>(elapsed_ns),
+                                         (cudaStream_t)stream),
+                    "spin_selftest_wait");
 }
 
 const char* spin_version(void) { return "spin-gb300 0.1.0 sm_103a"; }

@@ -95,6 +95,10 @@ cudaError_t launch_topk_hint(const spin_config& cfg, const float* scores, const 
 
 int device_sm_count();
 
+// Self-test of the bounded mbarrier wait (spin_selftest.cu).
+cudaError_t launch_wait_selftest(int mode, uint64_t limit_ns, uint32_t* status, unsigned long long* elapsed_ns,
+                                 cudaStream_t s);
+
 // Per-layer block budgets (host functions; spin_budget.cu).  Arguments are validated by the
 // C-ABI wrappers.
 int64_t budget_blocks_host(int64_t nb, int64_t top_k, int32_t rho_bp);

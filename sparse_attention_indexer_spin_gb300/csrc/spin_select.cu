@@ -85,6 +85,72 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
     float* Sq = S + (int64_t)rr * dm.MB;
     uint32_t* Xq = X + (int64_t)rr * dm.MB;
     const bool sum = cfg.combine == SPIN_COMBINE_SUM;
+    // the exploration draws of blocks j0 .. j0 + BPW - 1 (used only for blocks that end up
+    // unselected): lane l < BPW / 8 computes one Philox output, the draws of the 8 blocks of
+    // group j0 / 8 + l
+    auto draws = [&](int64_t j0) {
+        if (lane < BPW / 8) {
+            const int64_t g = j0 / 8 + lane;
+            if (g * 8 < nb) {
+                uint32_t k8[8];
+                explore_keys8(seed, layer, step, r, req, g, k8);
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                    if (g * 8 + h < nb) Xq[g * 8 + h] = k8[h];
+            }
+        }
+    };
+    if (cfg.pooling != SPIN_POOL_MAX) {
+        // the pooling ablations (§4.6): every slot's prediction, then the block's mean, or
+        // the mean of its four largest, summed in the fixed order the interface states
+        for (int64_t j0 = ((int64_t)blockIdx.x * nw + wid) * BPW; j0 < nb;
+             j0 += (int64_t)gridDim.x * nw * BPW) {
+            draws(j0);
+            for (int b = 0; b < BPW && j0 + b < nb; ++b) {  // (warp-uniform)
+                const int64_t i0 = (j0 + b) * kBlock + lane, i1 = i0 + 32;
+                const bool vl = i0 < n, vh = i1 < n;
+                auto pred = [&](int64_t i) {
+                    const float v = Vq[i], d = Dq[qr - i];
+                    return sum ? __fadd_rn(v, d) : fmaxf(v, d);
+                };
+                const float pl = vl ? pred(i0) : 0.0f, ph = vh ? pred(i1) : 0.0f;
+                float score;
+                if (cfg.pooling == SPIN_POOL_MEAN) {
+                    float t = __fadd_rn(vl ? pl : 0.0f, vh ? ph : 0.0f);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+                    const int cnt = __popc(__ballot_sync(0xffffffffu, vl)) + __popc(__ballot_sync(0xffffffffu, vh));
+                    score = __fdiv_rn(t, (float)cnt);
+                } else {
+                    // the four largest values, one slot at a time (absent slots are -inf)
+                    float a = vl ? pl : -INFINITY, c = vh ? ph : -INFINITY;
+                    float top[4];
+                    int k = 0;
+                    for (; k < 4; ++k) {
+                        float m = fmaxf(a, c);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if (m == -INFINITY) break;
+                        top[k] = m;
+                        const unsigned ba = __ballot_sync(0xffffffffu, a == m);
+                        if (ba) {
+                            if (lane == __ffs(ba) - 1) a = -INFINITY;
+                        } else {
+                            const unsigned bc = __ballot_sync(0xffffffffu, c == m);
+                            if (lane == __ffs(bc) - 1) c = -INFINITY;
+                        }
+                    }
+                    float s4 = top[0];
+                    if (k == 2) s4 = __fadd_rn(top[0], top[1]);
+                    if (k == 3) s4 = __fadd_rn(__fadd_rn(top[0], top[1]), top[2]);
+                    if (k == 4) s4 = __fadd_rn(__fadd_rn(top[0], top[1]), __fadd_rn(top[2], top[3]));
+                    score = __fdiv_rn(s4, (float)k);
+                }
+                if (lane == 0) Sq[j0 + b] = score;
+            }
+        }
+        return;
+    }
     // each warp owns BPW consecutive blocks and issues all their loads first
     for (int64_t j0 = ((int64_t)blockIdx.x * nw + wid) * BPW; j0 < nb;
          j0 += (int64_t)gridDim.x * nw * BPW) {
@@ -96,19 +162,7 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
             hi[b] = i1 < n ? (sum ? __fadd_rn(Vq[i1], Dq[qr - i1]) : Dq[qr - i1]) : -FLT_MAX;
         }
         const float vm = (!sum && lane < BPW && j0 + lane < nb) ? Vm[j0 + lane] : -FLT_MAX;
-        // the exploration draws of these blocks (used only for blocks that end up
-        // unselected), computed while the loads are in flight: lane l < BPW / 8 computes
-        // one Philox output, the draws of the 8 blocks of group j0 / 8 + l
-        if (lane < BPW / 8) {
-            const int64_t g = j0 / 8 + lane;
-            if (g * 8 < nb) {
-                uint32_t k8[8];
-                explore_keys8(seed, layer, step, r, req, g, k8);
-#pragma unroll
-                for (int h = 0; h < 8; ++h)
-                    if (g * 8 + h < nb) Xq[g * 8 + h] = k8[h];
-            }
-        }
+        draws(j0);  // while the loads are in flight
 #pragma unroll
         for (int b = 0; b < BPW; ++b) {
             // every block of the loop has at least one slot < N, so the max is a real value

@@ -20,6 +20,7 @@ HEADER = os.path.join(ROOT, "include", "spin.h")
 
 DTYPE = {"f32": 0, "bf16": 1, "e4m3": 2}
 COMBINE = {"max": 0, "sum": 1}
+POOLING = {"max": 0, "mean": 1, "top4": 2}
 SCORE_PATH = {"auto": 0, "generic": 1, "stream": 2, "tcgen05": 3}
 
 STATUS_BITS = {
@@ -48,7 +49,7 @@ class SpinConfig(ctypes.Structure):
         ("kv_heads", ctypes.c_int32), ("q_dtype", ctypes.c_int32), ("k_dtype", ctypes.c_int32),
         ("top_k", ctypes.c_int32), ("rho_bp", ctypes.c_int32), ("gamma_bp", ctypes.c_int32),
         ("alpha", ctypes.c_float), ("combine", ctypes.c_int32), ("seed", ctypes.c_uint64),
-        ("score_path", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("score_path", ctypes.c_int32), ("pooling", ctypes.c_int32),
     ]
 
     @property
@@ -62,11 +63,11 @@ class SpinConfig(ctypes.Structure):
 
 def make_config(n_req, max_slots, max_rows, n_heads, head_dim, kv_heads, q_dtype, k_dtype, top_k,
                 rho_bp, gamma_bp, alpha, combine="max", seed=0, block=64, score_path="auto",
-                **_ignored) -> SpinConfig:
+                pooling="max", **_ignored) -> SpinConfig:
     return SpinConfig(int(n_req), int(max_slots), int(max_rows), int(block), int(n_heads),
                       int(head_dim), int(kv_heads), DTYPE[q_dtype], DTYPE[k_dtype], int(top_k),
                       int(rho_bp), int(gamma_bp), float(alpha), COMBINE[combine],
-                      int(seed) & 0xFFFFFFFFFFFFFFFF, SCORE_PATH[score_path], 0)
+                      int(seed) & 0xFFFFFFFFFFFFFFFF, SCORE_PATH[score_path], POOLING[pooling])
 
 
 def ensure_built() -> str:
@@ -107,6 +108,7 @@ def lib():
             "spin_update_ema": [C, P, P, P, P, P, P, P, P, P, P, P],
             "spin_commit_mtp": [C, P, P, P, P, P, i32, P, P, P, P, P, P, P],
             "spin_workspace_size": [C, i32, ctypes.POINTER(ctypes.c_size_t)],
+            "spin_selftest_wait": [i32, u64, P, P, P],
             "spin_miss_curve": [P, i32, i64, P, P, i32, i32, P],
             "spin_allocate_budgets": [P, i32, i32, i32, i32, P, P],
         }
@@ -177,6 +179,12 @@ def allocate_budgets(miss, target_g, g_min=0):
     _check(lib().spin_allocate_budgets(pm, L, n_points, int(target_g), int(g_min),
                                        ctypes.c_void_p(g.ctypes.data), ctypes.c_void_p(rho.ctypes.data)))
     return g, rho
+
+
+def selftest_wait(mode, limit_ns, status, elapsed_ns, stream=None):
+    """spin_selftest_wait: the library's bounded barrier wait, with no arrival (mode 0), the
+    abort flag raised (1) or an arrival (2)."""
+    _check(lib().spin_selftest_wait(int(mode), int(limit_ns), _ptr(status), _ptr(elapsed_ns), _stream(stream)))
 
 
 def version() -> str:

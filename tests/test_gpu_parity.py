@@ -349,3 +349,25 @@ def test_mtp_full_size_sampled():
     with their unions and deferred commits."""
     h = Harness(syn.CONFIGS["mtp"])
     run_steps(h, 5, score_requests=[0])
+
+
+# ------------------------------------------------------------------ pooling ablations
+
+@pytest.mark.parametrize("pooling", ["mean", "top4"])
+@pytest.mark.parametrize("combine", ["max", "sum"])
+def test_pooling_ablations(pooling, combine):
+    """The block-pooling ablations of §4.6 (mean, mean of the four largest): selections
+    bit-identical to the oracle's on ragged contexts, every step teacher-forced."""
+    wl = syn.CONFIGS["pr1"].replace(pooling=pooling, combine=combine, steps=6, n_req=3, n0=3001,
+                                    gamma_bp=1000)
+    h = Harness(wl)
+    h.inp.n_slots.copy_(torch.tensor([3001, 700, 65], dtype=torch.int32))
+    run_steps(h, 6)
+
+
+def test_pooling_ablation_many_rows():
+    """Top-4 pooling with four verifier rows and the 16-blocks-per-warp instance (many rows)."""
+    wl = syn.CONFIGS["mtp"].replace(pooling="top4", n_req=3, n0=5000, steps=4, n_heads=8, head_dim=64,
+                                    q_dtype="f32", k_dtype="f32", top_k=256)
+    h = Harness(wl)
+    run_steps(h, 4)
