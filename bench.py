@@ -606,6 +606,53 @@ def measure_workload(base, rho, W, K, topk, schedule, share=None, score_events=T
     return wk, rec
 
 
+def measure_budgets(name, W, K, period=8):
+    """Per-layer block budgets ("Per-layer block budgets" of the project page): every
+    `period` steps each layer runs a dense probe (selection at the budget floor, dense step,
+    miss curve), the budgets are re-allocated and published to a device table, and the other
+    steps select with their layer's entry.  Timed over K steps against the same layer-by-layer
+    steps with the uniform budget; host work of the probe steps (curves, allocation, the
+    synchronising copies) is inside the timed region."""
+    from sparse_attention_indexer_spin_gb300 import spin
+    from sparse_attention_indexer_spin_gb300.budgets import BudgetController
+    base = syn.CONFIGS[name]
+    out = {"period": period, "target_rho_bp": base.rho_bp}
+    for mode in ("uniform", "per_layer"):
+        wk = Workload(base, W + K, base.rho_bp, topk="plain", schedule="serial")
+        ctl = BudgetController(wk.cfg, wk.L, base.rho_bp, period=period) if mode == "per_layer" else None
+
+        def run(steps):
+            for s in steps:
+                for layer in range(wk.L):
+                    st = wk.states[layer]
+                    q, w = wk.q[s % len(wk.q)][layer], wk.w[s % len(wk.w)][layer]
+                    ns, qp = wk.n_slots[s], wk.q_pos[s]
+                    if ctl is None:
+                        spin.run_step(wk.cfg, st, wk.buf, q, w, wk.inp.k_pool[layer], wk.inp.k_scale[layer],
+                                      wk.inp.n_pages, wk.inp.block_table, ns, qp, s, layer)
+                    else:
+                        ctl.step(st, wk.buf, q, w, wk.inp.k_pool[layer], wk.inp.k_scale[layer], wk.inp.n_pages,
+                                 wk.inp.block_table, ns, qp, s, layer)
+                if ctl is not None and ctl.is_probe(s):
+                    ctl.publish()
+
+        wk.reset()
+        run(range(W))
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        run(range(W, W + K))
+        t1.record()
+        torch.cuda.synchronize()
+        out[mode + "_ms_per_step"] = t0.elapsed_time(t1) / K
+        if ctl is not None:
+            out["layer_rho_bp"] = [int(x) for x in ctl.table.cpu().tolist()]
+        del wk
+        torch.cuda.empty_cache()
+    out["per_layer_vs_uniform"] = out["per_layer_ms_per_step"] / out["uniform_ms_per_step"]
+    return out
+
+
 def run_config(name, W, K, topk, schedule, extra=()):
     """Every measurement of one workload: its sparsity sweep (or its target and 0), the dense
     ratio, realized sparsity and miss rate at its target.  Returns a per_config entry."""
@@ -771,6 +818,8 @@ def main():
             per_config["v32"]["serial_schedule_ms_per_step"] = r_serial["ms_per_step"]
             per_config["v32"]["plain_topk_ms_per_step"] = r_plain["ms_per_step"]
             torch.cuda.empty_cache()
+            # per-layer budgets with a dense probe every 8 steps (16 steps: two probes per layer)
+            per_config["v32"]["budgets_probe_every_8"] = measure_budgets("v32", W, 16, period=8)
         per_config["clocks"] = clocks2.stop()
 
     if rank == 0:
