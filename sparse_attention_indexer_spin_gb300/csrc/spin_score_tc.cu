@@ -13,11 +13,11 @@
 //   by 2D TMA in the 128-byte-swizzled K-major layout the MMA reads.
 // FP8 (e4m3) keys: kind::f8f6f4 straight from the TMA-loaded pages, no conversion.  q is
 //   carried as two e4m3 terms: for every (row, head) a power-of-two scale g puts
-//   max|q|/g in (224, 448]; hi = e4m3(q/g), lo = e4m3(q/g - hi).  Both terms are rows of
-//   the B operand (N = 2 x 64 per query row), so one MMA of K = 32 covers both and a tile
-//   needs 4 MMAs; the epilogue adds the hi and lo columns of a head, k.(hi + lo), where
-//   |q/g - hi - lo| <= 2^-8 |q/g| per element (plus the e4m3 subnormal floor), and
-//   multiplies by g.  The per-slot dequantisation scale is applied before the ReLU.
+//   max|q|/g in (224, 448]; hi = e4m3(q/g), lo = e4m3(q/g - hi).  The two terms are two
+//   B regions (N = 64 per query row); a tile's four K-steps over the hi terms and four over
+//   the lo terms accumulate into the same accumulator, k.(hi + lo), where
+//   |q/g - hi - lo| <= 2^-8 |q/g| per element (plus the e4m3 subnormal floor), and the
+//   epilogue multiplies by g.  The per-slot dequantisation scale is applied before the ReLU.
 // A tcgen05.mma costs a near-constant issue time whatever its N, so the kernel keeps
 // the instruction count per tile low and interleaves two tiles (two accumulator chains)
 // when TMEM holds four accumulators.
@@ -26,18 +26,18 @@
 // owns a contiguous range of whole tile pairs):
 //   warps 0, 2  producers of the even and odd tiles: one (FP8) or two (bf16) 2D TMA loads
 //               per page into a shared-memory ring
-//   warps 1, 3  MMA issuers (one elected thread each): 4 (FP8) or 8 (bf16) tcgen05.mma
-//               per tile.  With four accumulators in TMEM (N <= 128) warp 1 takes the even
-//               tiles and warp 3 the odd ones, two independent chains; with two, warp 1
-//               issues every tile.  Warp 1 owns the TMEM allocation; q is staged whenever
-//               the request changes.
+//   warps 1, 3  MMA issuers (one elected thread each): 8 tcgen05.mma per tile (FP8: 4 K-steps
+//               x hi and lo terms; bf16: 8 K-steps).  Warp 1 takes the even tiles and warp 3
+//               the odd ones, two independent accumulator chains.  Warp 1 owns the TMEM
+//               allocation; q is staged whenever the request changes.
 //   warps 4-11  epilogue, two warps per TMEM lane quarter taking alternate tiles:
 //               tcgen05.ld of a tile's accumulators (one slot per thread),
 //               z = sum_h w_h g_h max(s_i acc_h, 0) per row, masked to i < N, stored
 // Accumulators are 2-4 deep in TMEM (N <= 128: 4); the epilogue fetches the per-slot FP8
 // scales of its next tile while it works on the current one.
 // Every warp resolves its tiles' pages 32 at a time (one tile per lane), so the dependent
-// list and block-table loads are paid once per 32 tiles.  Every barrier wait is bounded
+// list and block-table loads are paid once per 32 tiles; the requests' sizes are read once
+// into shared memory with the tile prefix.  Every barrier wait is bounded
 // and a timeout unwinds all roles.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -251,8 +251,8 @@ __host__ __device__ inline TcLayout tc_layout(int R, int rows, bool fp8) {
     TcLayout L;
     L.tile_bytes = fp8 ? kTcM * kTcD : kTcM * kTcD * 2;  // 16 KB or 32 KB
     uint32_t off = 1024;                                 // header
-    L.prefix = off;
-    off += ((uint32_t)(R + 1) * 4 + 1023) & ~1023u;
+    L.prefix = off;  // tile prefix [R + 1], then (N, list length) per request [R]
+    off += ((uint32_t)(R + 1) * 4 + (uint32_t)R * 8 + 8 + 1023) & ~1023u;
     const uint32_t qbytes = (uint32_t)(64 * rows) * 256;             // two regions of N rows x 128 B
     const uint32_t wbytes = (uint32_t)kTcEpiWarps * 64 * rows * 4;    // w (times g) per epilogue warp
     const uint32_t sbytes = fp8 ? (uint32_t)(kTcScSlots * kTcScBytes) : 0u;  // slot scale ring
@@ -286,6 +286,7 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     const TcLayout L = tc_layout(dm.R, rows, FP8);
     TcHdr* hdr = reinterpret_cast<TcHdr*>(smem);
     int* prefix = reinterpret_cast<int*>(smem + L.prefix);
+    int2* reqinfo = reinterpret_cast<int2*>(smem + L.prefix + (((uint32_t)dm.R + 1) * 4 + 7) / 8 * 8);
     unsigned char* sA = smem + L.stage_a;
     unsigned char* sQ = smem + L.qbuf;
     float* sW = reinterpret_cast<float*>(smem + L.wbuf);
@@ -300,19 +301,31 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
     // ------------------------------------------------------------------ set-up
     if (wid == 0) {
         int carry = 0;
-        for (int base = 0; base < dm.R; base += 32) {
-            const int r = base + lane;
-            int c = 0;
-            if (r < dm.R) {
-                const int64_t n = a.n_slots[r], cnt = a.n_list[r];
-                const bool ok = n >= 0 && n <= dm.max_slots && cnt >= 0 && cnt <= dm.MB;
-                if (!ok && blockIdx.x == 0)
-                    set_status(a.status, (n < 0 || n > dm.max_slots) ? SPIN_STATUS_BAD_N : SPIN_STATUS_BAD_LIST);
-                c = ok ? 2 * (int)((cnt + 3) / 4) : 0;  // tiles, padded to even: see the issuers
+        for (int base = 0; base < dm.R; base += 128) {
+            // four chunks of 32 requests, their loads in flight together
+            int nn[4], cc[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = base + 32 * u + lane;
+                nn[u] = r < dm.R ? a.n_slots[r] : 0;
+                cc[u] = r < dm.R ? a.n_list[r] : 0;
             }
-            const int inc = warp_incl_scan(c);
-            if (r < dm.R) prefix[r] = carry + inc - c;
-            carry += __shfl_sync(0xffffffffu, inc, 31);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = base + 32 * u + lane;
+                int c = 0;
+                if (r < dm.R) {
+                    const int64_t n = nn[u], cnt = cc[u];
+                    const bool ok = n >= 0 && n <= dm.max_slots && cnt >= 0 && cnt <= dm.MB;
+                    if (!ok && blockIdx.x == 0)
+                        set_status(a.status, (n < 0 || n > dm.max_slots) ? SPIN_STATUS_BAD_N : SPIN_STATUS_BAD_LIST);
+                    c = ok ? 2 * (int)((cnt + 3) / 4) : 0;  // tiles, padded to even: see the issuers
+                    reqinfo[r] = make_int2(nn[u], cc[u]);
+                }
+                const int inc = warp_incl_scan(c);
+                if (r < dm.R) prefix[r] = carry + inc - c;
+                carry += __shfl_sync(0xffffffffu, inc, 31);
+            }
         }
         if (lane == 0) {
             prefix[dm.R] = carry;
@@ -389,7 +402,8 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         }
         ti.req = lo;
         ti.k0 = 2 * (t - prefix[lo]);
-        const int64_t n = a.n_slots[lo], cnt = a.n_list[lo];
+        const int2 rq = reqinfo[lo];  // (a request that owns tiles passed the checks above)
+        const int64_t n = rq.x, cnt = rq.y;
         const int64_t nb = (n + kBlock - 1) / kBlock;
         int bl[2], pg[2];
 #pragma unroll
@@ -630,17 +644,8 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         for (int t = t0 + (split_rows ? 0 : parity), it = split_rows ? 0 : parity; t < t1; t += tstep, it += tstep) {
             // FP8: this slot's scale, from the scale-ring entry the producer filled for tile it
             // (the warps that drain the tile free the entry once they have read it)
-            float scale = 1.0f;
-            if (FP8) {
-                const int c = it % kTcScSlots;
-                if (!mbar_wait(&hdr->sfull[c], (uint32_t)(it / kTcScSlots) & 1u, &hdr->abort_flag)) {
-                    fail_wait();
-                    break;
-                }
-                scale = sScale[c * 128 + m];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&hdr->sempty[c]);
-            }
+            // the tile's pages and (on a request change) the head weights first: they need no
+            // barrier, so their loads overlap the wait for the tile's data
             const TileInfo ti = tile(t);
             const int req = ti.req;
             if (req != cur_req) {
@@ -656,6 +661,17 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                 }
                 __syncwarp();
                 cur_req = req;
+            }
+            float scale = 1.0f;
+            if (FP8) {
+                const int c = it % kTcScSlots;
+                if (!mbar_wait(&hdr->sfull[c], (uint32_t)(it / kTcScSlots) & 1u, &hdr->abort_flag)) {
+                    fail_wait();
+                    break;
+                }
+                scale = sScale[c * 128 + m];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&hdr->sempty[c]);
             }
             const int page = h ? ti.page1 : ti.page0;
             const int blk = h ? ti.blk1 : ti.blk0;
