@@ -101,8 +101,16 @@ typedef enum spin_combine { SPIN_COMBINE_MAX = 0, SPIN_COMBINE_SUM = 1 } spin_co
  * slot predictions (slots i < N), or the mean of its (up to) four largest.  Their fp32 sums
  * have a fixed order -- MEAN: slots l and l + 32 first, then the 32 pair sums pairwise at
  * distance 16, 8, 4, 2, 1; TOP4: (t1 + t2) + (t3 + t4) in descending order -- divided
- * (correctly rounded) by the count. */
-typedef enum spin_pooling { SPIN_POOL_MAX = 0, SPIN_POOL_MEAN = 1, SPIN_POOL_TOP4 = 2 } spin_pooling_t;
+ * (correctly rounded) by the count.  SLOTS is §4.6's A0: the top_k slots with the largest
+ * predicted score (equal scores: lower slot), then every block holding one, plus the sink and
+ * newest blocks; no exploration and no block budget (a cold request or a budget of every
+ * block still selects every block).  SLOTS needs a larger workspace (spin_workspace_size). */
+typedef enum spin_pooling {
+    SPIN_POOL_MAX = 0,
+    SPIN_POOL_MEAN = 1,
+    SPIN_POOL_TOP4 = 2,
+    SPIN_POOL_SLOTS = 3
+} spin_pooling_t;
 
 /* Indexer-score kernel choice.  AUTO takes the tensor-core kernel when the key is shared
  * by all heads (kv_heads == 1) and the shape is supported, the streaming CUDA-core
@@ -388,7 +396,10 @@ spin_status_t spin_allocate_budgets(const float* miss, int32_t n_layers, int32_t
 spin_status_t spin_selftest_wait(int32_t mode, uint64_t limit_ns, uint32_t* status,
                                  uint64_t* elapsed_ns, spin_stream_t stream);
 
-/* Bytes of device workspace spin_select_blocks needs for `rows` rows. */
+/* Bytes of device workspace spin_select_blocks needs for `rows` rows: block scores and
+ * exploration draws (2 x 4 B per request, row and block), or under SPIN_POOL_SLOTS the slot
+ * predictions, an identity block list and the top-K slots (4 B per request, row and slot,
+ * and more); the stacked calls need n_layers times this. */
 spin_status_t spin_workspace_size(const spin_config* cfg, int32_t rows, size_t* bytes);
 
 /* Version string of the library ("spin-gb300 <major>.<minor>.<patch> sm_103a"). */

@@ -63,7 +63,7 @@ static spin_status_t check_cfg(const spin_config* c) {
         return fail(SPIN_ERR_INVALID_ARG, "combine %d unknown", c->combine);
     if (c->score_path < SPIN_SCORE_AUTO || c->score_path > SPIN_SCORE_TCGEN05)
         return fail(SPIN_ERR_INVALID_ARG, "score_path %d unknown", c->score_path);
-    if (c->pooling < SPIN_POOL_MAX || c->pooling > SPIN_POOL_TOP4)
+    if (c->pooling < SPIN_POOL_MAX || c->pooling > SPIN_POOL_SLOTS)
         return fail(SPIN_ERR_INVALID_ARG, "pooling %d unknown", c->pooling);
     return SPIN_OK;
 }

@@ -665,6 +665,204 @@ __global__ void __launch_bounds__(kSrThreads, 1) select_reg_kernel(
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// A0 (the §4.6 block-reduction ablation, SPIN_POOL_SLOTS): the K slots with the largest
+// predicted score (ties: lower slot) are found by the library's top-K over the predictions,
+// then expanded to the blocks holding them, with the forced sink and newest blocks; no
+// exploration.  Cold requests and budgets of every block select every block, as under A1.
+// ---------------------------------------------------------------------------------------
+
+// Predicted slot scores Z [R][rows][MB * 64] in slot order (0 past the context), the
+// identity block list [R][MB] and its length nb per request (0 for a request that fails its
+// checks, so the top-K skips it).
+__global__ void __launch_bounds__(256) slot_pred_kernel(spin_config cfg, const float* __restrict__ V,
+                                                        const float* __restrict__ D,
+                                                        const int32_t* __restrict__ n_slots,
+                                                        const int32_t* __restrict__ q_pos, int rows,
+                                                        float* __restrict__ Z, int32_t* __restrict__ list,
+                                                        int32_t* __restrict__ n_list) {
+    pdl_begin();
+    const Dims dm = dims_of(cfg);
+    const int rr = blockIdx.y;
+    const int req = rr / rows, r = rr - req * rows;
+    const int64_t n = n_slots[req], q = q_pos[req];
+    const bool ok = request_check(n, q, rows, dm) == 0u;
+    const int64_t nb = ok ? (n + kBlock - 1) / kBlock : 0;
+    const int64_t qr = q + r;
+    const float* Vq = V + (int64_t)req * dm.max_slots;
+    const float* Dq = D + (int64_t)req * dm.DL;
+    float* Zq = Z + (int64_t)rr * dm.MB * kBlock;
+    const bool sum = cfg.combine == SPIN_COMBINE_SUM;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nb * kBlock; i += stride) {
+        float z = 0.0f;
+        if (i < n) {
+            const float v = Vq[i], d = Dq[qr - i];
+            z = sum ? __fadd_rn(v, d) : fmaxf(v, d);
+        }
+        Zq[i] = z;
+    }
+    if (r == 0) {
+        for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < nb; j += stride)
+            list[(int64_t)req * dm.MB + j] = (int32_t)j;
+        if (blockIdx.x == 0 && threadIdx.x == 0) n_list[req] = (int32_t)nb;
+    }
+}
+
+// One CTA per request: each row's block set (a bitmap of MB bits in shared memory) from its
+// K slot indices and the forced blocks, written in ascending order; the rows' union.
+constexpr int kExpThreads = 1024;
+
+__device__ void expand_write(const uint32_t* bits, int nwords, int32_t* out, int32_t* count, int* scan) {
+    // ordered compaction of the set bits: a CTA scan of per-thread popcounts
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int per = (nwords + kExpThreads - 1) / kExpThreads;
+    const int w0 = tid * per, w1 = min(w0 + per, nwords);
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(bits[w]);
+    const int inc = warp_incl_scan(c);
+    if (lane == 31) scan[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        const int v = lane < kExpThreads / 32 ? scan[lane] : 0;
+        const int vi = warp_incl_scan(v);
+        if (lane < kExpThreads / 32) scan[lane] = vi - v;
+        if (lane == 31) scan[32] = vi;
+    }
+    __syncthreads();
+    int pos = scan[wid] + inc - c;
+    for (int w = w0; w < w1; ++w) {
+        uint32_t u = bits[w];
+        while (u) {
+            const int b = __ffs(u) - 1;
+            u &= u - 1u;
+            out[pos++] = w * 32 + b;
+        }
+    }
+    if (tid == 0) *count = scan[32];
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kExpThreads) slot_expand_kernel(
+    spin_config cfg, const int32_t* __restrict__ warm, const int32_t* __restrict__ n_slots,
+    const int32_t* __restrict__ q_pos, int rows, const int32_t* __restrict__ rho_override,
+    const int32_t* __restrict__ topk_idx, int32_t* __restrict__ blocks, int32_t* __restrict__ n_blocks,
+    int32_t* __restrict__ union_blocks, int32_t* __restrict__ n_union, uint32_t* status) {
+    pdl_begin();
+    extern __shared__ uint32_t xbits[];  // [2][MB / 32]: a row's blocks, the union
+    __shared__ int scan[33];
+    const Dims dm = dims_of(cfg);
+    const int MB = dm.MB, nw = (MB + 31) / 32;
+    const int req = blockIdx.x, tid = threadIdx.x;
+    const int64_t n = n_slots[req], q = q_pos[req];
+    uint32_t bad = request_check(n, q, rows, dm);
+    int32_t rho = cfg.rho_bp;
+    if (rho_override) {
+        rho = *rho_override;
+        if (rho < 0 || rho > 10000) bad |= SPIN_STATUS_BAD_RHO;
+    }
+    if (bad) {
+        if (tid == 0) {
+            set_status(status, bad);
+            for (int r = 0; r < rows; ++r) n_blocks[(int64_t)req * rows + r] = 0;
+            if (union_blocks && n_union) n_union[req] = 0;
+        }
+        return;
+    }
+    const int64_t nb = (n + kBlock - 1) / kBlock;
+    const bool dense = warm[req] == 0 || nb <= 2 || budget_blocks(nb, cfg.top_k, rho) >= nb;
+    uint32_t* rowb = xbits;
+    uint32_t* unib = xbits + nw;
+    for (int w = tid; w < nw; w += kExpThreads) unib[w] = 0u;
+    for (int r = 0; r < rows; ++r) {
+        const int64_t rr = (int64_t)req * rows + r;
+        __syncthreads();
+        for (int w = tid; w < nw; w += kExpThreads) {
+            uint32_t v = 0u;
+            if (dense) {  // every block j < nb
+                const int64_t lo = (int64_t)w * 32;
+                if (lo + 32 <= nb) v = 0xffffffffu;
+                else if (lo < nb) v = (1u << (nb - lo)) - 1u;
+            }
+            rowb[w] = v;
+        }
+        __syncthreads();
+        if (!dense) {
+            const int32_t* ti = topk_idx + rr * cfg.top_k;
+            for (int k = tid; k < cfg.top_k; k += kExpThreads) {
+                const int32_t i = ti[k];
+                if (i >= 0 && i < n) {
+                    const int j = i / kBlock;
+                    atomicOr(&rowb[j >> 5], 1u << (j & 31));
+                }
+            }
+            if (tid == 0) {
+                atomicOr(&rowb[0], 1u);
+                const int last = (int)nb - 1;
+                atomicOr(&rowb[last >> 5], 1u << (last & 31));
+            }
+            __syncthreads();
+        }
+        for (int w = tid; w < nw; w += kExpThreads) unib[w] |= rowb[w];
+        expand_write(rowb, nw, blocks + rr * MB, n_blocks + rr, scan);
+    }
+    if (union_blocks && n_union) {
+        __syncthreads();
+        expand_write(unib, nw, union_blocks + (int64_t)req * MB, n_union + req, scan);
+    }
+}
+
+// Workspace of A0: Z [R][rows][MB * 64] fp32, the identity list [R][MB] and its lengths [R],
+// the top-K slots [R][rows][K], each 256-byte aligned.
+static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+static size_t slots_workspace_bytes(const spin_config& cfg, int rows) {
+    const Dims dm = dims_of(cfg);
+    const size_t rrows = (size_t)dm.R * (size_t)rows;
+    return align256(sizeof(float) * rrows * (size_t)dm.MB * kBlock) + align256(sizeof(int32_t) * (size_t)dm.R * dm.MB) +
+           align256(sizeof(int32_t) * (size_t)dm.R) + align256(sizeof(int32_t) * rrows * (size_t)cfg.top_k);
+}
+
+// Every layer of a stack in turn: predictions, the library's top-K over them, expansion.
+static cudaError_t launch_select_slots(const spin_config& cfg, const SelectArgs& a, cudaStream_t s) {
+    const Dims dm = dims_of(cfg);
+    const int L = a.n_layers > 1 ? a.n_layers : 1;
+    const size_t per_layer = slots_workspace_bytes(cfg, a.rows);
+    const int64_t rrows = (int64_t)dm.R * a.rows;
+    const size_t xsmem = sizeof(uint32_t) * 2 * (size_t)((dm.MB + 31) / 32);
+    if (xsmem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(slot_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)xsmem);
+        if (e != cudaSuccess) return e;
+    }
+    for (int l = 0; l < L; ++l) {
+        unsigned char* ws = reinterpret_cast<unsigned char*>(a.block_scores) + (size_t)l * per_layer;
+        float* Z = reinterpret_cast<float*>(ws);
+        ws += align256(sizeof(float) * (size_t)rrows * dm.MB * kBlock);
+        int32_t* list = reinterpret_cast<int32_t*>(ws);
+        ws += align256(sizeof(int32_t) * (size_t)dm.R * dm.MB);
+        int32_t* n_list = reinterpret_cast<int32_t*>(ws);
+        ws += align256(sizeof(int32_t) * (size_t)dm.R);
+        int32_t* topk_idx = reinterpret_cast<int32_t*>(ws);
+        const float* V = a.V + (int64_t)l * dm.R * dm.max_slots;
+        const float* D = a.D + (int64_t)l * dm.R * dm.DL;
+        int gx = (int)((dm.MB * (int64_t)kBlock + 255) / 256);
+        if (gx > 64) gx = 64;
+        cudaError_t e = launch_pdl(slot_pred_kernel, dim3((unsigned)gx, (unsigned)rrows), dim3(256), 0, s, nullptr, 0,
+                                   cfg, V, D, a.n_slots, a.q_pos, a.rows, Z, list, n_list);
+        if (e != cudaSuccess) return e;
+        e = launch_topk(cfg, Z, list, n_list, a.n_slots, a.rows, topk_idx, a.status, s);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(slot_expand_kernel, dim3((unsigned)dm.R), dim3(kExpThreads), xsmem, s, nullptr, 0, cfg,
+                       a.warm + (int64_t)l * dm.R, a.n_slots, a.q_pos, a.rows,
+                       a.rho_override ? a.rho_override + l : nullptr, (const int32_t*)topk_idx,
+                       a.blocks + (int64_t)l * rrows * dm.MB, a.n_blocks + (int64_t)l * rrows,
+                       a.union_blocks ? a.union_blocks + (int64_t)l * dm.R * dm.MB : nullptr,
+                       a.n_union ? a.n_union + (int64_t)l * dm.R : nullptr, a.status);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 // Workspace: block scores S [R][rows][MB] (fp32), then exploration draws X [R][rows][MB]
 // (u32), each 256-byte aligned.
 static size_t select_array_bytes(const spin_config& cfg, int rows) {
@@ -673,11 +871,15 @@ static size_t select_array_bytes(const spin_config& cfg, int rows) {
     return (b + 255) & ~(size_t)255;
 }
 
-size_t select_workspace_bytes(const spin_config& cfg, int rows) { return 2 * select_array_bytes(cfg, rows); }
+size_t select_workspace_bytes(const spin_config& cfg, int rows) {
+    if (cfg.pooling == SPIN_POOL_SLOTS) return slots_workspace_bytes(cfg, rows);
+    return 2 * select_array_bytes(cfg, rows);
+}
 
 // Layer stacks: every array of layer l starts l layer-sizes after layer 0's; the workspace
 // holds the n_layers block-score arrays, then the n_layers exploration-draw arrays.
 cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStream_t s) {
+    if (cfg.pooling == SPIN_POOL_SLOTS) return launch_select_slots(cfg, a, s);
     const Dims dm = dims_of(cfg);
     const int L = a.n_layers > 1 ? a.n_layers : 1;
     const bool many_rows = (int64_t)dm.R * a.rows * L >= 8;

@@ -353,11 +353,12 @@ def test_mtp_full_size_sampled():
 
 # ------------------------------------------------------------------ pooling ablations
 
-@pytest.mark.parametrize("pooling", ["mean", "top4"])
+@pytest.mark.parametrize("pooling", ["mean", "top4", "slots"])
 @pytest.mark.parametrize("combine", ["max", "sum"])
 def test_pooling_ablations(pooling, combine):
-    """The block-pooling ablations of §4.6 (mean, mean of the four largest): selections
-    bit-identical to the oracle's on ragged contexts, every step teacher-forced."""
+    """The block-reduction ablations of §4.6 (A1 with mean or top-4 pooling; A0, the top-K
+    predicted slots expanded to their blocks): selections bit-identical to the oracle's on
+    ragged contexts (one of them all forced blocks), every step teacher-forced."""
     wl = syn.CONFIGS["pr1"].replace(pooling=pooling, combine=combine, steps=6, n_req=3, n0=3001,
                                     gamma_bp=1000)
     h = Harness(wl)
@@ -365,9 +366,20 @@ def test_pooling_ablations(pooling, combine):
     run_steps(h, 6)
 
 
-def test_pooling_ablation_many_rows():
-    """Top-4 pooling with four verifier rows and the 16-blocks-per-warp instance (many rows)."""
-    wl = syn.CONFIGS["mtp"].replace(pooling="top4", n_req=3, n0=5000, steps=4, n_heads=8, head_dim=64,
+@pytest.mark.parametrize("pooling", ["top4", "slots"])
+def test_pooling_ablation_many_rows(pooling):
+    """Top-4 pooling and A0 with four verifier rows (per-row selections and their union);
+    top-4 runs the 16-blocks-per-warp instance."""
+    wl = syn.CONFIGS["mtp"].replace(pooling=pooling, n_req=3, n0=5000, steps=4, n_heads=8, head_dim=64,
                                     q_dtype="f32", k_dtype="f32", top_k=256)
     h = Harness(wl)
     run_steps(h, 4)
+
+
+def test_a0_many_requests_and_budget_table():
+    """A0 over 40 requests (the sampled top-K kernel's instance), with a sparsity read from a
+    device table and then a table of 0 (every block)."""
+    wl = syn.CONFIGS["pr1"].replace(pooling="slots", n_req=40, n0=2500, steps=4, top_k=128)
+    h = Harness(wl)
+    run_steps(h, 2, rho=torch.tensor([5000], dtype=torch.int32, device="cuda"))
+    run_steps(h, 2, rho=torch.tensor([0], dtype=torch.int32, device="cuda"))
