@@ -231,8 +231,9 @@ spin_status_t spin_commit_mtp_layers(const spin_config* cfg, int32_t n_layers, f
  * (a static device array of 8 MiB, held on every GPU that loads the library until the
  * process exits).  It calls no cudaMalloc/cudaFree and no allocating library routine.
  *   - Capacity: n_req * rows * ceil(max_slots/64) <= 1048576 (a block score and an
- *     exploration draw per block and row); larger configurations are rejected with
- *     SPIN_ERR_CAPACITY.
+ *     exploration draw per block and row), and spin_workspace_size <= 8 MiB (which under
+ *     SPIN_POOL_SLOTS holds a prediction per slot); larger configurations are rejected
+ *     with SPIN_ERR_CAPACITY.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.  The cached
  *     address belongs to the device's current context: it does not survive

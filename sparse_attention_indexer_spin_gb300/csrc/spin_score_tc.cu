@@ -29,7 +29,10 @@
 //   warps 1, 3  MMA issuers (one elected thread each): 8 tcgen05.mma per tile (FP8: 4 K-steps
 //               x hi and lo terms; bf16: 8 K-steps).  Warp 1 takes the even tiles and warp 3
 //               the odd ones, two independent accumulator chains.  Warp 1 owns the TMEM
-//               allocation; q is staged whenever the request changes.
+//               allocation.  When the request changes, the issuers wait for their MMAs of
+//               the previous one and restage q: FP8, both convert half of the vectors (a
+//               quad of lanes per vector, the loads of four vectors in flight per lane);
+//               bf16, warp 1 copies the rows by TMA.
 //   warps 4-11  epilogue, two warps per TMEM lane quarter taking alternate tiles:
 //               tcgen05.ld of a tile's accumulators (one slot per thread),
 //               z = sum_h w_h g_h max(s_i acc_h, 0) per row, masked to i < N, stored
@@ -159,20 +162,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 
 
-// Scale g of one q row (128 values): the power of two with max|q|/g in (224, 448].
-__device__ __forceinline__ float q_row_scale(const __nv_bfloat16* qrow) {
-    float amax = 0.0f;
-    const uint4* p = reinterpret_cast<const uint4*>(qrow);
+// max|x| over the 8 bf16 values of one 16-byte word group
+__device__ __forceinline__ float amax_u4(float amax, const uint4 u) {
+    const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int c = 0; c < kTcD / 8; ++c) {
-        const uint4 u = p[c];
-        const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(wds[e] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(wds[e] & 0xffff0000u)));
-        }
+    for (int e = 0; e < 4; ++e) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(wds[e] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(wds[e] & 0xffff0000u)));
     }
+    return amax;
+}
+
+// Scale g of a q row from its max|q|: the power of two with max|q|/g in (224, 448].
+__device__ __forceinline__ float q_scale_of(float amax) {
     if (!(amax > 0.0f)) return 1.0f;
     const float t = fmaxf(amax * (1.0f / 448.0f), 1e-30f);
     const uint32_t bits = __float_as_uint(t);
@@ -181,40 +183,53 @@ __device__ __forceinline__ float q_row_scale(const __nv_bfloat16* qrow) {
     return g;
 }
 
-// FP8 query terms of one query vector (128 bf16 values, row n of both B regions) for its
-// 16-element chunks [c0, c1): hi = e4m3(q/g) into the region at sHi, lo = e4m3(q/g - hi)
-// into the region at sLo, each in the 128-byte-swizzled K-major layout the MMA reads.
-__device__ __forceinline__ void q8_convert(const __nv_bfloat16* qrow, float inv_g, int n, int c0, int c1,
-                                           unsigned char* sHi, unsigned char* sLo) {
-    const uint4* src = reinterpret_cast<const uint4*>(qrow);
-#pragma unroll 2
-    for (int ch = c0; ch < c1; ++ch) {
-        const uint4 u0 = src[2 * ch], u1 = src[2 * ch + 1];
-        const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-        uint32_t hw[4], lw[4];
+// Query vectors handled by a quad of lanes: lane (lane & 3) holds the 32 values
+// [32 (lane & 3), 32 (lane & 3) + 32) of the quad's vector as four 16-byte words, and the
+// quad agrees on the vector's scale.
+__device__ __forceinline__ void quad_load(const __nv_bfloat16* qrow, int lane, uint4 (&u)[4]) {
+    const uint4* p = reinterpret_cast<const uint4*>(qrow) + 4 * (lane & 3);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            uint32_t hv = 0, lv = 0;
+    for (int i = 0; i < 4; ++i) u[i] = p[i];
+}
+
+__device__ __forceinline__ float quad_scale(const uint4 (&u)[4]) {
+    float amax = 0.0f;
 #pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-                const uint32_t wd = wds[2 * e + pr];
-                const float2 x = make_float2(__uint_as_float(wd << 16) * inv_g, __uint_as_float(wd & 0xffff0000u) * inv_g);
-                const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
-                const __half2 hf = *reinterpret_cast<const __half2*>(
-                    &static_cast<const __half2_raw&>(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
-                const float2 hx = __half22float2(hf);
-                const float2 rx = make_float2(x.x - hx.x, x.y - hx.y);
-                const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(rx, __NV_SATFINITE, __NV_E4M3);
-                hv |= (uint32_t)h2 << (16 * pr);
-                lv |= (uint32_t)l2 << (16 * pr);
-            }
-            hw[e] = hv;
-            lw[e] = lv;
+    for (int i = 0; i < 4; ++i) amax = amax_u4(amax, u[i]);
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    return q_scale_of(amax);
+}
+
+// FP8 query terms of chunk ch (16 values held in u0, u1) of query vector n: hi = e4m3(q/g)
+// into the region at sHi, lo = e4m3(q/g - hi) into the region at sLo, row n of each, in the
+// 128-byte-swizzled K-major layout the MMA reads.
+__device__ __forceinline__ void q8_convert_chunk(const uint4 u0, const uint4 u1, float inv_g, int n, int ch,
+                                                 unsigned char* sHi, unsigned char* sLo) {
+    const uint32_t wds[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        uint32_t hv = 0, lv = 0;
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+            const uint32_t wd = wds[2 * e + pr];
+            const float2 x = make_float2(__uint_as_float(wd << 16) * inv_g, __uint_as_float(wd & 0xffff0000u) * inv_g);
+            const __nv_fp8x2_storage_t h2 = __nv_cvt_float2_to_fp8x2(x, __NV_SATFINITE, __NV_E4M3);
+            const __half2 hf = *reinterpret_cast<const __half2*>(
+                &static_cast<const __half2_raw&>(__nv_cvt_fp8x2_to_halfraw2(h2, __NV_E4M3)));
+            const float2 hx = __half22float2(hf);
+            const float2 rx = make_float2(x.x - hx.x, x.y - hx.y);
+            const __nv_fp8x2_storage_t l2 = __nv_cvt_float2_to_fp8x2(rx, __NV_SATFINITE, __NV_E4M3);
+            hv |= (uint32_t)h2 << (16 * pr);
+            lv |= (uint32_t)l2 << (16 * pr);
         }
-        const uint32_t o = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((ch ^ (n & 7)) << 4));
-        *reinterpret_cast<uint4*>(sHi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(sLo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        hw[e] = hv;
+        lw[e] = lv;
     }
+    const uint32_t o = (uint32_t)((n >> 3) * 1024 + (n & 7) * 128 + ((ch ^ (n & 7)) << 4));
+    *reinterpret_cast<uint4*>(sHi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(sLo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
 struct TileInfo {
@@ -382,11 +397,18 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         }
         const int req0 = lo;
         const int part = (wid == 1 ? 0 : wid == 3 ? 1 : wid - 2) * 32 + lane;  // 0 .. 319
-        for (int p = part; p < NQ * 4; p += 320) {
-            const int n = p >> 2, c = p & 3, r = n / kTcNH, h = n % kTcNH;
-            const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                        (((int64_t)req0 * rows + r) * kTcNH + h) * kTcD;
-            q8_convert(qrow, 1.0f / q_row_scale(qrow), r * kTcNH + h, 2 * c, 2 * c + 2, sQ, sQ + qregion);
+        for (int n0 = 0; n0 < NQ; n0 += 80) {  // 80 quads of lanes, one query vector each
+            const int n = n0 + (part >> 2);
+            uint4 u[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                          make_uint4(0, 0, 0, 0)};
+            if (n < NQ)
+                quad_load(reinterpret_cast<const __nv_bfloat16*>(a.q) + ((int64_t)req0 * rows * kTcNH + n) * kTcD,
+                          lane, u);
+            const float inv_g = 1.0f / quad_scale(u);
+            if (n < NQ) {
+                q8_convert_chunk(u[0], u[1], inv_g, n, 2 * (lane & 3), sQ, sQ + qregion);
+                q8_convert_chunk(u[2], u[3], inv_g, n, 2 * (lane & 3) + 1, sQ, sQ + qregion);
+            }
         }
         fence_async_smem();
         if (wid == 1 || wid == 3) named_barrier(1, 320);
@@ -552,33 +574,46 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
                     if (lane == 0) tc_commit(&hdr->qdone);
                     __syncwarp();
                 }
-                if (par == 0) {
-                    if (nchange > 0 && !mbar_wait(&hdr->qdone, (nchange - 1) & 1u, &hdr->abort_flag)) { fail_wait(); break; }
-                    if (FP8) {
-                        // row n = r*64 + h of the hi and of the lo region, 128 e4m3 each; lane
-                        // handles the query vectors n = lane, lane + 32, ... (the first request
-                        // of the range was staged by ten warps before the loops started)
-                        if (!(nchange == 0 && prestaged))
-                            for (int n = lane; n < NQ; n += 32) {
-                                const int r = n / kTcNH, h = n % kTcNH;
-                                const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                                            (((int64_t)req * rows + r) * kTcNH + h) * kTcD;
-                                q8_convert(qrow, 1.0f / q_row_scale(qrow), n, 0, kTcD / 16, sQ, sQ + qregion);
-                            }
-                        fence_async_smem();
-                        __syncwarp();
-                    } else {
-                        // q rows of this request by TMA, straight into the swizzled B layout
-                        if (lane == 0) {
-                            mbar_arrive_expect_tx(&hdr->qfull, (uint32_t)NQ * kTcD * 2);
-                            const int y = req * rows * kTcNH;
-                            tma_load_2d(sQ, &qmap, 0, y, &hdr->qfull);
-                            tma_load_2d(sQ + qregion, &qmap, 64, y, &hdr->qfull);
+                if (FP8) {
+                    // both issuers restage the query terms (the first request's were staged by ten
+                    // warps before the loops): each converts half of the vectors, a quad of lanes
+                    // per vector, four vectors' loads per lane in flight
+                    if (nchange > 0) {
+                        if (!__all_sync(0xffffffffu, mbar_wait(&hdr->qdone, (nchange - 1) & 1u, &hdr->abort_flag))) {
+                            fail_wait();
+                            break;
                         }
-                        __syncwarp();
-                        if (!mbar_wait(&hdr->qfull, qload_phase, &hdr->abort_flag)) { fail_wait(); break; }
-                        qload_phase ^= 1u;
+                        for (int p0 = 0; p0 < NQ / 16; p0 += 4) {
+                            uint4 u[4][4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int n = par * (NQ / 2) + 8 * (p0 + i) + (lane >> 2);
+                                quad_load(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                              ((int64_t)req * rows * kTcNH + n) * kTcD, lane, u[i]);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int n = par * (NQ / 2) + 8 * (p0 + i) + (lane >> 2);
+                                const float inv_g = 1.0f / quad_scale(u[i]);
+                                q8_convert_chunk(u[i][0], u[i][1], inv_g, n, 2 * (lane & 3), sQ, sQ + qregion);
+                                q8_convert_chunk(u[i][2], u[i][3], inv_g, n, 2 * (lane & 3) + 1, sQ, sQ + qregion);
+                            }
+                        }
+                        fence_async_smem();
+                        named_barrier(2, 64);  // both halves written
                     }
+                } else if (par == 0) {
+                    if (nchange > 0 && !mbar_wait(&hdr->qdone, (nchange - 1) & 1u, &hdr->abort_flag)) { fail_wait(); break; }
+                    // q rows of this request by TMA, straight into the swizzled B layout
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&hdr->qfull, (uint32_t)NQ * kTcD * 2);
+                        const int y = req * rows * kTcNH;
+                        tma_load_2d(sQ, &qmap, 0, y, &hdr->qfull);
+                        tma_load_2d(sQ + qregion, &qmap, 64, y, &hdr->qfull);
+                    }
+                    __syncwarp();
+                    if (!mbar_wait(&hdr->qfull, qload_phase, &hdr->abort_flag)) { fail_wait(); break; }
+                    qload_phase ^= 1u;
                     if (lane == 0) mbar_arrive(&hdr->qready);
                 } else {
                     if (!mbar_wait(&hdr->qready, nchange & 1u, &hdr->abort_flag)) { fail_wait(); break; }
@@ -650,14 +685,26 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
             const int req = ti.req;
             if (req != cur_req) {
                 __syncwarp();
-                for (int n = lane; n < NQ; n += 32) {
-                    float g = 1.0f;
-                    if (FP8) {
-                        const int r = n / kTcNH, hh = n % kTcNH;
-                        g = q_row_scale(reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                        (((int64_t)req * rows + r) * kTcNH + hh) * kTcD);
+                if (FP8) {
+                    // w_n g_n, a quad of lanes per query vector, four vectors' loads in flight
+                    for (int p0 = 0; p0 < NQ / 8; p0 += 4) {
+                        uint4 u[4][4];
+                        float wv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int n = 8 * (p0 + i) + (lane >> 2);
+                            quad_load(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                          ((int64_t)req * rows * kTcNH + n) * kTcD, lane, u[i]);
+                            wv[i] = a.w[(int64_t)req * rows * kTcNH + n];
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float g = quad_scale(u[i]);
+                            if ((lane & 3) == 0) wloc[8 * (p0 + i) + (lane >> 2)] = wv[i] * g;
+                        }
                     }
-                    wloc[n] = a.w[(int64_t)req * rows * kTcNH + n] * g;
+                } else {
+                    for (int n = lane; n < NQ; n += 32) wloc[n] = a.w[(int64_t)req * rows * kTcNH + n];
                 }
                 __syncwarp();
                 cur_req = req;
