@@ -447,13 +447,84 @@ score_tc_kernel(spin_config cfg, ScoreArgs a, const __grid_constant__ CUtensorMa
         ti.blk0 = bl[0]; ti.blk1 = bl[1]; ti.page0 = pg[0]; ti.page1 = pg[1];
         ti.n = (int)n;
     };
-    // warp-cooperative: lane j resolves tile base + j; tile() broadcasts one tile's info
-    TileInfo mine;
-    int batch_base = -1;
+    // warp-cooperative: lane j resolves tile base + j; tile() broadcasts one tile's info.  FP8:
+    // the next batch (base + 32, where every role's next request lands) is resolved ahead in
+    // two steps whose loads are consumed only later: its list entries when a batch starts, its
+    // block-table entries half-way through it.
+    TileInfo mine, pf;
+    int batch_base = -1, pf_base = -1, pf_step = 0;  // pf_step: 1 = list entries read, 2 = pages read
+    int pf_b0 = -1, pf_b1 = -1, pf_p0 = -1, pf_p1 = -1;
+    auto pf_list = [&](int base) {
+        pf_base = base;
+        pf_step = 1;
+        const int t = base + lane;
+        pf.req = -1;
+        pf_b0 = pf_b1 = -1;
+        if (t < t1) {
+            int lo = 0, hi = dm.R - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+            }
+            pf.req = lo;
+            pf.k0 = 2 * (t - prefix[lo]);
+            const int2 rq = reqinfo[lo];
+            pf.n = rq.x;
+            if (pf.k0 < rq.y) pf_b0 = a.list[(int64_t)lo * dm.MB + pf.k0];
+            if (pf.k0 + 1 < rq.y) pf_b1 = a.list[(int64_t)lo * dm.MB + pf.k0 + 1];
+        }
+    };
+    auto pf_pages = [&]() {
+        pf_step = 2;
+        pf_p0 = pf_p1 = -1;
+        if (pf.req >= 0) {
+            const int64_t nb = ((int64_t)pf.n + kBlock - 1) / kBlock;
+            if (pf_b0 >= 0 && pf_b0 < nb) pf_p0 = a.block_table[(int64_t)pf.req * a.bt_stride + pf_b0];
+            if (pf_b1 >= 0 && pf_b1 < nb) pf_p1 = a.block_table[(int64_t)pf.req * a.bt_stride + pf_b1];
+        }
+    };
+    auto pf_finish = [&](TileInfo& ti) {  // the same values decode() gives
+        ti.req = pf.req;
+        ti.k0 = pf.k0;
+        ti.n = pf.n;
+        const int64_t nb = ((int64_t)pf.n + kBlock - 1) / kBlock;
+        const int2 rq = pf.req >= 0 ? reqinfo[pf.req] : make_int2(0, 0);
+        int bl[2] = {-1, -1}, pg[2] = {-1, -1};
+        const int braw[2] = {pf_b0, pf_b1}, praw[2] = {pf_p0, pf_p1};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (pf.req >= 0 && pf.k0 + h < rq.y) {
+                const int b = braw[h];
+                bl[h] = b;
+                if (b >= 0 && b < nb) {
+                    const int p = praw[h];
+                    if (p >= 0 && p < a.n_pages) pg[h] = p;
+                } else {
+                    bl[h] = -2;
+                }
+            }
+        }
+        ti.blk0 = bl[0]; ti.blk1 = bl[1]; ti.page0 = pg[0]; ti.page1 = pg[1];
+    };
     auto refresh = [&](int t) {  // make the batch hold tile t (t non-decreasing per warp)
+        if (!FP8) {  // bf16 tiles take twice as long: their dependent loads hide (measured)
+            if (batch_base < 0 || t >= batch_base + 32) {
+                batch_base = t;
+                if (t + lane < t1) decode(t + lane, mine);
+            }
+            return;
+        }
         if (batch_base < 0 || t >= batch_base + 32) {
+            if (t == pf_base && pf_step > 0) {
+                if (pf_step == 1) pf_pages();
+                if (t + lane < t1) pf_finish(mine);
+            } else if (t + lane < t1) {
+                decode(t + lane, mine);
+            }
             batch_base = t;
-            if (t + lane < t1) decode(t + lane, mine);
+            pf_list(t + 32);
+        } else if (pf_step == 1 && t - batch_base >= 16) {
+            pf_pages();
         }
     };
     auto bc = [&](int v, int t) { return __shfl_sync(0xffffffffu, v, t - batch_base); };
