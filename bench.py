@@ -520,6 +520,13 @@ def host_inputs_for_oracle(wk_or_inp, wl, layer=0):
     return pool, scale, bt
 
 
+def workload_label(wl, n_layers, n0, rho):
+    """The workload as both arms name it in their JSON line's config."""
+    return ("%s: %d req x %d layers, %d slots, %d heads x %d, kv_heads %d, %s keys, K=%d, rho=%.0f%%, "
+            "gamma=%.0f%%, rows=%d" % (wl.name, wl.n_req, n_layers, n0, wl.n_heads, wl.head_dim, wl.kv_heads,
+                                       wl.k_dtype, wl.top_k, rho / 100, wl.gamma_bp / 100, wl.rows))
+
+
 def run_reference(args):
     """The CPU oracle arm: each step a bounded sample of the workload on host cores."""
     wl = syn.CONFIGS[args.config]
@@ -548,7 +555,9 @@ def run_reference(args):
         "unit": "slots/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "sample": "request 0, layer 0, %d selected blocks per step" % bps},
+        "config": {"workload": workload_label(wl, args.layers or wl.n_layers, args.n0 or wl.n0, rho),
+                   "combine": wl.combine,
+                   "sample": "request 0, layer 0, %d selected blocks per step" % bps},
         "cpu_baseline": {"kind": "oracle", "value": rate, "unit": "slots/s", "cores": 1,
                          "sample": "per step: selection over the full context of request 0 (layer 0), "
                                    "then score/top-K/EMA over its first %d selected blocks" % bps},
@@ -837,10 +846,7 @@ def main():
             "vs_baseline": None,
             "dtype": wl.k_dtype if wl.k_dtype != "e4m3" else "e4m3/bf16",
             "data": "synthetic",
-            "config": {"workload": "%s: %d req x %d layers, %d slots, %d heads x %d, kv_heads %d, %s keys, "
-                                   "K=%d, rho=%.0f%%, gamma=%.0f%%, rows=%d"
-                                   % (wl.name, wl.n_req, base.n_layers, base.n0, wl.n_heads, wl.head_dim,
-                                      wl.kv_heads, wl.k_dtype, wl.top_k, rho / 100, wl.gamma_bp / 100, wl.rows),
+            "config": {"workload": workload_label(wl, base.n_layers, base.n0, rho),
                        "l2": "inputs larger than L2 (keys of every layer in their own pool, %.2f GB each)"
                              % (base.n_req * base.max_blocks * 64 * (wl.kv_heads * wl.head_dim *
                                 {"f32": 4, "bf16": 2, "e4m3": 1}[wl.k_dtype]) / 1e9),

@@ -68,7 +68,7 @@ def test_reference_arm_prints_contract_line(oracle_mod):
     assert d["value"] > 0 and d["steps"] == 2 and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
-    assert d["config"]["workload"] == "pr1"
+    assert d["config"]["workload"].startswith("pr1: 1 req x 1 layers")
 
 
 def test_reference_arm_other_ranks_exit_quietly(oracle_mod):
