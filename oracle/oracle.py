@@ -18,7 +18,7 @@ from . import build as _build
 
 DTYPES = {"f32": 0, "bf16": 1, "e4m3": 2}
 COMBINES = {"max": 0, "sum": 1}
-POOLINGS = {"max": 0, "mean": 1, "top4": 2, "slots": 3}
+POOLINGS = {"max": 0, "mean": 1, "top4": 2, "slots": 3, "a2": 4}
 RAW_NP = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}
 
 

@@ -204,11 +204,27 @@ static float pool_top4(const float* p, const int* valid) {
     return sum / (float)c;
 }
 
+/* §4.6, A2: block reduction before the predictor.  The state is kept per block: Vb[j] (the
+ * request's V[j]) and Db[o] (the request's D[o]) at the block offset o = floor(q / 64) - j of
+ * block j from the query's block, both EMAs of the block's pooled indexer score (its max over
+ * the live slots).  A block's predicted score combines them as Eq. 1 combines V and D. */
+static float a2_block_score(const oracle_cfg* cfg, const float* V_req, const float* D_req,
+                            int64_t q, int64_t j) {
+    float v = V_req[j];
+    float d = D_req[q / cfg->block - j];
+    if (cfg->combine == ORACLE_COMBINE_SUM) return v + d;
+    return v > d ? v : d;
+}
+
 void oracle_block_scores(const oracle_cfg* cfg, const float* V_req, const float* D_req,
                          int64_t n_slots, int64_t q, float* S_out) {
     int64_t b = cfg->block;
     int64_t nb = (n_slots + b - 1) / b;
     for (int64_t j = 0; j < nb; ++j) {
+        if (cfg->pooling == ORACLE_POOL_A2) {
+            S_out[j] = a2_block_score(cfg, V_req, D_req, q, j);
+            continue;
+        }
         int64_t lo = j * b;
         int64_t hi = (j + 1) * b < n_slots ? (j + 1) * b : n_slots;
         if (cfg->pooling == ORACLE_POOL_MEAN || cfg->pooling == ORACLE_POOL_TOP4) {
@@ -357,6 +373,7 @@ int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
     int64_t DL = d_len_of(cfg);
     int bad = 0;
     if (rho_bp < 0) rho_bp = cfg->rho_bp;
+    if (cfg->pooling == ORACLE_POOL_A2 && rows != 1) return -1;  /* A2: one query row */
     unsigned char* mask = (unsigned char*)malloc((size_t)MB + 1);
     unsigned char* umask = (unsigned char*)malloc((size_t)MB + 1);
     for (int32_t req = 0; req < cfg->n_req; ++req) {
@@ -539,6 +556,29 @@ int oracle_replay_ema(const oracle_cfg* cfg, float* V, float* D, int32_t* warm,
         }
         float* V_req = V + (int64_t)req * cfg->max_slots;
         float* D_req = D + (int64_t)req * DL;
+        if (cfg->pooling == ORACLE_POOL_A2) {
+            /* §4.6, A2: one observation per scored block, its max over the live slots (one
+             * query row) */
+            if (rows != 1) { bad = 1; continue; }
+            for (int64_t k = 0; k < cnt; ++k) {
+                int64_t blk = list[(int64_t)req * MB + k];
+                float zb = 0.0f;
+                int seen = 0;
+                for (int64_t s = 0; s < b; ++s) {
+                    int64_t i = blk * b + s;
+                    if (i >= n) continue;
+                    float z = scores[((int64_t)req * MB + k) * b + s];
+                    if (!seen || z > zb) zb = z;
+                    seen = 1;
+                }
+                if (!seen) continue;
+                float t = one_minus_alpha * zb;
+                V_req[blk] = fmaf(alpha, V_req[blk], t);
+                D_req[q / b - blk] = fmaf(alpha, D_req[q / b - blk], t);
+            }
+            warm[req] = 1;
+            continue;
+        }
         for (int64_t r = 0; r <= a; ++r) {
             for (int64_t k = 0; k < cnt; ++k) {
                 int64_t blk = list[(int64_t)req * MB + k];

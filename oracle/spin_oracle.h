@@ -31,7 +31,7 @@ extern "C" {
 
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2 };
 enum { ORACLE_COMBINE_MAX = 0, ORACLE_COMBINE_SUM = 1 };
-enum { ORACLE_POOL_MAX = 0, ORACLE_POOL_MEAN = 1, ORACLE_POOL_TOP4 = 2, ORACLE_POOL_SLOTS = 3 };
+enum { ORACLE_POOL_MAX = 0, ORACLE_POOL_MEAN = 1, ORACLE_POOL_TOP4 = 2, ORACLE_POOL_SLOTS = 3, ORACLE_POOL_A2 = 4 };
 
 typedef struct oracle_cfg {
     int32_t n_req;      /* R */
@@ -49,8 +49,11 @@ typedef struct oracle_cfg {
     float alpha;        /* EMA decay */
     int32_t combine;    /* ORACLE_COMBINE_MAX (Eq. 1) or ORACLE_COMBINE_SUM */
     uint64_t seed;      /* exploration key */
-    int32_t pooling;    /* ORACLE_POOL_MAX (Eq. 2), the MEAN / TOP4 ablations, or the A0
-                           ablation ORACLE_POOL_SLOTS (§4.6) */
+    int32_t pooling;    /* ORACLE_POOL_MAX (Eq. 2), the MEAN / TOP4 ablations, the A0
+                           ablation ORACLE_POOL_SLOTS or the A2 ablation ORACLE_POOL_A2
+                           (§4.6); under A2 the first ceil(max_slots/64) entries of a
+                           request's V hold the block-level vertical EMA and D[o] the
+                           block-level diagonal EMA at block offset o (one query row) */
 } oracle_cfg;
 
 /* Philox4x64-10 block function (Salmon et al., SC'11). */

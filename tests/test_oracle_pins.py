@@ -718,3 +718,87 @@ def test_a0_dense_cases(oracle_mod):
                                                 np.array([n], np.int32), np.array([n + 1], np.int32),
                                                 1, -1, 0, 0)
         assert ok and blocks[0, 0, : nb_[0, 0]].tolist() == list(range(-(-n // 64)))
+
+
+# ------------------------------------------------------- A2 block reduction (§4.6)
+
+def _a2_step(o, cfg, V, D, n, q, blocks, zfun):
+    """Score the listed blocks with zfun(slot) and apply the oracle's A2 update (one row)."""
+    MB = o.max_blocks(cfg)
+    blist = np.full((1, MB), -1, np.int32)
+    blist[0, : len(blocks)] = blocks
+    scores = np.zeros((1, 1, MB * 64), np.float32)
+    for k, b in enumerate(blocks):
+        for s in range(64):
+            scores[0, 0, k * 64 + s] = zfun(b * 64 + s)
+    warm = np.zeros(1, np.int32)
+    assert o.replay_ema(cfg, V, D, warm, scores, blist, np.array([len(blocks)], np.int32),
+                        np.array([n], np.int32), np.array([q], np.int32), 1)
+    return warm
+
+
+def test_a2_update_closed_form(oracle_mod):
+    """A2: n equal observations of a block give alpha^n V0 + (1 - alpha^n) z for the
+    block-level V and for the diagonal entry at the block offset floor(q/64) - j; the
+    observation is the block's max over its live slots; other entries stay unchanged."""
+    o = oracle_mod
+    cfg = tiny_cfg(o, pooling="a2", n_req=1, alpha=0.9)
+    n, q = 200, 203                      # blocks 0..3, the last holding slots 192..199
+    V = np.zeros((1, cfg.max_slots), np.float32)
+    D = np.zeros((1, o.d_len(cfg)), np.float32)
+    V[0, :4] = [1.0, -2.0, 0.5, 3.0]
+    D[0, :4] = [0.25, -1.0, 2.0, 0.0]
+    V0, D0 = V.copy(), D.copy()
+    # slot values: block 1 peaks at slot 100 (7.0), block 3's live slots peak at 199 (-0.5);
+    # slots past N (200..255) hold larger values, which must be ignored
+    z = lambda i: {100: 7.0, 199: -0.5}.get(i, -0.5 if 192 <= i < 200 else (9.0 if i >= 200 else -3.0))
+    for step in range(5):
+        warm = _a2_step(o, cfg, V, D, n, q, [1, 3], z)
+        assert warm[0] == 1
+    qb = q // 64
+    a5 = 0.9 ** 5
+    for j, zb in ((1, 7.0), (3, -0.5)):
+        assert abs(V[0, j] - (a5 * V0[0, j] + (1 - a5) * zb)) < 1e-5
+        assert abs(D[0, qb - j] - (a5 * D0[0, qb - j] + (1 - a5) * zb)) < 1e-5
+    assert V[0, 0] == V0[0, 0] and V[0, 2] == V0[0, 2]          # unscored blocks
+    assert D[0, qb - 0] == D0[0, qb] and D[0, qb - 2] == D0[0, qb - 2]
+    assert np.all(V[0, 4:] == 0) and np.all(D[0, 4:] == 0)      # no slot-level entries touched
+
+
+@pytest.mark.parametrize("combine", ["max", "sum"])
+def test_a2_selection_ranks_block_states(oracle_mod, combine):
+    """A2 selection: with D = -inf-like (or 0 under sum) the top blocks are numpy's ranking
+    of V's block entries; with V low the ranking follows D read at floor(q/64) - j, which
+    pins the direction of the block offset."""
+    o = oracle_mod
+    n, q = 297, 300                       # 5 blocks, query block 4
+    cfg = tiny_cfg(o, combine=combine, pooling="a2", n_req=1, rho_bp=4000, gamma_bp=0)
+    rng = np.random.default_rng(3)
+    nb = 5
+    m = max(-(-cfg.top_k // 64), -(-(10000 - 4000) * nb // 10000))
+    for which in ("V", "D"):
+        V = np.full((1, cfg.max_slots), -1e6 if which == "D" else 0.0, np.float32)
+        D = np.full((1, o.d_len(cfg)), -1e6 if which == "V" else 0.0, np.float32)
+        if combine == "sum":
+            (D if which == "V" else V)[:] = 0.0
+        vals = rng.permutation(nb).astype(np.float32)
+        if which == "V":
+            V[0, :nb] = vals
+            score = vals
+        else:
+            D[0, q // 64 - np.arange(nb)] = vals
+            score = vals
+        blocks, nbk, _, _, ok = o.select_blocks(cfg, V, D, np.ones(1, np.int32), np.array([n], np.int32),
+                                                np.array([q], np.int32), 1, -1, 0, 0)
+        assert ok
+        free = [j for j in range(nb) if j not in (0, nb - 1)]
+        ranked = sorted(free, key=lambda j: (-score[j], j))[: m - 2]
+        assert blocks[0, 0, : nbk[0, 0]].tolist() == sorted({0, nb - 1} | set(ranked))
+
+
+def test_a2_refuses_several_rows(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, pooling="a2", n_req=1)
+    V, D, warm = o.new_state(cfg)
+    *_, ok = o.select_blocks(cfg, V, D, warm, np.array([200], np.int32), np.array([203], np.int32), 2)
+    assert not ok
