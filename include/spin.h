@@ -104,12 +104,20 @@ typedef enum spin_combine { SPIN_COMBINE_MAX = 0, SPIN_COMBINE_SUM = 1 } spin_co
  * (correctly rounded) by the count.  SLOTS is §4.6's A0: the top_k slots with the largest
  * predicted score (equal scores: lower slot), then every block holding one, plus the sink and
  * newest blocks; no exploration and no block budget (a cold request or a budget of every
- * block still selects every block).  SLOTS needs a larger workspace (spin_workspace_size). */
+ * block still selects every block).  SLOTS needs a larger workspace (spin_workspace_size).
+ * A2 is §4.6's A2 with max pooling, for one query row: the state is kept per block -- the
+ * first ceil(max_slots/64) entries of a request's V hold the block-level vertical EMA Vb[j],
+ * and D[o] the block-level diagonal EMA at the block offset o = floor(q/64) - j from the
+ * query's block; spin_update_ema updates both with each scored block's max over its slots
+ * i < N (t = fl((1-alpha) zb), fma(alpha, old, t)); the predicted block score is
+ * max(Vb[j], Db[floor(q/64) - j]) (or their sum under SPIN_COMBINE_SUM); Vmax and the
+ * slot-level entries are not used.  rows > 1 is rejected with SPIN_ERR_UNSUPPORTED. */
 typedef enum spin_pooling {
     SPIN_POOL_MAX = 0,
     SPIN_POOL_MEAN = 1,
     SPIN_POOL_TOP4 = 2,
-    SPIN_POOL_SLOTS = 3
+    SPIN_POOL_SLOTS = 3,
+    SPIN_POOL_A2 = 4
 } spin_pooling_t;
 
 /* Indexer-score kernel choice.  AUTO takes the tensor-core kernel when the key is shared

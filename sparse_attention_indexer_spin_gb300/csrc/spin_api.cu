@@ -63,7 +63,7 @@ static spin_status_t check_cfg(const spin_config* c) {
         return fail(SPIN_ERR_INVALID_ARG, "combine %d unknown", c->combine);
     if (c->score_path < SPIN_SCORE_AUTO || c->score_path > SPIN_SCORE_TCGEN05)
         return fail(SPIN_ERR_INVALID_ARG, "score_path %d unknown", c->score_path);
-    if (c->pooling < SPIN_POOL_MAX || c->pooling > SPIN_POOL_SLOTS)
+    if (c->pooling < SPIN_POOL_MAX || c->pooling > SPIN_POOL_A2)
         return fail(SPIN_ERR_INVALID_ARG, "pooling %d unknown", c->pooling);
     return SPIN_OK;
 }
@@ -71,6 +71,8 @@ static spin_status_t check_cfg(const spin_config* c) {
 static spin_status_t check_rows(const spin_config* c, int rows) {
     if (rows < 1 || rows > c->max_rows) return fail(SPIN_ERR_SHAPE, "rows %d outside [1, max_rows=%d]", rows, c->max_rows);
     if ((int64_t)c->n_req * rows > 65535) return fail(SPIN_ERR_CAPACITY, "n_req * rows above 65535");
+    if (c->pooling == SPIN_POOL_A2 && rows > 1)
+        return fail(SPIN_ERR_UNSUPPORTED, "the A2 ablation keeps block-level state for one query row");
     return SPIN_OK;
 }
 

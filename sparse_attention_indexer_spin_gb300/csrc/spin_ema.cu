@@ -191,6 +191,31 @@ __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs 
     float* Dq = a.D + (int64_t)req * dm.DL;
     const int32_t* lst = a.list + (int64_t)req * dm.MB;
     const float* zq = a.scores + (int64_t)req * dm.MB * kBlock;
+    if (cfg.pooling == SPIN_POOL_A2) {
+        // the A2 ablation (§4.6): one observation per scored block, its max over the slots
+        // i < N, into the block-level EMAs (Vb[j] in V, Db at floor(q / 64) - j in D)
+        const int64_t qb = q / kBlock;
+        for (int64_t k = (int64_t)blockIdx.x * kEmaListWarps + wid; k < cnt;
+             k += (int64_t)gridDim.x * kEmaListWarps) {
+            const int64_t blk = lst[k];
+            if (!(blk >= 0 && blk < nb)) {  // (warp-uniform)
+                if (lane == 0) set_status(a.status, SPIN_STATUS_BAD_LIST);
+                continue;
+            }
+            float m = -INFINITY;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+                if (blk * kBlock + lane + 32 * hh < n) m = fmaxf(m, zq[k * kBlock + lane + 32 * hh]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) {
+                const float t = __fmul_rn(oma, m);
+                Vq[blk] = __fmaf_rn(alpha, Vq[blk], t);
+                Dq[qb - blk] = __fmaf_rn(alpha, Dq[qb - blk], t);
+            }
+        }
+        return;
+    }
     const int64_t stride = 2 * (int64_t)gridDim.x * kEmaListWarps;
     int64_t k0 = 2 * ((int64_t)blockIdx.x * kEmaListWarps + wid);
     int64_t nxt[2];

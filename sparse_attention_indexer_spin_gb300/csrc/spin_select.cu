@@ -100,6 +100,21 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
             }
         }
     };
+    if (cfg.pooling == SPIN_POOL_A2) {
+        // the A2 ablation (§4.6): block-level EMAs, Vb[j] in V and Db at the block offset
+        // floor(q / 64) - j in D, combined as Eq. 1 combines V and D
+        const int64_t qb = qr / kBlock;
+        for (int64_t j0 = ((int64_t)blockIdx.x * nw + wid) * BPW; j0 < nb;
+             j0 += (int64_t)gridDim.x * nw * BPW) {
+            draws(j0);
+            const int64_t j = j0 + lane;
+            if (lane < BPW && j < nb) {
+                const float v = Vq[j], d = Dq[qb - j];
+                Sq[j] = sum ? __fadd_rn(v, d) : fmaxf(v, d);
+            }
+        }
+        return;
+    }
     if (cfg.pooling != SPIN_POOL_MAX) {
         // the pooling ablations (§4.6): every slot's prediction, then the block's mean, or
         // the mean of its four largest, summed in the fixed order the interface states

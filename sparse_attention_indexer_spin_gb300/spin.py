@@ -20,7 +20,7 @@ HEADER = os.path.join(ROOT, "include", "spin.h")
 
 DTYPE = {"f32": 0, "bf16": 1, "e4m3": 2}
 COMBINE = {"max": 0, "sum": 1}
-POOLING = {"max": 0, "mean": 1, "top4": 2, "slots": 3}
+POOLING = {"max": 0, "mean": 1, "top4": 2, "slots": 3, "a2": 4}
 SCORE_PATH = {"auto": 0, "generic": 1, "stream": 2, "tcgen05": 3}
 
 STATUS_BITS = {

@@ -85,7 +85,8 @@ class Harness:
             assert gV.tobytes() == V1.tobytes(), "V differs"
             assert gD.tobytes() == D1.tobytes(), "D differs"
             np.testing.assert_array_equal(np_(st.warm), W1)
-            self.check_vmax(layer)
+            if wl.pooling != "a2":  # A2 keeps block-level state and no Vmax
+                self.check_vmax(layer)
         assert int(buf.status.item()) == 0, "status %#x" % int(buf.status.item())
         return dict(blocks=gb, n_blocks=gnb, blist=blist, nlist=nlist, scores=gsc,
                     topk=np_(buf.topk), worst=worst)

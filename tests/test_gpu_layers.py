@@ -189,12 +189,12 @@ def test_layers_host_validation():
                                st.warm, st.warm, buf.status)
 
 
-@pytest.mark.parametrize("rows", [1, 4])
-def test_select_layers_a0_equals_per_layer(rows):
-    """A0 (the top-K predicted slots expanded to blocks) through the stacked call, with a
-    per-layer sparsity table: identical to the per-layer calls."""
+@pytest.mark.parametrize("pooling,rows", [("slots", 1), ("slots", 4), ("a2", 1)])
+def test_select_layers_ablations_equal_per_layer(pooling, rows):
+    """A0 (the top-K predicted slots expanded to blocks) and A2 (block-level states) through
+    the stacked call, with a per-layer sparsity table: identical to the per-layer calls."""
     base = syn.CONFIGS["pr1"] if rows == 1 else syn.CONFIGS["mtp"]
-    wl = base.replace(pooling="slots", n_req=2, n0=6000, steps=6, n_heads=8, head_dim=64, kv_heads=8,
+    wl = base.replace(pooling=pooling, n_req=2, n0=6000, steps=6, n_heads=8, head_dim=64, kv_heads=8,
                       q_dtype="f32", k_dtype="f32", top_k=256, rows=rows,
                       mean_accept=2.4 if rows > 1 else 0.0, gamma_bp=1000)
     L = 3

@@ -353,12 +353,13 @@ def test_mtp_full_size_sampled():
 
 # ------------------------------------------------------------------ pooling ablations
 
-@pytest.mark.parametrize("pooling", ["mean", "top4", "slots"])
+@pytest.mark.parametrize("pooling", ["mean", "top4", "slots", "a2"])
 @pytest.mark.parametrize("combine", ["max", "sum"])
 def test_pooling_ablations(pooling, combine):
     """The block-reduction ablations of §4.6 (A1 with mean or top-4 pooling; A0, the top-K
-    predicted slots expanded to their blocks): selections bit-identical to the oracle's on
-    ragged contexts (one of them all forced blocks), every step teacher-forced."""
+    predicted slots expanded to their blocks; A2, block-level EMAs of max-pooled scores):
+    selections and EMA states bit-identical to the oracle's on ragged contexts (one of them
+    all forced blocks), every step teacher-forced."""
     wl = syn.CONFIGS["pr1"].replace(pooling=pooling, combine=combine, steps=6, n_req=3, n0=3001,
                                     gamma_bp=1000)
     h = Harness(wl)
@@ -383,3 +384,19 @@ def test_a0_many_requests_and_budget_table():
     h = Harness(wl)
     run_steps(h, 2, rho=torch.tensor([5000], dtype=torch.int32, device="cuda"))
     run_steps(h, 2, rho=torch.tensor([0], dtype=torch.int32, device="cuda"))
+
+
+def test_a2_refuses_several_rows():
+    """A2 keeps block-level state for one query row: several rows are refused on the host."""
+    wl = syn.CONFIGS["pr1"].replace(pooling="a2", n_req=2, rows=2, mean_accept=1.5)
+    cfg = spin.make_config(**wl.config_fields())
+    st = spin.LayerState(cfg)
+    buf = spin.StepBuffers(cfg)
+    ns = torch.tensor([700, 300], dtype=torch.int32, device="cuda")
+    blocks = torch.zeros((2, 2, cfg.max_blocks), dtype=torch.int32, device="cuda")
+    nbk = torch.zeros((2, 2), dtype=torch.int32, device="cuda")
+    un = torch.zeros((2, cfg.max_blocks), dtype=torch.int32, device="cuda")
+    nun = torch.zeros(2, dtype=torch.int32, device="cuda")
+    with pytest.raises(spin.SpinError):
+        spin.select_blocks(cfg, st.V, st.D, st.Vmax, st.warm, ns, ns - 1, 2, None, 0, 0, blocks, nbk, un, nun,
+                           buf.workspace, buf.status)
