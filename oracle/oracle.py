@@ -19,6 +19,7 @@ from . import build as _build
 DTYPES = {"f32": 0, "bf16": 1, "e4m3": 2}
 COMBINES = {"max": 0, "sum": 1}
 POOLINGS = {"max": 0, "mean": 1, "top4": 2, "slots": 3, "a2": 4}
+EXPLORES = {"random": 0, "age": 1}
 RAW_NP = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}
 
 
@@ -40,6 +41,7 @@ class OracleCfg(ctypes.Structure):
         ("combine", ctypes.c_int32),
         ("seed", ctypes.c_uint64),
         ("pooling", ctypes.c_int32),
+        ("explore", ctypes.c_int32),
     ]
 
 
@@ -68,6 +70,10 @@ def lib():
         L.oracle_block_scores.argtypes = [C, P, P, i64, i64, P]
         L.oracle_select_blocks.argtypes = [C, P, P, P, P, P, i32, i32, u64, i32, P, P, P, P]
         L.oracle_select_blocks.restype = ctypes.c_int
+        L.oracle_select_blocks_age.argtypes = [C, P, P, P, P, P, i32, i32, u64, i32, P, P, P, P, P]
+        L.oracle_select_blocks_age.restype = ctypes.c_int
+        L.oracle_block_age_update.argtypes = [C, P, P, P, P, u64]
+        L.oracle_block_age_update.restype = ctypes.c_int
         L.oracle_indexer_score.argtypes = [C, P, P, P, P, i64, P, i64, P, P, P, i32, P, P]
         L.oracle_indexer_score.restype = ctypes.c_int
         L.oracle_score_slot.argtypes = [C, P, P, P, ctypes.c_float, i32, P, P]
@@ -82,11 +88,12 @@ def lib():
 
 def make_cfg(n_req, max_slots, max_rows, n_heads, head_dim, kv_heads, q_dtype, k_dtype,
              top_k, rho_bp, gamma_bp, alpha, combine="max", seed=0, block=64, pooling="max",
-             **_ignored):
+             explore="random", **_ignored):
     return OracleCfg(int(n_req), int(max_slots), int(max_rows), int(block), int(n_heads),
                      int(head_dim), int(kv_heads), DTYPES[q_dtype], DTYPES[k_dtype],
                      int(top_k), int(rho_bp), int(gamma_bp), float(alpha),
-                     COMBINES[combine], int(seed) & 0xFFFFFFFFFFFFFFFF, POOLINGS[pooling])
+                     COMBINES[combine], int(seed) & 0xFFFFFFFFFFFFFFFF, POOLINGS[pooling],
+                     EXPLORES[explore])
 
 
 def max_blocks(cfg) -> int:
@@ -150,8 +157,9 @@ def block_scores(cfg, V_req, D_req, n_slots, q):
 
 # ---------------------------------------------------------------- the step
 
-def select_blocks(cfg, V, D, warm, n_slots, q_pos, rows=1, rho_bp=-1, step=0, layer=0):
-    """Returns (blocks [R][rows][MB], n_blocks [R][rows], union [R][MB], n_union [R], ok)."""
+def select_blocks(cfg, V, D, warm, n_slots, q_pos, rows=1, rho_bp=-1, step=0, layer=0, age=None):
+    """Returns (blocks [R][rows][MB], n_blocks [R][rows], union [R][MB], n_union [R], ok).
+    age: the block ages [R][MB] (uint32) of block-age exploration."""
     R, MB = cfg.n_req, max_blocks(cfg)
     V = _arr(V, np.float32)
     D = _arr(D, np.float32)
@@ -162,10 +170,24 @@ def select_blocks(cfg, V, D, warm, n_slots, q_pos, rows=1, rho_bp=-1, step=0, la
     n_blocks = np.zeros((R, rows), dtype=np.int32)
     union = np.full((R, MB), -1, dtype=np.int32)
     n_union = np.zeros(R, dtype=np.int32)
-    rc = lib().oracle_select_blocks(ctypes.byref(cfg), _p(V), _p(D), _p(warm), _p(n_slots),
-                                    _p(q_pos), rows, rho_bp, step, layer, _p(blocks),
-                                    _p(n_blocks), _p(union), _p(n_union))
+    if age is None:
+        rc = lib().oracle_select_blocks(ctypes.byref(cfg), _p(V), _p(D), _p(warm), _p(n_slots),
+                                        _p(q_pos), rows, rho_bp, step, layer, _p(blocks),
+                                        _p(n_blocks), _p(union), _p(n_union))
+    else:
+        age = _arr(age, np.uint32)
+        rc = lib().oracle_select_blocks_age(ctypes.byref(cfg), _p(V), _p(D), _p(warm), _p(n_slots),
+                                            _p(q_pos), rows, rho_bp, step, layer, _p(age), _p(blocks),
+                                            _p(n_blocks), _p(union), _p(n_union))
     return blocks, n_blocks, union, n_union, rc == 0
+
+
+def block_age_update(cfg, age, blist, n_list, n_slots, step):
+    """In place: age[req][blk] = step + 1 for every listed block (numpy uint32 [R][MB])."""
+    assert age.dtype == np.uint32 and age.flags["C_CONTIGUOUS"]
+    rc = lib().oracle_block_age_update(ctypes.byref(cfg), _p(age), _p(_arr(blist, np.int32)),
+                                       _p(_arr(n_list, np.int32)), _p(_arr(n_slots, np.int32)), int(step))
+    return rc == 0
 
 
 def indexer_score(cfg, q, w, k_pool, k_scale, block_table, blist, n_list, n_slots, rows=1,

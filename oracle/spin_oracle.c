@@ -293,7 +293,7 @@ static int request_ok(const oracle_cfg* cfg, int64_t n, int64_t q, int32_t rows)
 static int64_t select_row(const oracle_cfg* cfg, const float* V_req, const float* D_req,
                           int64_t n_slots, int64_t q, int warm, int32_t rho_bp,
                           uint64_t step, int32_t layer, int32_t row, int32_t req,
-                          unsigned char* mask) {
+                          const uint32_t* age_req, unsigned char* mask) {
     int64_t b = cfg->block;
     int64_t nb = (n_slots + b - 1) / b;                      /* block count */
     memset(mask, 0, (size_t)(nb > 0 ? nb : 1));
@@ -342,14 +342,15 @@ static int64_t select_row(const oracle_cfg* cfg, const float* V_req, const float
     qsort(cand, (size_t)nc, sizeof(score_idx), cmp_score_desc);
     for (int64_t k = 0; k < t && k < nc; ++k) mask[cand[k].j] = 1;
 
-    /* exploration: e distinct blocks drawn uniformly from the ones not yet selected,
-     * as the e smallest counter-based random keys */
+    /* exploration: e distinct blocks drawn uniformly from the ones not yet selected, as the
+     * e smallest counter-based random keys; or (block age, §4.6) the e observed least
+     * recently, as the e smallest ages */
     if (e > 0) {
         key_idx* ex = (key_idx*)malloc(sizeof(key_idx) * (size_t)nb);
         int64_t ne = 0;
         for (int64_t j = 0; j < nb; ++j)
             if (!mask[j]) {
-                ex[ne].u = oracle_explore_key(cfg->seed, layer, step, row, req, j);
+                ex[ne].u = age_req ? age_req[j] : oracle_explore_key(cfg->seed, layer, step, row, req, j);
                 ex[ne].j = j;
                 ++ne;
             }
@@ -364,16 +365,18 @@ static int64_t select_row(const oracle_cfg* cfg, const float* V_req, const float
     return cnt;
 }
 
-int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
-                         const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos,
-                         int32_t rows, int32_t rho_bp, uint64_t step, int32_t layer,
-                         int32_t* blocks, int32_t* n_blocks,
-                         int32_t* union_blocks, int32_t* n_union) {
+static int select_impl(const oracle_cfg* cfg, const float* V, const float* D,
+                       const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos,
+                       int32_t rows, int32_t rho_bp, uint64_t step, int32_t layer,
+                       const uint32_t* age, int32_t* blocks, int32_t* n_blocks,
+                       int32_t* union_blocks, int32_t* n_union) {
     int64_t MB = max_blocks_of(cfg);
     int64_t DL = d_len_of(cfg);
     int bad = 0;
     if (rho_bp < 0) rho_bp = cfg->rho_bp;
     if (cfg->pooling == ORACLE_POOL_A2 && rows != 1) return -1;  /* A2: one query row */
+    if ((cfg->explore == ORACLE_EXPLORE_AGE) != (age != NULL)) return -1;
+    if (cfg->explore == ORACLE_EXPLORE_AGE && rows != 1) return -1;  /* block age: one row */
     unsigned char* mask = (unsigned char*)malloc((size_t)MB + 1);
     unsigned char* umask = (unsigned char*)malloc((size_t)MB + 1);
     for (int32_t req = 0; req < cfg->n_req; ++req) {
@@ -388,7 +391,8 @@ int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
             int64_t cnt = 0;
             if (ok) {
                 select_row(cfg, V + (int64_t)req * cfg->max_slots, D + (int64_t)req * DL,
-                           n, q + r, warm[req], rho_bp, step, layer, r, req, mask);
+                           n, q + r, warm[req], rho_bp, step, layer, r, req,
+                           age ? age + (int64_t)req * MB : NULL, mask);
                 for (int64_t j = 0; j < nb; ++j)
                     if (mask[j]) { out[cnt++] = (int32_t)j; umask[j] = 1; }
             }
@@ -404,6 +408,44 @@ int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
     }
     free(mask);
     free(umask);
+    return bad ? -1 : 0;
+}
+
+int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
+                         const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos,
+                         int32_t rows, int32_t rho_bp, uint64_t step, int32_t layer,
+                         int32_t* blocks, int32_t* n_blocks,
+                         int32_t* union_blocks, int32_t* n_union) {
+    return select_impl(cfg, V, D, warm, n_slots, q_pos, rows, rho_bp, step, layer, NULL, blocks, n_blocks,
+                       union_blocks, n_union);
+}
+
+int oracle_select_blocks_age(const oracle_cfg* cfg, const float* V, const float* D,
+                             const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos,
+                             int32_t rows, int32_t rho_bp, uint64_t step, int32_t layer,
+                             const uint32_t* age, int32_t* blocks, int32_t* n_blocks,
+                             int32_t* union_blocks, int32_t* n_union) {
+    if (!age) return -1;
+    return select_impl(cfg, V, D, warm, n_slots, q_pos, rows, rho_bp, step, layer, age, blocks, n_blocks,
+                       union_blocks, n_union);
+}
+
+/* §4.6 "Staleness mitigation", block age: the listed blocks (those inside the context) were
+ * observed at this decode step. */
+int oracle_block_age_update(const oracle_cfg* cfg, uint32_t* age, const int32_t* list,
+                            const int32_t* n_list, const int32_t* n_slots, uint64_t step) {
+    int64_t MB = max_blocks_of(cfg);
+    int bad = 0;
+    for (int32_t req = 0; req < cfg->n_req; ++req) {
+        int64_t n = n_slots[req], cnt = n_list[req];
+        if (n < 0 || n > cfg->max_slots || cnt < 0 || cnt > MB) { bad = 1; continue; }
+        int64_t nb = (n + cfg->block - 1) / cfg->block;
+        for (int64_t k = 0; k < cnt; ++k) {
+            int64_t blk = list[(int64_t)req * MB + k];
+            if (blk < 0 || blk >= nb) { bad = 1; continue; }
+            age[(int64_t)req * MB + blk] = (uint32_t)(step + 1);
+        }
+    }
     return bad ? -1 : 0;
 }
 

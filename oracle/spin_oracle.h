@@ -32,6 +32,7 @@ extern "C" {
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2 };
 enum { ORACLE_COMBINE_MAX = 0, ORACLE_COMBINE_SUM = 1 };
 enum { ORACLE_POOL_MAX = 0, ORACLE_POOL_MEAN = 1, ORACLE_POOL_TOP4 = 2, ORACLE_POOL_SLOTS = 3, ORACLE_POOL_A2 = 4 };
+enum { ORACLE_EXPLORE_RANDOM = 0, ORACLE_EXPLORE_AGE = 1 };
 
 typedef struct oracle_cfg {
     int32_t n_req;      /* R */
@@ -54,6 +55,8 @@ typedef struct oracle_cfg {
                            (§4.6); under A2 the first ceil(max_slots/64) entries of a
                            request's V hold the block-level vertical EMA and D[o] the
                            block-level diagonal EMA at block offset o (one query row) */
+    int32_t explore;    /* ORACLE_EXPLORE_RANDOM (§3.2.1) or the block-age exploration of
+                           §4.6 "Staleness mitigation" (ORACLE_EXPLORE_AGE, one query row) */
 } oracle_cfg;
 
 /* Philox4x64-10 block function (Salmon et al., SC'11). */
@@ -85,6 +88,18 @@ int oracle_select_blocks(const oracle_cfg* cfg, const float* V, const float* D,
                          int32_t rows, int32_t rho_bp, uint64_t step, int32_t layer,
                          int32_t* blocks, int32_t* n_blocks,
                          int32_t* union_blocks, int32_t* n_union);
+/* oracle_select_blocks with block-age exploration (§4.6 "Staleness mitigation"): the
+ * exploration share goes to the not yet selected blocks observed least recently, i.e. with
+ * the smallest age[req][j] (the decode step + 1 at which block j was last scored, 0 =
+ * never), equal ages to the lower block. */
+int oracle_select_blocks_age(const oracle_cfg* cfg, const float* V, const float* D,
+                             const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos,
+                             int32_t rows, int32_t rho_bp, uint64_t step, int32_t layer,
+                             const uint32_t* age, int32_t* blocks, int32_t* n_blocks,
+                             int32_t* union_blocks, int32_t* n_union);
+/* Record that the listed blocks were scored at decode step `step`: age[req][blk] = step + 1. */
+int oracle_block_age_update(const oracle_cfg* cfg, uint32_t* age, const int32_t* list,
+                            const int32_t* n_list, const int32_t* n_slots, uint64_t step);
 
 /* Indexer score (Algorithm 1's scoring step) of every slot i < N of every listed block, for
  * `rows` query rows.  q: [R][rows][n_heads][d] in q_dtype; w: [R][rows][n_heads];

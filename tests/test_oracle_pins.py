@@ -802,3 +802,60 @@ def test_a2_refuses_several_rows(oracle_mod):
     V, D, warm = o.new_state(cfg)
     *_, ok = o.select_blocks(cfg, V, D, warm, np.array([200], np.int32), np.array([203], np.int32), 2)
     assert not ok
+
+
+# ------------------------------------------------ block-age exploration (§4.6)
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_block_age_exploration_takes_the_least_recently_observed(oracle_mod, seed):
+    """Block-age exploration: numpy brute force -- the forced blocks, the top m - f - e blocks
+    by score (lower block on ties), then the e not yet selected blocks with the smallest age
+    (the step + 1 of their last observation, 0 = never), lower block on equal ages."""
+    o = oracle_mod
+    n, q = 64 * 40 - 5, 64 * 40 - 2                  # 40 blocks
+    cfg = tiny_cfg(o, explore="age", n_req=1, max_slots=64 * 40, rho_bp=5000, gamma_bp=2500, top_k=16)
+    rng = np.random.default_rng(seed)
+    V = rng.integers(-20, 21, (1, cfg.max_slots)).astype(np.float32)
+    D = np.full((1, o.d_len(cfg)), -1e6, np.float32)
+    age = rng.integers(0, 6, (1, o.max_blocks(cfg))).astype(np.uint32)   # many equal ages
+    blocks, nbk, _, _, ok = o.select_blocks(cfg, V, D, np.ones(1, np.int32), np.array([n], np.int32),
+                                            np.array([q], np.int32), 1, -1, 3, 0, age=age)
+    assert ok
+    nb = 40
+    S = np.array([V[0, j * 64:min((j + 1) * 64, n)].max() for j in range(nb)])
+    m = max(-(-16 // 64), -(-(10000 - 5000) * nb // 10000))
+    f = 2
+    e = min(2500 * m // 10000, m - f)
+    free = [j for j in range(1, nb - 1)]
+    top = sorted(free, key=lambda j: (-S[j], j))[: m - f - e]
+    rest = [j for j in free if j not in top]
+    explore = sorted(rest, key=lambda j: (int(age[0, j]), j))[:e]
+    assert e > 0 and blocks[0, 0, : nbk[0, 0]].tolist() == sorted({0, nb - 1} | set(top) | set(explore))
+
+
+def test_block_age_update_marks_the_listed_blocks(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, explore="age", n_req=2)
+    MB = o.max_blocks(cfg)
+    age = np.full((2, MB), 7, np.uint32)
+    blist = np.full((2, MB), -1, np.int32)
+    blist[0, :3] = [0, 2, 4]
+    blist[1, :1] = [1]
+    assert o.block_age_update(cfg, age, blist, np.array([3, 1], np.int32), np.array([300, 100], np.int32), 41)
+    want = np.full((2, MB), 7, np.uint32)
+    want[0, [0, 2, 4]] = 42
+    want[1, 1] = 42
+    np.testing.assert_array_equal(age, want)
+    blist[1, 0] = 3                                     # outside a 100-slot context
+    assert not o.block_age_update(cfg, age, blist, np.array([3, 1], np.int32), np.array([300, 100], np.int32), 41)
+
+
+def test_block_age_mode_needs_ages_and_one_row(oracle_mod):
+    o = oracle_mod
+    cfg = tiny_cfg(o, explore="age", n_req=1)
+    V, D, warm = o.new_state(cfg)
+    ns, qp = np.array([200], np.int32), np.array([203], np.int32)
+    assert not o.select_blocks(cfg, V, D, warm, ns, qp)[-1]
+    age = np.zeros((1, o.max_blocks(cfg)), np.uint32)
+    assert o.select_blocks(cfg, V, D, warm, ns, qp, age=age)[-1]
+    assert not o.select_blocks(cfg, V, D, warm, ns, qp, rows=2, age=age)[-1]
