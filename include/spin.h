@@ -112,6 +112,14 @@ typedef enum spin_combine { SPIN_COMBINE_MAX = 0, SPIN_COMBINE_SUM = 1 } spin_co
  * i < N (t = fl((1-alpha) zb), fma(alpha, old, t)); the predicted block score is
  * max(Vb[j], Db[floor(q/64) - j]) (or their sum under SPIN_COMBINE_SUM); Vmax and the
  * slot-level entries are not used.  rows > 1 is rejected with SPIN_ERR_UNSUPPORTED. */
+/* Exploration policy of the selection's exploration share (gamma).  RANDOM is §3.2.1 (the
+ * method): Philox draws.  BLOCK_AGE is the block-age alternative of §4.6 ("Staleness
+ * mitigation"), for diagnostics and one query row: the not yet selected blocks observed least
+ * recently, i.e. with the smallest age (the decode step + 1 at which the block was last
+ * scored, 0 = never), equal ages to the lower block.  It keeps a caller-owned age array
+ * uint32 [R][MB] and needs spin_select_blocks_age / spin_update_ema_age. */
+typedef enum spin_explore { SPIN_EXPLORE_RANDOM = 0, SPIN_EXPLORE_BLOCK_AGE = 1 } spin_explore_t;
+
 typedef enum spin_pooling {
     SPIN_POOL_MAX = 0,
     SPIN_POOL_MEAN = 1,
@@ -148,6 +156,8 @@ typedef struct spin_config {
     uint64_t seed;       /* exploration key */
     int32_t score_path;  /* spin_score_path_t */
     int32_t pooling;     /* spin_pooling_t: MAX (Eq. 2, the method) or an ablation variant */
+    int32_t explore;     /* spin_explore_t: RANDOM (the method) or BLOCK_AGE */
+    int32_t reserved;    /* must be 0 */
 } spin_config;
 
 /* Zero V, D and Vmax and mark the request cold: the reset after prefill and at every
@@ -259,6 +269,18 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
                                          int32_t* n_blocks, int32_t* union_blocks,
                                          int32_t* n_union, uint32_t* status,
                                          spin_stream_t stream);
+
+/* spin_select_blocks under SPIN_EXPLORE_BLOCK_AGE (rows = 1): block_age uint32 [R][MB]
+ * (device, read) gives each block's age; the exploration share goes to the not yet selected
+ * blocks with the smallest age, equal ages to the lower block.  The other selection entry
+ * points refuse BLOCK_AGE (SPIN_ERR_INVALID_ARG); a NULL block_age is SPIN_ERR_INVALID_ARG. */
+spin_status_t spin_select_blocks_age(const spin_config* cfg, const float* V, const float* D,
+                                     const float* Vmax, const int32_t* warm,
+                                     const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
+                                     const int32_t* rho_override, uint64_t step, int32_t layer,
+                                     const uint32_t* block_age, int32_t* blocks, int32_t* n_blocks,
+                                     int32_t* union_blocks, int32_t* n_union, void* workspace,
+                                     size_t workspace_bytes, uint32_t* status, spin_stream_t stream);
 
 /* Indexer score (§2; Algorithm 1's scoring step) of every slot of every listed block for `rows`
  * query rows: z_r[i] = sum_h w[r][h] * ReLU(s_i * (q[r][h] . k[i][h'])), h' = h for
@@ -404,6 +426,15 @@ spin_status_t spin_allocate_budgets(const float* miss, int32_t n_layers, int32_t
  * receives the time the wait took. */
 spin_status_t spin_selftest_wait(int32_t mode, uint64_t limit_ns, uint32_t* status,
                                  uint64_t* elapsed_ns, spin_stream_t stream);
+
+/* spin_update_ema under SPIN_EXPLORE_BLOCK_AGE: also sets block_age[req][blk] = step + 1 for
+ * every listed block inside the context (device, read-write; zero it at a reset).  The other
+ * update entry points refuse BLOCK_AGE (SPIN_ERR_INVALID_ARG). */
+spin_status_t spin_update_ema_age(const spin_config* cfg, float* V, float* D, float* Vmax,
+                                  int32_t* warm, const float* scores, const int32_t* list,
+                                  const int32_t* n_list, const int32_t* n_slots,
+                                  const int32_t* q_pos, uint32_t* block_age, uint64_t step,
+                                  uint32_t* status, spin_stream_t stream);
 
 /* Bytes of device workspace spin_select_blocks needs for `rows` rows: block scores and
  * exploration draws (2 x 4 B per request, row and block), or under SPIN_POOL_SLOTS the slot

@@ -65,6 +65,9 @@ static spin_status_t check_cfg(const spin_config* c) {
         return fail(SPIN_ERR_INVALID_ARG, "score_path %d unknown", c->score_path);
     if (c->pooling < SPIN_POOL_MAX || c->pooling > SPIN_POOL_A2)
         return fail(SPIN_ERR_INVALID_ARG, "pooling %d unknown", c->pooling);
+    if (c->explore < SPIN_EXPLORE_RANDOM || c->explore > SPIN_EXPLORE_BLOCK_AGE)
+        return fail(SPIN_ERR_INVALID_ARG, "explore %d unknown", c->explore);
+    if (c->reserved != 0) return fail(SPIN_ERR_INVALID_ARG, "reserved must be 0");
     return SPIN_OK;
 }
 
@@ -73,6 +76,8 @@ static spin_status_t check_rows(const spin_config* c, int rows) {
     if ((int64_t)c->n_req * rows > 65535) return fail(SPIN_ERR_CAPACITY, "n_req * rows above 65535");
     if (c->pooling == SPIN_POOL_A2 && rows > 1)
         return fail(SPIN_ERR_UNSUPPORTED, "the A2 ablation keeps block-level state for one query row");
+    if (c->explore == SPIN_EXPLORE_BLOCK_AGE && rows > 1)
+        return fail(SPIN_ERR_UNSUPPORTED, "block-age exploration keeps one age per block: one query row");
     return SPIN_OK;
 }
 
@@ -115,11 +120,15 @@ static spin_status_t select_impl(const spin_config* cfg, const float* V, const f
                                  const int32_t* rho_override, uint64_t step, const uint64_t* step_dev, int32_t layer,
                                  int32_t* blocks, int32_t* n_blocks, int32_t* union_blocks, int32_t* n_union,
                                  void* workspace, size_t workspace_bytes, uint32_t* status, spin_stream_t stream,
-                                 int32_t n_layers = 1) {
+                                 int32_t n_layers = 1, const uint32_t* block_age = nullptr) {
     spin_status_t st = check_cfg(cfg);
     if (st) return st;
     if ((st = check_rows(cfg, rows))) return st;
     if ((st = check_layers(n_layers))) return st;
+    if ((cfg->explore == SPIN_EXPLORE_BLOCK_AGE) != (block_age != nullptr))
+        return fail(SPIN_ERR_INVALID_ARG, cfg->explore == SPIN_EXPLORE_BLOCK_AGE
+                                              ? "block-age exploration needs spin_select_blocks_age and an age array"
+                                              : "an age array needs explore = SPIN_EXPLORE_BLOCK_AGE");
     const Dims dm = dims_of(*cfg);
     if (dm.MB > kSelectMaxBlocks)
         return fail(SPIN_ERR_CAPACITY, "max_slots %d needs %d blocks; selection supports %d", cfg->max_slots, dm.MB,
@@ -135,7 +144,7 @@ static spin_status_t select_impl(const spin_config* cfg, const float* V, const f
         return fail(SPIN_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
     if (((uintptr_t)workspace & 255) != 0) return fail(SPIN_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, step_dev, layer, blocks, n_blocks,
-                 union_blocks, n_union, reinterpret_cast<float*>(workspace), status, n_layers};
+                 union_blocks, n_union, reinterpret_cast<float*>(workspace), status, n_layers, block_age};
     return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks");
 }
 
@@ -157,6 +166,18 @@ spin_status_t spin_select_blocks_layers(const spin_config* cfg, int32_t n_layers
                                         spin_stream_t stream) {
     return select_impl(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, step_dev, layer0, blocks,
                        n_blocks, union_blocks, n_union, workspace, workspace_bytes, status, stream, n_layers);
+}
+
+spin_status_t spin_select_blocks_age(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
+                                     const int32_t* warm, const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
+                                     const int32_t* rho_override, uint64_t step, int32_t layer,
+                                     const uint32_t* block_age, int32_t* blocks, int32_t* n_blocks,
+                                     int32_t* union_blocks, int32_t* n_union, void* workspace,
+                                     size_t workspace_bytes, uint32_t* status, spin_stream_t stream) {
+    g_err[0] = 0;
+    if (!block_age) return fail(SPIN_ERR_INVALID_ARG, "block_age is NULL");
+    return select_impl(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, nullptr, layer, blocks,
+                       n_blocks, union_blocks, n_union, workspace, workspace_bytes, status, stream, 1, block_age);
 }
 
 spin_status_t spin_select_blocks_dstep(const spin_config* cfg, const float* V, const float* D, const float* Vmax,
@@ -217,6 +238,8 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
     spin_status_t st = check_cfg(cfg);
     if (st) return st;
     if ((st = check_rows(cfg, rows))) return st;
+    if (cfg->explore == SPIN_EXPLORE_BLOCK_AGE)
+        return fail(SPIN_ERR_INVALID_ARG, "block-age exploration needs spin_select_blocks_age and an age array");
     const Dims dm = dims_of(*cfg);
     if (dm.MB > kSelectMaxBlocks)
         return fail(SPIN_ERR_CAPACITY, "max_slots %d needs %d blocks; selection supports %d", cfg->max_slots, dm.MB,
@@ -365,13 +388,19 @@ spin_status_t spin_topk(const spin_config* cfg, const float* scores, const int32
 
 static spin_status_t update_impl(const spin_config* cfg, int32_t n_layers, float* V, float* D, float* Vmax,
                                  int32_t* warm, const float* scores, const int32_t* list, const int32_t* n_list,
-                                 const int32_t* n_slots, const int32_t* q_pos, uint32_t* status, spin_stream_t stream) {
+                                 const int32_t* n_slots, const int32_t* q_pos, uint32_t* status, spin_stream_t stream,
+                                 uint32_t* block_age = nullptr, uint64_t age_step = 0) {
     spin_status_t st = check_cfg(cfg);
     if (st) return st;
     if ((st = check_layers(n_layers))) return st;
     if (!V || !D || !Vmax || !warm || !scores || !list || !n_list || !n_slots || !q_pos)
         return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
-    EmaArgs a{V, D, Vmax, warm, scores, 1, list, n_list, n_slots, q_pos, nullptr, status, n_layers};
+    if ((cfg->explore == SPIN_EXPLORE_BLOCK_AGE) != (block_age != nullptr))
+        return fail(SPIN_ERR_INVALID_ARG, cfg->explore == SPIN_EXPLORE_BLOCK_AGE
+                                              ? "block-age exploration needs spin_update_ema_age and an age array"
+                                              : "an age array needs explore = SPIN_EXPLORE_BLOCK_AGE");
+    EmaArgs a{V, D, Vmax, warm, scores, 1, list, n_list, n_slots, q_pos, nullptr, status, n_layers, block_age,
+              age_step};
     return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_update_ema");
 }
 
@@ -385,6 +414,8 @@ static spin_status_t commit_impl(const spin_config* cfg, int32_t n_layers, float
     if ((st = check_layers(n_layers))) return st;
     if (!V || !D || !Vmax || !warm || !scores || !union_blocks || !n_union || !n_slots || !q_pos || !accepted)
         return fail(SPIN_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (cfg->explore == SPIN_EXPLORE_BLOCK_AGE)
+        return fail(SPIN_ERR_INVALID_ARG, "block-age exploration has no MTP commit");
     EmaArgs a{V, D, Vmax, warm, scores, rows, union_blocks, n_union, n_slots, q_pos, accepted, status, n_layers};
     return launched(launch_ema(*cfg, a, (cudaStream_t)stream), "spin_commit_mtp");
 }
@@ -393,6 +424,16 @@ spin_status_t spin_update_ema(const spin_config* cfg, float* V, float* D, float*
                               const float* scores, const int32_t* list, const int32_t* n_list, const int32_t* n_slots,
                               const int32_t* q_pos, uint32_t* status, spin_stream_t stream) {
     return update_impl(cfg, 1, V, D, Vmax, warm, scores, list, n_list, n_slots, q_pos, status, stream);
+}
+
+spin_status_t spin_update_ema_age(const spin_config* cfg, float* V, float* D, float* Vmax, int32_t* warm,
+                                  const float* scores, const int32_t* list, const int32_t* n_list,
+                                  const int32_t* n_slots, const int32_t* q_pos, uint32_t* block_age, uint64_t step,
+                                  uint32_t* status, spin_stream_t stream) {
+    g_err[0] = 0;
+    if (!block_age) return fail(SPIN_ERR_INVALID_ARG, "block_age is NULL");
+    return update_impl(cfg, 1, V, D, Vmax, warm, scores, list, n_list, n_slots, q_pos, status, stream, block_age,
+                       step);
 }
 
 spin_status_t spin_update_ema_layers(const spin_config* cfg, int32_t n_layers, float* V, float* D, float* Vmax,

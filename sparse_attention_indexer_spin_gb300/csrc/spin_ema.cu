@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs 
                 const float t = __fmul_rn(oma, m);
                 Vq[blk] = __fmaf_rn(alpha, Vq[blk], t);
                 Dq[qb - blk] = __fmaf_rn(alpha, Dq[qb - blk], t);
+                if (a.block_age) a.block_age[(int64_t)req * dm.MB + blk] = (uint32_t)(a.age_step + 1);
             }
         }
         return;
@@ -259,7 +260,11 @@ __global__ void __launch_bounds__(256) ema_list_kernel(spin_config cfg, EmaArgs 
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) a.Vmax[(int64_t)req * dm.MB + blk[e]] = m;
+            if (lane == 0) {
+                a.Vmax[(int64_t)req * dm.MB + blk[e]] = m;
+                // block-age exploration (§4.6): the block was observed at this step
+                if (a.block_age) a.block_age[(int64_t)req * dm.MB + blk[e]] = (uint32_t)(a.age_step + 1);
+            }
         }
     }
 }

@@ -29,6 +29,7 @@ struct SelectArgs {
     float* block_scores;  // workspace: S [R][rows][MB] fp32, then exploration draws [R][rows][MB] u32
     uint32_t* status;
     int n_layers;         // layers stacked along the outermost dimension of every array (0 or 1: one)
+    const uint32_t* block_age = nullptr;  // block-age exploration: ages [R][MB] replace the draws
 };
 
 struct ScoreArgs {
@@ -62,6 +63,8 @@ struct EmaArgs {
     const int32_t* accepted;  // NULL: a = 0
     uint32_t* status;
     int n_layers;             // layers stacked along the outermost dimension (0 or 1: one)
+    uint32_t* block_age = nullptr;  // block-age exploration: listed blocks get age_step + 1
+    uint64_t age_step = 0;
 };
 
 size_t select_workspace_bytes(const spin_config& cfg, int rows);

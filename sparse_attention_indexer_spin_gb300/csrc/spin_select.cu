@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
                                                           const int32_t* __restrict__ rho_override,
                                                           uint64_t seed, uint64_t step,
                                                           const uint64_t* __restrict__ step_dev, int layer,
+                                                          const uint32_t* __restrict__ block_age,
                                                           float* __restrict__ S, uint32_t* __restrict__ X) {
     pdl_begin();
     if (step_dev) step = *step_dev;
@@ -93,7 +94,13 @@ __global__ void __launch_bounds__(256) block_score_kernel(spin_config cfg, const
             const int64_t g = j0 / 8 + lane;
             if (g * 8 < nb) {
                 uint32_t k8[8];
-                explore_keys8(seed, layer, step, r, req, g, k8);
+                if (block_age) {  // block-age exploration (§4.6): the ages are the keys
+#pragma unroll
+                    for (int h = 0; h < 8; ++h)
+                        k8[h] = g * 8 + h < nb ? block_age[(int64_t)req * dm.MB + g * 8 + h] : 0u;
+                } else {
+                    explore_keys8(seed, layer, step, r, req, g, k8);
+                }
 #pragma unroll
                 for (int h = 0; h < 8; ++h)
                     if (g * 8 + h < nb) Xq[g * 8 + h] = k8[h];
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
     const int32_t* __restrict__ q_pos, int rows, const int32_t* __restrict__ rho_override, uint64_t step,
     int layer, const float* __restrict__ S, int32_t* __restrict__ blocks, int32_t* __restrict__ n_blocks,
     int32_t* __restrict__ union_blocks, int32_t* __restrict__ n_union, uint32_t* status,
-    const uint64_t* __restrict__ step_dev) {
+    const uint64_t* __restrict__ step_dev, const uint32_t* __restrict__ block_age) {
     pdl_begin();
     if (step_dev) step = *step_dev;
     extern __shared__ __align__(16) unsigned char sel_smem[];
@@ -370,7 +377,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(
             if (e > 0) {
                 // smallest Philox key first == largest complement
                 for (int j = tid; j < nb; j += kSelThreads)
-                    if (flag[j] == 0) keys[j] = ~explore_key(cfg.seed, layer, step, r, req, j);
+                    if (flag[j] == 0)
+                        keys[j] = ~(block_age ? block_age[(int64_t)req * MB + j]
+                                              : explore_key(cfg.seed, layer, step, r, req, j));
                 __syncthreads();
                 top_select(keys, flag, nb, (int)e, 1, sh);
             }
@@ -907,7 +916,7 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
                                               (size_t)L * select_array_bytes(cfg, a.rows));
     cudaError_t e = launch_pdl(many_rows ? block_score_kernel<16> : block_score_kernel<8>, g1, dim3(256), 0, s,
                                nullptr, 0, cfg, a.V, a.D, a.Vmax, a.warm, a.n_slots, a.q_pos, a.rows,
-                               a.rho_override, cfg.seed, a.step, a.step_dev, a.layer, S, X);
+                               a.rho_override, cfg.seed, a.step, a.step_dev, a.layer, a.block_age, S, X);
     if (e != cudaSuccess) return e;
     if (dm.MB <= kSrMaxBlocks && a.rows >= 1 && a.rows <= 8) {
         const int kpt = dm.MB <= kSrThreads ? 1 : dm.MB <= 2 * kSrThreads ? 2 : dm.MB <= 4 * kSrThreads ? 4
@@ -932,7 +941,7 @@ cudaError_t launch_select(const spin_config& cfg, const SelectArgs& a, cudaStrea
     }
     return launch_pdl(select_kernel, dim3(dm.R, L), dim3(kSelThreads), smem, s, nullptr, 0, cfg, a.warm, a.n_slots,
                       a.q_pos, a.rows, a.rho_override, a.step, a.layer, (const float*)a.block_scores, a.blocks,
-                      a.n_blocks, a.union_blocks, a.n_union, a.status, a.step_dev);
+                      a.n_blocks, a.union_blocks, a.n_union, a.status, a.step_dev, a.block_age);
 }
 
 }  // namespace spin

@@ -21,6 +21,7 @@ HEADER = os.path.join(ROOT, "include", "spin.h")
 DTYPE = {"f32": 0, "bf16": 1, "e4m3": 2}
 COMBINE = {"max": 0, "sum": 1}
 POOLING = {"max": 0, "mean": 1, "top4": 2, "slots": 3, "a2": 4}
+EXPLORE = {"random": 0, "age": 1}
 SCORE_PATH = {"auto": 0, "generic": 1, "stream": 2, "tcgen05": 3}
 
 STATUS_BITS = {
@@ -49,7 +50,8 @@ class SpinConfig(ctypes.Structure):
         ("kv_heads", ctypes.c_int32), ("q_dtype", ctypes.c_int32), ("k_dtype", ctypes.c_int32),
         ("top_k", ctypes.c_int32), ("rho_bp", ctypes.c_int32), ("gamma_bp", ctypes.c_int32),
         ("alpha", ctypes.c_float), ("combine", ctypes.c_int32), ("seed", ctypes.c_uint64),
-        ("score_path", ctypes.c_int32), ("pooling", ctypes.c_int32),
+        ("score_path", ctypes.c_int32), ("pooling", ctypes.c_int32), ("explore", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
     @property
@@ -63,11 +65,12 @@ class SpinConfig(ctypes.Structure):
 
 def make_config(n_req, max_slots, max_rows, n_heads, head_dim, kv_heads, q_dtype, k_dtype, top_k,
                 rho_bp, gamma_bp, alpha, combine="max", seed=0, block=64, score_path="auto",
-                pooling="max", **_ignored) -> SpinConfig:
+                pooling="max", explore="random", **_ignored) -> SpinConfig:
     return SpinConfig(int(n_req), int(max_slots), int(max_rows), int(block), int(n_heads),
                       int(head_dim), int(kv_heads), DTYPE[q_dtype], DTYPE[k_dtype], int(top_k),
                       int(rho_bp), int(gamma_bp), float(alpha), COMBINE[combine],
-                      int(seed) & 0xFFFFFFFFFFFFFFFF, SCORE_PATH[score_path], POOLING[pooling])
+                      int(seed) & 0xFFFFFFFFFFFFFFFF, SCORE_PATH[score_path], POOLING[pooling],
+                      EXPLORE[explore], 0)
 
 
 def ensure_built() -> str:
@@ -106,6 +109,9 @@ def lib():
             "spin_topk_hinted": [C, P, P, P, P, P, i32, P, P, ctypes.c_size_t, P, P],
             "spin_topk": [C, P, P, P, P, i32, P, P, P],
             "spin_update_ema": [C, P, P, P, P, P, P, P, P, P, P, P],
+            "spin_select_blocks_age": [C, P, P, P, P, P, P, i32, P, u64, i32, P, P, P, P, P, P,
+                                       ctypes.c_size_t, P, P],
+            "spin_update_ema_age": [C, P, P, P, P, P, P, P, P, P, P, u64, P, P],
             "spin_commit_mtp": [C, P, P, P, P, P, i32, P, P, P, P, P, P, P],
             "spin_workspace_size": [C, i32, ctypes.POINTER(ctypes.c_size_t)],
             "spin_selftest_wait": [i32, u64, P, P, P],
@@ -218,6 +224,25 @@ def select_blocks(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, ste
         ctypes.byref(cfg), _ptr(V), _ptr(D), _ptr(Vmax), _ptr(warm), _ptr(n_slots), _ptr(q_pos),
         rows, _ptr(rho_override), int(step), int(layer), _ptr(blocks), _ptr(n_blocks),
         _ptr(union_blocks), _ptr(n_union), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+
+
+def select_blocks_age(cfg, V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, layer, block_age,
+                      blocks, n_blocks, union_blocks, n_union, workspace, status, stream=None):
+    """spin_select_blocks_age: block-age exploration; block_age is an int32 device tensor
+    [R][MB] holding the uint32 ages."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().spin_select_blocks_age(
+        ctypes.byref(cfg), _ptr(V), _ptr(D), _ptr(Vmax), _ptr(warm), _ptr(n_slots), _ptr(q_pos),
+        rows, _ptr(rho_override), int(step), int(layer), _ptr(block_age), _ptr(blocks), _ptr(n_blocks),
+        _ptr(union_blocks), _ptr(n_union), _ptr(workspace), ws_bytes, _ptr(status), _stream(stream)))
+
+
+def update_ema_age(cfg, V, D, Vmax, warm, scores, list_, n_list, n_slots, q_pos, block_age, step, status,
+                   stream=None):
+    """spin_update_ema_age: the EMA update that also records the listed blocks' age."""
+    _check(lib().spin_update_ema_age(ctypes.byref(cfg), _ptr(V), _ptr(D), _ptr(Vmax), _ptr(warm),
+                                     _ptr(scores), _ptr(list_), _ptr(n_list), _ptr(n_slots), _ptr(q_pos),
+                                     _ptr(block_age), int(step), _ptr(status), _stream(stream)))
 
 
 def select_blocks_layers(cfg, n_layers, layer0, V, D, Vmax, warm, n_slots, q_pos, rows, rho_table,
@@ -384,7 +409,7 @@ class StepBuffers:
 
 def run_step(cfg, state: LayerState, buf: StepBuffers, q, w, k_pool, k_scale, n_pages,
              block_table, n_slots, q_pos, step=0, layer=0, rho_override=None, accepted=None,
-             stream=None, hint: Optional[TopkHint] = None):
+             stream=None, hint: Optional[TopkHint] = None, block_age=None):
     """One decode step of one layer through the C ABI: select -> score -> top-K -> EMA
     (or, with rows > 1, select -> union -> score -> top-K -> deferred commit).  With a
     TopkHint the score kernel collects the temporal top-K's candidates and the hinted top-K
@@ -392,9 +417,14 @@ def run_step(cfg, state: LayerState, buf: StepBuffers, q, w, k_pool, k_scale, n_
     rows = buf.rows
     union = buf.union if rows > 1 else None
     n_union = buf.n_union if rows > 1 else None
-    select_blocks(cfg, state.V, state.D, state.Vmax, state.warm, n_slots, q_pos, rows,
-                  rho_override, step, layer, buf.blocks, buf.n_blocks, union, n_union,
-                  buf.workspace, buf.status, stream)
+    if block_age is None:
+        select_blocks(cfg, state.V, state.D, state.Vmax, state.warm, n_slots, q_pos, rows,
+                      rho_override, step, layer, buf.blocks, buf.n_blocks, union, n_union,
+                      buf.workspace, buf.status, stream)
+    else:
+        select_blocks_age(cfg, state.V, state.D, state.Vmax, state.warm, n_slots, q_pos, rows,
+                          rho_override, step, layer, block_age, buf.blocks, buf.n_blocks, union, n_union,
+                          buf.workspace, buf.status, stream)
     if rows == 1:
         blist = buf.blocks            # row 0 list: stride MB per request
         nlist = buf.n_blocks
@@ -408,7 +438,10 @@ def run_step(cfg, state: LayerState, buf: StepBuffers, q, w, k_pool, k_scale, n_
         indexer_score_ex(cfg, q, w, k_pool, k_scale, n_pages, block_table, blist, nlist, n_slots,
                          rows, buf.scores, buf.status, hint, stream)
         topk_hinted(cfg, buf.scores, w, blist, nlist, n_slots, rows, buf.topk, hint, buf.status, stream)
-    if rows == 1:
+    if rows == 1 and block_age is not None:
+        update_ema_age(cfg, state.V, state.D, state.Vmax, state.warm, buf.scores, blist, nlist,
+                       n_slots, q_pos, block_age, step, buf.status, stream)
+    elif rows == 1:
         update_ema(cfg, state.V, state.D, state.Vmax, state.warm, buf.scores, blist, nlist,
                    n_slots, q_pos, buf.status, stream)
     elif accepted is not None:

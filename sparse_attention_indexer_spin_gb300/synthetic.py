@@ -53,7 +53,8 @@ class Workload:
     grow_every: int = 1   # one new slot every `grow_every` steps (rows == 1)
     mean_accept: float = 0.0  # rows > 1: mean acceptance length
     combine: str = "max"
-    pooling: str = "max"  # block pooling of the slot predictions (max: Eq. 2; mean, top4: ablations)
+    pooling: str = "max"  # block reduction (max: Eq. 2; mean, top4, slots, a2: the ablations)
+    explore: str = "random"  # exploration policy (random: the method; age: the block-age ablation)
     seed: int = 0
     sweep: tuple = ()
 
@@ -80,7 +81,8 @@ class Workload:
                     n_heads=self.n_heads, head_dim=self.head_dim, kv_heads=self.kv_heads,
                     q_dtype=self.q_dtype, k_dtype=self.k_dtype, top_k=self.top_k,
                     rho_bp=self.rho_bp, gamma_bp=self.gamma_bp, alpha=self.alpha,
-                    combine=self.combine, pooling=self.pooling, seed=self.seed, block=BLOCK)
+                    combine=self.combine, pooling=self.pooling, explore=self.explore, seed=self.seed,
+                    block=BLOCK)
 
 
 # The five workloads.  Slot counts follow the paper's serving setup (507K cached + 5K

@@ -36,25 +36,32 @@ class Harness:
             spin.init_state(self.cfg, s.V, s.D, s.Vmax, s.warm)
         self.buf = spin.StepBuffers(self.cfg, wl.rows, device)
         self.tol = TOL[wl.k_dtype]
+        # block-age exploration: the ages (uint32 bit patterns in an int32 tensor), one array per layer
+        self.ages = None
+        if wl.explore == "age":
+            self.ages = [torch.zeros((wl.n_req, self.cfg.max_blocks), dtype=torch.int32, device=device)
+                         for _ in range(self.inp.n_layers)]
 
     def step(self, step, layer, q, w, qp, rho_override=None, accepted=None, check=True,
              score_requests=None, hint=None):
         wl, cfg, st, buf, inp = self.wl, self.cfg, self.states[layer], self.buf, self.inp
         rows = wl.rows
         pre = dict(V=np_(st.V).copy(), D=np_(st.D).copy(), warm=np_(st.warm).copy())
+        age = None if self.ages is None else self.ages[layer]
+        pre_age = None if age is None else np_(age).view(np.uint32).copy()
         ns = np_(inp.n_slots).copy()
         qpn = np_(qp).copy()
         buf.status.zero_()
         spin.run_step(cfg, st, buf, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
                       inp.block_table, inp.n_slots, qp, step, layer, rho_override, accepted,
-                      hint=hint)
+                      hint=hint, block_age=age)
         torch.cuda.synchronize()
         if not check:
             return None
         rho = -1 if rho_override is None else int(rho_override.item())
         gb, gnb = np_(buf.blocks), np_(buf.n_blocks)
         ob, onb, ou, onu, ok = o.select_blocks(self.ocfg, pre["V"], pre["D"], pre["warm"], ns, qpn,
-                                               rows, rho, step, layer)
+                                               rows, rho, step, layer, age=pre_age)
         assert ok
         np.testing.assert_array_equal(gnb, onb)
         for r in range(wl.n_req):
@@ -87,6 +94,9 @@ class Harness:
             np.testing.assert_array_equal(np_(st.warm), W1)
             if wl.pooling != "a2":  # A2 keeps block-level state and no Vmax
                 self.check_vmax(layer)
+            if pre_age is not None:  # the listed blocks' ages: step + 1
+                assert o.block_age_update(self.ocfg, pre_age, blist, nlist, ns, step)
+                np.testing.assert_array_equal(np_(age).view(np.uint32), pre_age)
         assert int(buf.status.item()) == 0, "status %#x" % int(buf.status.item())
         return dict(blocks=gb, n_blocks=gnb, blist=blist, nlist=nlist, scores=gsc,
                     topk=np_(buf.topk), worst=worst)

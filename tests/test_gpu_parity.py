@@ -400,3 +400,43 @@ def test_a2_refuses_several_rows():
     with pytest.raises(spin.SpinError):
         spin.select_blocks(cfg, st.V, st.D, st.Vmax, st.warm, ns, ns - 1, 2, None, 0, 0, blocks, nbk, un, nun,
                            buf.workspace, buf.status)
+
+
+# ------------------------------------------------------------------ block-age exploration
+
+@pytest.mark.parametrize("combine", ["max", "sum"])
+def test_block_age_exploration(combine):
+    """Block-age exploration (§4.6, Staleness mitigation): selections bit-identical to the
+    oracle's given the same ages, and the ages after each step equal to the oracle's update
+    (listed blocks get step + 1), every step teacher-forced on ragged contexts."""
+    wl = syn.CONFIGS["pr1"].replace(explore="age", combine=combine, steps=8, n_req=3, n0=3001, gamma_bp=2500)
+    h = Harness(wl)
+    h.inp.n_slots.copy_(torch.tensor([3001, 700, 65], dtype=torch.int32))
+    run_steps(h, 8)
+    assert int(h.ages[0].max().item()) == 8        # blocks scored at the last step
+
+
+def test_block_age_entry_points():
+    """Block-age exploration needs the age entry points and one row; the age entry points need
+    the mode."""
+    wl = syn.CONFIGS["pr1"].replace(explore="age", n_req=2)
+    cfg = spin.make_config(**wl.config_fields())
+    st, buf = spin.LayerState(cfg), spin.StepBuffers(cfg)
+    ns = torch.tensor([700, 300], dtype=torch.int32, device="cuda")
+    age = torch.zeros((2, cfg.max_blocks), dtype=torch.int32, device="cuda")
+    with pytest.raises(spin.SpinError):
+        spin.select_blocks(cfg, st.V, st.D, st.Vmax, st.warm, ns, ns - 1, 1, None, 0, 0, buf.blocks, buf.n_blocks,
+                           None, None, buf.workspace, buf.status)
+    with pytest.raises(spin.SpinError):
+        spin.select_blocks_noalloc(cfg, st.V, st.D, st.Vmax, st.warm, ns, ns - 1, 1, None, 0, 0, buf.blocks,
+                                   buf.n_blocks, None, None, buf.status)
+    with pytest.raises(spin.SpinError):
+        spin.update_ema(cfg, st.V, st.D, st.Vmax, st.warm, buf.scores, buf.blist, buf.n_list, ns, ns - 1,
+                        buf.status)
+    spin.select_blocks_age(cfg, st.V, st.D, st.Vmax, st.warm, ns, ns - 1, 1, None, 0, 0, age, buf.blocks,
+                           buf.n_blocks, None, None, buf.workspace, buf.status)
+    torch.cuda.synchronize()
+    plain = spin.make_config(**syn.CONFIGS["pr1"].replace(n_req=2).config_fields())
+    with pytest.raises(spin.SpinError):
+        spin.select_blocks_age(plain, st.V, st.D, st.Vmax, st.warm, ns, ns - 1, 1, None, 0, 0, age, buf.blocks,
+                               buf.n_blocks, None, None, buf.workspace, buf.status)
