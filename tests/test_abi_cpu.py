@@ -37,7 +37,7 @@ def test_workspace_size(spin_lib):
     ("block", 32, 1), ("n_req", 0, 1), ("max_rows", 9, 1), ("kv_heads", 3, 2),
     ("q_dtype", 2, 4), ("k_dtype", 7, 4), ("top_k", 0, 1), ("rho_bp", 10001, 1),
     ("gamma_bp", -1, 1), ("alpha", 1.5, 1), ("combine", 2, 1), ("score_path", 9, 1),
-    ("max_slots", 0, 3),
+    ("max_slots", 0, 3), ("pooling", 5, 1), ("explore", 2, 1), ("reserved", 1, 1),
 ])
 def test_config_validation(spin_lib, field, value, code):
     fields = syn.CONFIGS["pr1"].config_fields()
@@ -75,3 +75,21 @@ def test_library_refuses_to_run_without_build(tmp_path, monkeypatch):
     monkeypatch.setattr(spin, "_LIB", None)
     with pytest.raises(RuntimeError):
         spin.lib()
+
+
+def test_config_struct_layout(tmp_path):
+    """The binding's spin_config has the C struct's size and field offsets (gcc on the
+    header, no GPU)."""
+    import os
+    names = [f[0] for f in spin.SpinConfig._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "spin.h"\nint main(void) {\n'
+                   '    printf("%zu", sizeof(spin_config));\n' +
+                   "".join('    printf(" %%zu", offsetof(spin_config, %s));\n' % n for n in names) +
+                   "    return 0;\n}\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(spin.HEADER))
+    subprocess.run(["gcc", "-std=c11", "-I", inc, str(src), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(spin.SpinConfig)
+    assert vals[1:] == [getattr(spin.SpinConfig, n).offset for n in names]
