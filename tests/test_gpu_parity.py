@@ -440,3 +440,15 @@ def test_block_age_entry_points():
     with pytest.raises(spin.SpinError):
         spin.select_blocks_age(plain, st.V, st.D, st.Vmax, st.warm, ns, ns - 1, 1, None, 0, 0, age, buf.blocks,
                                buf.n_blocks, None, None, buf.workspace, buf.status)
+
+
+@pytest.mark.parametrize("pooling,explore", [("max", "random"), ("mean", "random"), ("top4", "random"),
+                                             ("slots", "random"), ("a2", "random"), ("max", "age")])
+def test_ablations_tiny_contexts(pooling, explore):
+    """Empty, one-slot, one-block, one-block-plus-one and two-block contexts next to a long one,
+    under the method and every ablation: selections, scores, top-K and state as the oracle's."""
+    wl = syn.CONFIGS["pr1"].replace(pooling=pooling, explore=explore, n_req=6, n0=3001, steps=4,
+                                    gamma_bp=2500)
+    h = Harness(wl)
+    h.inp.n_slots.copy_(torch.tensor([0, 1, 64, 65, 130, 3001], dtype=torch.int32))
+    run_steps(h, 4)
