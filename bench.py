@@ -333,6 +333,88 @@ class Workload:
                 spin.commit_mtp(cfg, lst_st.V, lst_st.D, lst_st.Vmax, lst_st.warm, self.scores[layer], rows, lst,
                                 nl, ns, qp, self.accepted[s], status)
 
+    def capture_graph(self):
+        """One stacked step captured in a CUDA graph over static input buffers: the decode step
+        is read from device memory by the selection (spin_select_blocks_layers with a device
+        step), so a replay serves any step once its inputs are copied in."""
+        spin, cfg, rows, L = self.spin, self.cfg, self.rows, self.L
+        # every input of a step packed in one device buffer (256-byte aligned pieces), so that a
+        # step's inputs arrive with one copy: N, q positions, the step, accepted counts, q and w
+        def pieces(s):
+            out = [self.n_slots[s], self.q_pos[s], torch.full((1,), s, dtype=torch.int64, device="cuda")]
+            if rows > 1:
+                out.append(self.accepted[s])
+            for layer in range(L):
+                out += [self.q[s % len(self.q)][layer], self.w[s % len(self.w)][layer]]
+            return out
+        offs, off = [], 0
+        for t in pieces(0):
+            offs.append(off)
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.g_in = torch.zeros(off, dtype=torch.uint8, device="cuda")
+
+        def views(buf):
+            return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                    for o, t in zip(offs, pieces(0))]
+
+        self.g_src = []
+        for s_ in range(self.n_steps):
+            src = torch.zeros(off, dtype=torch.uint8, device="cuda")
+            for v, t in zip(views(src), pieces(s_)):
+                v.copy_(t)
+            self.g_src.append(src)
+        vs = views(self.g_in)
+        self.g_ns, self.g_qp, self.g_step = vs[0], vs[1], vs[2]
+        self.g_acc = vs[3] if rows > 1 else None
+        k = 4 if rows > 1 else 3
+        self.g_q = [vs[k + 2 * layer] for layer in range(L)]
+        self.g_w = [vs[k + 2 * layer + 1] for layer in range(L)]
+        blocks, nbk, un, nun = self.blocks[0], self.n_blocks[0], self.unions[0], self.n_unions[0]
+        st, status, inp = self.state, self.buf.status, self.inp
+
+        def body():
+            spin.select_blocks_layers(cfg, L, 0, st.V, st.D, st.Vmax, st.warm, self.g_ns, self.g_qp, rows, None,
+                                      self.g_step, blocks, nbk, un if rows > 1 else None,
+                                      nun if rows > 1 else None, self.workspace, status)
+            for layer in range(L):
+                lst, nl = (blocks[layer, :, 0], nbk[layer, :, 0]) if rows == 1 else (un[layer], nun[layer])
+                hint = self.hints[layer] if self.hints else None
+                sc, tk = self.scores[layer], self.topk[layer]
+                q, w = self.g_q[layer], self.g_w[layer]
+                if hint is None:
+                    spin.indexer_score(cfg, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
+                                       inp.block_table, lst, nl, self.g_ns, rows, sc, status)
+                    spin.topk(cfg, sc, lst, nl, self.g_ns, rows, tk, status)
+                else:
+                    spin.indexer_score_ex(cfg, q, w, inp.k_pool[layer], inp.k_scale[layer], inp.n_pages,
+                                          inp.block_table, lst, nl, self.g_ns, rows, sc, status, hint)
+                    spin.topk_hinted(cfg, sc, w, lst, nl, self.g_ns, rows, tk, hint, status)
+            if rows == 1:
+                spin.update_ema_layers(cfg, L, st.V, st.D, st.Vmax, st.warm, self.scores, blocks[:, :, 0],
+                                       nbk[:, :, 0], self.g_ns, self.g_qp, status)
+            else:
+                spin.commit_mtp_layers(cfg, L, st.V, st.D, st.Vmax, st.warm, self.scores, rows, un, nun,
+                                       self.g_ns, self.g_qp, self.g_acc, status)
+
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="relaxed"):
+            body()
+        torch.cuda.synchronize()
+
+    def replay_steps(self, steps):
+        """Replays of the captured step, each after one copy of that step's packed inputs;
+        returns the elapsed ms (CUDA events on the stream around all of them)."""
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for s in steps:
+            self.g_in.copy_(self.g_src[s])      # the step's inputs, one copy
+            self.graph.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
     def scored_slots(self, steps, unique=False):
         """Slots scored per (step, layer) launch, from the recorded lists: times the query
         rows (the metric's count), or each slot once (unique=True, the key bytes read)."""
@@ -681,6 +763,14 @@ def run_config(name, W, K, topk, schedule, extra=()):
             time_steps(wm, range(W))
             rec["miss_rate"] = miss_rate(wm, range(W, W + 4))
             del wm
+            # the same step captured once in a CUDA graph and replayed (inputs copied in per step)
+            wk.reset()
+            time_steps(wk, range(W))
+            wk.capture_graph()
+            wk.replay_steps(range(W, 2 * W))
+            rec["graph_ms_per_step"] = wk.replay_steps(range(W, W + K)) / K
+            rec["graph_status"] = int(wk.buf.status.item())
+            del wk.graph
         elif wk is not first:
             del wk
         recs[rho] = rec

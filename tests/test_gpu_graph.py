@@ -73,3 +73,32 @@ def test_graph_replay_equals_eager(name, over):
         _same(eager, graphed, buf_e, buf_g)
         assert int(buf_g.status.item()) == 0
         inp.advance(step)
+
+
+@pytest.mark.parametrize("name,over,topk", [
+    ("v4flash", dict(n_req=4, n0=20000, n_layers=2), "hinted"),
+    ("v32", dict(n_req=1, n0=6000, n_layers=3), "hinted"),
+    ("mtp", dict(n_req=3, n0=8000, n_layers=2), "plain"),
+])
+def test_bench_graph_step_equals_eager(name, over, topk):
+    """The bench's captured layer-stacked step (selection with a device step for every layer,
+    each layer's score and top-K -- temporal or plain -- then one EMA or MTP commit launch),
+    replayed step after step, gives the eager steps' states and outputs bit for bit."""
+    import bench
+    base = syn.CONFIGS[name].replace(**over)
+    eager = bench.Workload(base, 8, base.rho_bp, topk=topk, schedule="stacked")
+    graphed = bench.Workload(base, 8, base.rho_bp, share=eager, topk=topk, schedule="stacked")
+    for s in range(2):
+        eager.step(s)
+        graphed.step(s)
+    graphed.capture_graph()
+    for s in range(2, 8):
+        eager.step(s)
+        graphed.replay_steps([s])
+        for n in ("V", "D", "Vmax", "warm"):
+            assert torch.equal(getattr(eager.state, n), getattr(graphed.state, n)), (s, n)
+        assert torch.equal(eager.scores, graphed.scores) and torch.equal(eager.topk, graphed.topk), s
+        assert torch.equal(eager.n_blocks[s], graphed.n_blocks[0]), s
+        if base.rows > 1:
+            assert torch.equal(eager.n_unions[s], graphed.n_unions[0]), s
+    assert int(graphed.buf.status.item()) == 0 and int(eager.buf.status.item()) == 0
