@@ -278,12 +278,24 @@ topk_hint_kernel(spin_config cfg, const float* __restrict__ scores, const float*
     const int64_t C = cnt * kBlock;
     const int W = (int)((C + 31) / 32);  // bitmap words
 
-    // the whole list array (MB entries) is staged, so its loads need not wait for the count
+    // the whole list array (MB entries) is staged, so its loads need not wait for the count;
+    // four entries per thread are loaded before any is stored
     bool bad_list = false;
-    for (int k = tid; k < dm.MB; k += kThThreads) {
-        const int b = list[(int64_t)req * dm.MB + k];
-        if (k < cnt && (b < 0 || b >= nb)) bad_list = true;
-        slist[k] = b;
+    for (int k0 = tid; k0 < dm.MB; k0 += 4 * kThThreads) {
+        int b4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u * kThThreads;
+            b4[u] = k < dm.MB ? list[(int64_t)req * dm.MB + k] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u * kThThreads;
+            if (k < dm.MB) {
+                if (k < cnt && (b4[u] < 0 || b4[u] >= nb)) bad_list = true;
+                slist[k] = b4[u];
+            }
+        }
     }
     if (bad_list && rr % rows == 0) set_status(status, SPIN_STATUS_BAD_LIST);
     for (int wd = tid; wd < W; wd += kThThreads) bits[wd] = 0u;
@@ -389,11 +401,22 @@ topk_hint_kernel(spin_config cfg, const float* __restrict__ scores, const float*
             hit = true;
             const unsigned long long* src = h.cand + (int64_t)rr * h.cap;
             uint32_t lo = 0xffffffffu, hi = 0u;
-            for (int i = tid; i < (int)count; i += kThThreads) {
-                const unsigned long long x = src[i];
-                cand[i] = x;
-                lo = min(lo, (uint32_t)(x >> 32));
-                hi = max(hi, (uint32_t)(x >> 32));
+            for (int i0 = tid; i0 < (int)count; i0 += 4 * kThThreads) {  // four loads in flight
+                unsigned long long x4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kThThreads;
+                    x4[u] = i < (int)count ? src[i] : 0ull;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * kThThreads;
+                    if (i < (int)count) {
+                        cand[i] = x4[u];
+                        lo = min(lo, (uint32_t)(x4[u] >> 32));
+                        hi = max(hi, (uint32_t)(x4[u] >> 32));
+                    }
+                }
             }
             th_minmax(lo, hi, sh);
             __syncthreads();
