@@ -124,6 +124,21 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak(k_dtype):
+    """Dense tensor peak (TFLOP/s) for a contraction in k_dtype: the measured sustained bf16
+    figure, times 2 for e4m3 (the nominal FP8 : bf16 ratio); the fallback without the file."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    base, kind = 1700.0, "fallback"
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            base, kind = float(d["bf16_tflops_sustained"]), "measured (bf16 sustained)"
+    if k_dtype == "e4m3":
+        return 2.0 * base, kind + " x 2 for e4m3"
+    return base, kind
+
+
 def kernel_source_hash(names):
     h = hashlib.sha256()
     for n in names:
@@ -693,6 +708,14 @@ def measure_workload(base, rho, W, K, topk, schedule, share=None, score_events=T
         rec["score_us"] = 1000.0 * avg
         rec["score_alg_bytes"] = alg
         rec["score_frac"] = alg / (avg / 1000.0) / 1e9 / peak
+        if wk.wl.kv_heads == 1:
+            # the shared-key score is a contraction on the tensor cores: its algorithmic FLOPs
+            # (2 n_h d per slot and row) against the measured sustained bf16 peak, or twice it
+            # for FP8 keys (the nominal e4m3 : bf16 ratio)
+            flops = float(np.mean(unique)) * 2.0 * wk.wl.n_heads * wk.wl.head_dim * wk.rows
+            tpeak, tkind = tensor_peak(wk.wl.k_dtype)
+            rec["score_tensor"] = {"achieved_tflops": flops / (avg / 1000.0) / 1e12, "peak_tflops": tpeak,
+                                   "frac": flops / (avg / 1000.0) / 1e12 / tpeak, "peak_kind": tkind}
     rec["topk_hint"] = wk.hint_stats()
     return wk, rec
 
