@@ -204,8 +204,8 @@ spin_status_t spin_select_blocks_dstep(const spin_config* cfg, const float* V, c
 /* Layer stacks.  A model runs the indexer step in every layer, and a layer's selection for
  * decode step t needs only that layer's state after step t-1 -- not the layer's query -- so
  * the selections of all layers can be computed together at the start of a step
- * (§3.2: block prediction and the EMA update can be scheduled asynchronously, overlapped
- * with the forward pass of other layers).  The _layers calls take n_layers layers whose
+ * (§3.2 lets block prediction and the EMA update run off the layer's own critical path,
+ * hidden behind other layers' work).  The _layers calls take n_layers layers whose
  * arrays are stacked along a new outermost dimension -- V [L][R][max_slots], D [L][R][DL],
  * Vmax [L][R][MB], warm [L][R], blocks [L][R][rows][MB], n_blocks [L][R][rows], union
  * [L][R][MB], n_union [L][R], scores [L][R][rows][MB*64], list [L][R][MB], n_list [L][R]
