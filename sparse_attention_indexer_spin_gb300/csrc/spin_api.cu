@@ -259,7 +259,7 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
     float* scratch = nullptr;
     if ((st = scratch_of_current_device(&scratch))) return st;
     SelectArgs a{V, D, Vmax, warm, n_slots, q_pos, rows, rho_override, step, nullptr, layer, blocks, n_blocks,
-                 union_blocks, n_union, scratch, status};
+                 union_blocks, n_union, scratch, status, 1};
     return launched(launch_select(*cfg, a, (cudaStream_t)stream), "spin_select_blocks_noalloc");
 }
 

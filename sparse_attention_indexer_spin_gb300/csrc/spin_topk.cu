@@ -28,7 +28,7 @@ topk_kernel(spin_config cfg, const float* __restrict__ scores, const int32_t* __
     __shared__ TopkShared sh;
     const Dims dm = dims_of(cfg);
     const int rr = blockIdx.x, req = rr / rows;
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int tid = threadIdx.x;
     const int K = cfg.top_k;
     int32_t* out = topk_idx + (int64_t)rr * K;
     const int64_t n = n_slots[req];
