@@ -253,10 +253,9 @@ spin_status_t spin_commit_mtp_layers(const spin_config* cfg, int32_t n_layers, f
  *     SPIN_POOL_SLOTS holds a prediction per slot); larger configurations are rejected
  *     with SPIN_ERR_CAPACITY.
  *   - The first call on a device looks up the array's device address (with that device
- *     current) and caches it; make that first call before any stream capture.  The cached
- *     address belongs to the device's current context: it does not survive
- *     cudaDeviceReset, after which this entry point must not be called again in the
- *     process.
+ *     current) and caches it.  The cached address belongs to the device's current
+ *     context: it does not survive cudaDeviceReset, after which this entry point must
+ *     not be called again in the process.
  *   - Every call shares the one array, which keeps the last call's contents: calls that
  *     may overlap on the GPU (different streams, or different host threads, on one
  *     device) race on it and must be serialised by the caller.
