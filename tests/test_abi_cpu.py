@@ -93,3 +93,38 @@ def test_config_struct_layout(tmp_path):
     vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
     assert vals[0] == ctypes.sizeof(spin.SpinConfig)
     assert vals[1:] == [getattr(spin.SpinConfig, n).offset for n in names]
+
+
+def test_ablation_modes_refused_on_the_host(spin_lib):
+    """The one-row ablations (A2 block states, block-age exploration) and the age entry points
+    are refused before any device access: every pointer the checks read first is NULL, so a
+    missing check would end at the NULL-pointer check, never at a launch."""
+    L = spin.lib()
+    fake_age = ctypes.c_void_p(256)
+    err = lambda: L.spin_last_error_string().decode()
+
+    def cfg_of(**kw):
+        return spin.make_config(**syn.CONFIGS["pr1"].replace(rows=2, mean_accept=1.5, **kw).config_fields())
+
+    a2 = cfg_of(pooling="a2")
+    assert L.spin_select_blocks(ctypes.byref(a2), *([None] * 6), 2, None, 0, 0, *([None] * 5), 0, None,
+                                None) == 4 and "A2" in err()
+    assert L.spin_commit_mtp(ctypes.byref(a2), *([None] * 5), 2, *([None] * 7)) == 4 and "A2" in err()
+    assert L.spin_select_blocks_noalloc(ctypes.byref(a2), *([None] * 6), 2, None, 0, 0,
+                                        *([None] * 6)) == 4 and "A2" in err()
+
+    age = cfg_of(explore="age")
+    assert L.spin_select_blocks(ctypes.byref(age), *([None] * 6), 1, None, 0, 0, *([None] * 5), 0, None,
+                                None) == 1 and "spin_select_blocks_age" in err()
+    assert L.spin_select_blocks_noalloc(ctypes.byref(age), *([None] * 6), 1, None, 0, 0,
+                                        *([None] * 6)) == 1 and "spin_select_blocks_age" in err()
+    assert L.spin_select_blocks_age(ctypes.byref(age), *([None] * 6), 2, None, 0, 0, fake_age, *([None] * 5), 0,
+                                    None, None) == 4 and "one query row" in err()
+    assert L.spin_select_blocks_age(ctypes.byref(age), *([None] * 6), 1, None, 0, 0, None, *([None] * 5), 0,
+                                    None, None) == 1 and "block_age is NULL" in err()
+    assert L.spin_update_ema_age(ctypes.byref(age), *([None] * 9), None, 0, None, None) == 1 \
+        and "block_age is NULL" in err()
+
+    plain = cfg_of()
+    assert L.spin_select_blocks_age(ctypes.byref(plain), *([None] * 6), 1, None, 0, 0, fake_age,
+                                    *([None] * 5), 0, None, None) == 1 and "SPIN_EXPLORE_BLOCK_AGE" in err()
