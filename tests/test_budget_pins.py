@@ -70,6 +70,17 @@ def test_miss_curve_hand_example():
     assert curve == [0.75, 0.25, 0.0]
 
 
+def test_miss_curve_ties_go_to_the_lower_block():
+    # Blocks 1 and 2 tie at the best predicted score; the dense top-K lies in block 2 only.
+    # At 50 % (budget 3: the forced blocks 0 and 5 plus one) the method's ranking takes the
+    # lower block of a tie, block 1, so every top-K slot is missed; at 100 % none is.
+    S = [0.0, 7.0, 7.0, 1.0, 0.5, 0.0]
+    topk = [130, 131, 140, 150]
+    assert ob.miss_curve(S, 6, topk, 4, 3) == [1.0, 1.0, 0.0]
+    # the same context with the top-K in block 1 is fully covered from 50 % on
+    assert ob.miss_curve(S, 6, [70, 71, 80, 90], 4, 3) == [1.0, 0.0, 0.0]
+
+
 def test_miss_curve_closed_form_when_ranking_follows_counts():
     rng = random.Random(3)
     nb, K = 40, 64

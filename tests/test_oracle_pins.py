@@ -423,6 +423,39 @@ def test_scores_integer_inputs_exact(oracle_mod):
     np.testing.assert_array_equal(sc.astype(np.float64), ref)
 
 
+def test_scores_fp8_scale_sign_and_scaling(oracle_mod):
+    """The per-slot FP8 scale multiplies the dot product before the ReLU (§2 with per-slot
+    key scales).  Pinned without retyping the score: since ReLU(x) - ReLU(-x) = x, scoring
+    with scales s and -s differs by sum_h w_h s (q_h . k), a plain numpy dot product with no
+    ReLU; and doubling every scale doubles every score exactly."""
+    o = oracle_mod
+    kw = dict(n_req=1, max_slots=128, max_rows=1, n_heads=4, head_dim=16, kv_heads=1,
+              q_dtype="bf16", k_dtype="e4m3", top_k=8, rho_bp=0, gamma_bp=0, alpha=0.5)
+    cfg = o.make_cfg(**kw)
+    rng = np.random.default_rng(11)
+    q = rng.integers(0, 65535, (1, 1, 4, 16)).astype(np.uint16) & 0xBFFF   # finite bf16, both signs
+    w = rng.random((1, 1, 4)).astype(np.float32)
+    pool = rng.integers(0, 255, (2, 64, 1, 16)).astype(np.uint8)
+    pool[(pool & 0x7F) == 0x7F] = 0x01                                       # no NaN codes
+    scale = (rng.random((2, 64)) * 2 - 1).astype(np.float32)                 # signed scales
+    bt = np.array([[1, 0]], dtype=np.int32)
+    args = (bt, np.array([[0, 1]], np.int32), np.array([2], np.int32), np.array([128], np.int32), 1)
+    zp, mp, ok1 = o.indexer_score(cfg, q, w, pool, scale, *args, want_mags=True)
+    zn, _, ok2 = o.indexer_score(cfg, q, w, pool, -scale, *args, want_mags=True)
+    z2, ok3 = o.indexer_score(cfg, q, w, pool, 2 * scale, *args)
+    assert ok1 and ok2 and ok3
+    qd = _decode_torch(q, "bf16").reshape(4, 16)
+    kd = _decode_torch(pool, "e4m3").reshape(2, 64, 16)
+    lin = np.zeros(128)
+    for i in range(128):
+        page, s = bt[0, i // 64], i % 64
+        lin[i] = float(scale[page, s]) * float(np.dot(w[0, 0].astype(np.float64), qd @ kd[page, s]))
+    diff = zp[0, 0].astype(np.float64) - zn[0, 0].astype(np.float64)
+    np.testing.assert_allclose(diff, lin, rtol=0, atol=1e-6 * (1 + 2 * mp.max()))
+    assert np.any(zp[0, 0] > 0) and np.any(zn[0, 0] > 0) and np.any(lin < 0) and np.any(lin > 0)
+    np.testing.assert_array_equal(z2, 2 * zp)
+
+
 def test_score_slot_matches_block_scores(oracle_mod):
     o = oracle_mod
     kw = dict(n_req=1, max_slots=128, max_rows=1, n_heads=4, head_dim=16, kv_heads=1,
