@@ -27,7 +27,8 @@
  *   oracle_select_blocks ...... |selection| = budget, forced blocks kept, top set
  *                               dominance, exploration uniformity (chi-square),
  *                               rho = 0 gives the dense selection
- *   oracle_indexer_score ...... numpy einsum brute force; integer-valued inputs exact
+ *   oracle_indexer_score ...... numpy einsum brute force; integer-valued inputs exact;
+ *                               signed scales: z(s) - z(-s) is the plain dot product
  *   oracle_topk ............... numpy lexsort brute force; rho = 0 equals dense top-K
  *   oracle_replay_ema ......... closed forms of the EMA recurrence and of the
  *                               prefix-valid replay; a = 0 equals the one-row update
