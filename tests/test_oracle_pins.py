@@ -264,6 +264,26 @@ def test_selection_invariants(oracle_mod, n, rho):
                          explore=(7, 2, 5, r))
 
 
+def test_reset_of_one_request_leaves_the_others(oracle_mod):
+    """A reset (§3.2: a request starts cold, and its first step is dense) clears that request's
+    V, D and warm flag only; req = -1 clears every request."""
+    o = oracle_mod
+    cfg = o.make_cfg(n_req=3, max_slots=256, max_rows=2, n_heads=2, head_dim=4, kv_heads=2,
+                     q_dtype="f32", k_dtype="f32", top_k=16, rho_bp=4000, gamma_bp=500, alpha=0.5)
+    rng = np.random.default_rng(5)
+    V, D, warm = o.new_state(cfg)
+    V[:] = rng.random(V.shape) + 1
+    D[:] = rng.random(D.shape) + 1
+    warm[:] = 1
+    V0, D0 = V.copy(), D.copy()
+    o.init_state(cfg, V, D, warm, 1)
+    assert np.all(V[1] == 0) and np.all(D[1] == 0) and warm[1] == 0
+    for r in (0, 2):
+        assert np.array_equal(V[r], V0[r]) and np.array_equal(D[r], D0[r]) and warm[r] == 1
+    o.init_state(cfg, V, D, warm)
+    assert not V.any() and not D.any() and not warm.any()
+
+
 def test_rho_zero_and_cold_are_dense(oracle_mod):
     o = oracle_mod
     cfg = tiny_cfg(o, n_req=2, max_slots=2000, top_k=64)
