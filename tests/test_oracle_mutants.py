@@ -93,6 +93,21 @@ MUTANTS = [
      "D_req[q - i] = fmaf(alpha, D_req[q - i], t);", PINS),
     ("replay-keeps-rejected-rows", C, "for (int64_t r = 0; r <= a; ++r) {", "for (int64_t r = 0; r < rows; ++r) {",
      PINS),
+    ("explore-counter-per-block", C, "(uint64_t)(uint32_t)req, (uint64_t)(j >> 3)}",
+     "(uint64_t)(uint32_t)req, (uint64_t)j}", PINS),
+    ("e4m3-no-nan", C, "if (e == 0xF && m == 0x7) return NAN;", "", PINS),
+    ("budget-not-capped-at-block-count", C, "return m < n_blocks ? m : n_blocks;", "return m;", PINS),
+    ("explore-count-rounded", C, "int64_t e = ((int64_t)gamma_bp * m) / 10000;",
+     "int64_t e = ((int64_t)gamma_bp * m + 5000) / 10000;", PINS),
+    ("query-before-context-accepted", C, "if (n > 0 && q < n - 1) return 0;", "", PINS),
+    ("scores-past-n-not-zero", C, "scores[o] = scored ? z[r] : 0.0f;", "scores[o] = scored ? z[r] : -1.0f;",
+     PINS),
+    ("topk-pads-with-zero", C, "out[k] = k < take ? sel[k] : -1;", "out[k] = k < take ? sel[k] : 0;", PINS),
+    ("topk-in-score-order", C, "qsort(sel, (size_t)take, sizeof(int32_t), cmp_i32_asc);", "", PINS),
+    ("replay-ignores-accepted", C, "int64_t a = accepted ? accepted[req] : 0;", "int64_t a = 0;", PINS),
+    ("a2-update-at-slot-offset", C, "D_req[q / b - blk] = fmaf(alpha, D_req[q / b - blk], t);",
+     "D_req[q - blk] = fmaf(alpha, D_req[q - blk], t);", PINS),
+    ("reset-clears-every-request", C, "if (req >= 0 && r != req) continue;", "", PINS),
     # per-layer budgets (project page, "Per-layer block budgets")
     ("miss-curve-without-forced", B, "chosen = set(forced) | set(free[: max(m - f, 0)])",
      "chosen = set(free[: max(m - f, 0)])", BUDGET_PINS),
