@@ -56,7 +56,7 @@ def parse():
     p.add_argument("--no-configs", action="store_true", help="skip the per-workload measurements")
     p.add_argument("--configs", default="pr1,v32,v4flash,mtp,serving")
     p.add_argument("--config-steps", type=int, default=20, help="timed steps per workload measurement")
-    p.add_argument("--cpu-steps", type=int, default=8, help="oracle steps of the CPU baseline")
+    p.add_argument("--cpu-steps", type=int, default=32, help="oracle steps of the CPU baseline (about 10 s)")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--layers", type=int, default=None, help="fewer layers (small profiling case)")
     p.add_argument("--n0", type=int, default=None, help="fewer slots per request (small profiling case)")
