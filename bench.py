@@ -501,6 +501,40 @@ def time_steps(wk, steps, with_score_events=False, topk_ms=None):
     return t0.elapsed_time(t1), score_ms
 
 
+def time_pure_dense(wk, W, K):
+    """The "pure dense" indexer: score and top-K over every block, with no prediction, no
+    selection and no EMA update.  `wk` must be a workload at sparsity 0 whose steps 0..W+K-1
+    have run, so its stored lists hold every block of each step's context.  Returns the mean
+    ms per step over steps W..W+K-1 after a warm-up pass over 0..W-1."""
+    def run(steps):
+        for s in steps:
+            qs, ws = wk.q[s % len(wk.q)], wk.w[s % len(wk.w)]
+            for layer in range(wk.L):
+                wk.score_topk(s, layer, qs[layer], ws[layer])
+
+    for h in wk.hints or []:
+        h.reset()
+    run(range(W))
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    run(range(W, W + K))
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / K
+
+
+def pure_dense_entry(wk, W, K, sparse_ms):
+    """time_pure_dense as a JSON entry beside the dense step.  It only re-runs the score and
+    top-K launches of steps already run; a failure is recorded in the entry rather than ending
+    the benchmark."""
+    try:
+        ms = time_pure_dense(wk, W, K)
+        return {"ms_per_step": ms, "latency_ratio": sparse_ms / ms}
+    except Exception as e:  # noqa: BLE001 -- the entry is a side measurement
+        return {"error": repr(e)[:200]}
+
+
 def time_e2e(wk, steps):
     """Same steps with per-step inputs staged from pinned host memory and the top-K read
     back to pinned host memory inside the timed region."""
@@ -794,7 +828,9 @@ def run_config(name, W, K, topk, schedule, extra=()):
             rec["graph_ms_per_step"] = wk.replay_steps(range(W, W + K)) / K
             rec["graph_status"] = int(wk.buf.status.item())
             del wk.graph
-        elif wk is not first:
+        if rho == 0:
+            rec["pure_dense"] = pure_dense_entry(wk, W, K, recs.get(base.rho_bp, rec)["ms_per_step"])
+        if wk is not first:
             del wk
         recs[rho] = rec
     tgt, dense = recs[base.rho_bp], recs[0]
@@ -889,6 +925,7 @@ def main():
         msd, _ = time_steps(wd, range(W, W + K))
         dense = {"rho": 0.0, "ms_per_step": msd / K, "latency_ratio": (ms / K) / (msd / K),
                  "topk_hint": wd.hint_stats()}
+        dense["pure_dense"] = pure_dense_entry(wd, W, K, ms / K)
         del wd
         torch.cuda.empty_cache()
 

@@ -76,3 +76,53 @@ def test_reference_arm_other_ranks_exit_quietly(oracle_mod):
                    {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def test_pure_dense_runs_only_score_and_topk(monkeypatch):
+    """The pure-dense variant re-runs each step's score and top-K launches for every layer
+    (warm-up steps first, hints reset), nothing else; a failure lands in its JSON entry."""
+    import bench
+
+    class Event:
+        def __init__(self, enable_timing=False):
+            pass
+
+        def record(self):
+            pass
+
+        def elapsed_time(self, other):
+            return 12.0
+
+    monkeypatch.setattr(torch.cuda, "Event", Event)
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda: None)
+
+    class Hint:
+        resets = 0
+
+        def reset(self):
+            Hint.resets += 1
+
+    class FakeWorkload:
+        L = 2
+        q = [["q0a", "q0b"], ["q1a", "q1b"]]
+        w = [["w0a", "w0b"], ["w1a", "w1b"]]
+
+        def __init__(self):
+            self.hints = [Hint(), Hint()]
+            self.calls = []
+
+        def score_topk(self, s, layer, q, w, ev=None):
+            self.calls.append((s, layer, q, w))
+
+    wk = FakeWorkload()
+    assert bench.time_pure_dense(wk, 3, 4) == 3.0          # 12 ms over the 4 timed steps
+    assert Hint.resets == 2
+    assert [c[:2] for c in wk.calls] == [(s, l) for s in range(7) for l in range(2)]
+    assert wk.calls[3] == (1, 1, "q1b", "w1b")
+    assert bench.pure_dense_entry(wk, 3, 4, 1.5) == {"ms_per_step": 3.0, "latency_ratio": 0.5}
+
+    class Failing(FakeWorkload):
+        def score_topk(self, *a, **k):
+            raise RuntimeError("launch failed")
+
+    assert "launch failed" in bench.pure_dense_entry(Failing(), 3, 4, 1.5)["error"]
