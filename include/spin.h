@@ -269,10 +269,12 @@ spin_status_t spin_select_blocks_noalloc(const spin_config* cfg, const float* V,
                                          int32_t* n_union, uint32_t* status,
                                          spin_stream_t stream);
 
-/* spin_select_blocks under SPIN_EXPLORE_BLOCK_AGE (rows = 1): block_age uint32 [R][MB]
- * (device, read) gives each block's age; the exploration share goes to the not yet selected
- * blocks with the smallest age, equal ages to the lower block.  The other selection entry
- * points refuse BLOCK_AGE (SPIN_ERR_INVALID_ARG); a NULL block_age is SPIN_ERR_INVALID_ARG. */
+/* spin_select_blocks under SPIN_EXPLORE_BLOCK_AGE (rows = 1; rows > 1 is
+ * SPIN_ERR_UNSUPPORTED): block_age uint32 [R][MB] (device, read) gives each block's age; the
+ * exploration share goes to the not yet selected blocks with the smallest age, equal ages to
+ * the lower block.  The other selection entry points, the MTP commit and the stacked calls
+ * refuse BLOCK_AGE (SPIN_ERR_INVALID_ARG, or SPIN_ERR_UNSUPPORTED for rows > 1); a NULL
+ * block_age is SPIN_ERR_INVALID_ARG, and so is an age array under SPIN_EXPLORE_RANDOM. */
 spin_status_t spin_select_blocks_age(const spin_config* cfg, const float* V, const float* D,
                                      const float* Vmax, const int32_t* warm,
                                      const int32_t* n_slots, const int32_t* q_pos, int32_t rows,
