@@ -128,3 +128,6 @@ def test_ablation_modes_refused_on_the_host(spin_lib):
     plain = cfg_of()
     assert L.spin_select_blocks_age(ctypes.byref(plain), *([None] * 6), 1, None, 0, 0, fake_age,
                                     *([None] * 5), 0, None, None) == 1 and "SPIN_EXPLORE_BLOCK_AGE" in err()
+    # the stacked selection has no age array: refused under BLOCK_AGE before any pointer check
+    assert L.spin_select_blocks_layers(ctypes.byref(age), 2, 0, *([None] * 6), 1, None, 0, None,
+                                       *([None] * 5), 0, None, None) == 1 and "spin_select_blocks_age" in err()
