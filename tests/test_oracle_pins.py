@@ -773,6 +773,25 @@ def test_a0_dense_cases(oracle_mod):
         assert ok and blocks[0, 0, : nb_[0, 0]].tolist() == list(range(-(-n // 64)))
 
 
+def test_a0_hand_example_each_top_slot_alone_in_its_block(oracle_mod):
+    """A0 on predictions that put each of the K = 3 best slots in a block of its own, and
+    every other prediction far below: dropping any one of the K slots would drop its block.
+    A budget of every block (rho = 0) still selects every block."""
+    o = oracle_mod
+    n = 640                                                   # 10 blocks
+    for rho, want in ((4000, [0, 2, 4, 6, 9]), (0, list(range(10)))):
+        cfg = tiny_cfg(o, pooling="slots", top_k=3, n_req=1, rho_bp=rho, max_slots=n)
+        V = np.full(cfg.max_slots, -100.0, np.float32)
+        D = np.full(o.d_len(cfg), -100.0, np.float32)
+        V[2 * 64 + 5], V[4 * 64 + 1], V[6 * 64 + 63] = 10.0, 9.0, 8.0
+        V[6 * 64 + 62] = 7.0                                  # 4th best: same block as the 3rd
+        V[8 * 64] = 6.0                                       # 5th best: a block of its own
+        blocks, nb_, _, _, ok = o.select_blocks(cfg, V[None], D[None], np.ones(1, np.int32),
+                                                np.array([n], np.int32), np.array([n - 1], np.int32),
+                                                1, -1, 0, 0)
+        assert ok and blocks[0, 0, : nb_[0, 0]].tolist() == want
+
+
 # ------------------------------------------------------- A2 block reduction (§4.6)
 
 def _a2_step(o, cfg, V, D, n, q, blocks, zfun):
