@@ -108,6 +108,34 @@ MUTANTS = [
     ("a2-update-at-slot-offset", C, "D_req[q / b - blk] = fmaf(alpha, D_req[q / b - blk], t);",
      "D_req[q - blk] = fmaf(alpha, D_req[q - blk], t);", PINS),
     ("reset-clears-every-request", C, "if (req >= 0 && r != req) continue;", "", PINS),
+    ("philox-output-words-mixed", C, "uint64_t n1 = lo1;", "uint64_t n1 = lo0;", PINS),
+    ("explore-key-without-layer", C, "uint64_t key[2] = {seed, (uint64_t)(uint32_t)layer};",
+     "uint64_t key[2] = {seed, (uint64_t)0};", PINS),
+    ("e4m3-unsigned", C, "return sign ? -v : v;", "return v;", PINS),
+    ("budget-ignores-topk-floor", C, "int64_t m = floor_k > keep ? floor_k : keep;", "int64_t m = keep;", PINS),
+    ("rho-override-ignored", C, "if (rho_bp < 0) rho_bp = cfg->rho_bp;", "", PINS),
+    ("sink-block-not-forced", C, "    mask[0] = 1;                                             /* sink block */",
+     "    (void)0;                                                 /* sink block */", PINS),
+    ("mean-count-misses-last-slot", C, "for (int l = 0; l < 64; ++l) count += valid[l] != 0;",
+     "for (int l = 0; l < 63; ++l) count += valid[l] != 0;", PINS),
+    ("a0-one-slot-short", C, "for (int64_t k = 0; k < cfg->top_k && k < n_slots; ++k)",
+     "for (int64_t k = 0; k < cfg->top_k - 1 && k < n_slots; ++k)", PINS),
+    ("a0-without-dense-budget-rule", C, "if (oracle_budget(nb, cfg->top_k, b, rho_bp) >= nb) {", "if (0) {", PINS),
+    ("a2-observation-counts-slots-past-n", C,
+     "if (i >= n) continue;\n                    float z = scores[((int64_t)req * MB + k) * b + s];",
+     "float z = scores[((int64_t)req * MB + k) * b + s];", PINS),
+    ("score-slots-past-n", C, "int scored = valid_page && i < n;", "int scored = valid_page;", PINS),
+    ("magnitude-signed", C, "adot += fabs(qv * kv);", "adot += qv * kv;", PINS),
+    ("per-head-keys-as-shared", C, "int64_t kh = cfg->kv_heads == 1 ? 0 : h;", "int64_t kh = 0;", PINS),
+    ("weights-of-request-zero", C, "const float* w_req = w + (int64_t)req * rows * H;", "const float* w_req = w;",
+     PINS),
+    ("query-of-request-zero", C, "const void* q_req = (const char*)q + (int64_t)req * q_elems * qsz;",
+     "const void* q_req = (const char*)q;", PINS),
+    ("topk-reads-row-zero", C, "cand[nc].s = scores[(((int64_t)req * rows + r) * MB + k) * b + s];",
+     "cand[nc].s = scores[(((int64_t)req * rows) * MB + k) * b + s];", PINS),
+    ("replay-reads-row-zero", C, "float z = scores[(((int64_t)req * rows + r) * MB + k) * b + s];",
+     "float z = scores[(((int64_t)req * rows) * MB + k) * b + s];", PINS),
+    ("reset-keeps-warm", C, "        warm[r] = 0;\n", "", PINS),
     # per-layer budgets (project page, "Per-layer block budgets")
     ("miss-curve-without-forced", B, "chosen = set(forced) | set(free[: max(m - f, 0)])",
      "chosen = set(free[: max(m - f, 0)])", BUDGET_PINS),
