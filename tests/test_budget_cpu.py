@@ -83,3 +83,12 @@ def test_uniform_layers_get_the_target():
     curve = np.linspace(1, 0, 101, dtype=np.float32)
     g, rho = spin.allocate_budgets(np.stack([curve] * 21), 60)
     assert g.tolist() == [60] * 21 and rho.tolist() == [4000] * 21
+
+
+def test_layer_at_the_grid_top_takes_no_spare_point():
+    # the worst miss 0.9 needs all 4 points of the first layer and none of the second; both
+    # spare points of the total 6 go to the second layer, although the first misses more
+    miss = np.array([[1.0, 0.97, 0.95, 0.92, 0.9], [0.5, 0.1, 0.0, 0.0, 0.0]], np.float32)
+    g, rho = spin.allocate_budgets(miss, 3)
+    assert g.tolist() == [4, 2] and rho.tolist() == [0, 5000]
+    assert ob.allocate(miss.astype(np.float64).tolist(), 3, 0) == [4, 2]

@@ -51,6 +51,10 @@ def test_allocation_hand_example():
     # equal misses at different points: the layer with fewer points first
     C = [1.0, 0.5, 0.5, 0.5, 0.0]
     assert ob.allocate([C, C], 1, 0) == [1, 1]
+    # a layer at the top of the grid takes no spare point, even with the largest miss: the
+    # worst miss 0.9 needs all 3 points of the first layer and none of the second; the one
+    # spare point of the total 4 goes to the second layer
+    assert ob.allocate([[1.0, 0.95, 0.92, 0.9], [0.5, 0.1, 0.0, 0.0]], 2, 0) == [3, 1]
 
 
 def test_rho_of_grid():
