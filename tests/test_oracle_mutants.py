@@ -143,6 +143,16 @@ MUTANTS = [
      BUDGET_PINS),
     ("allocate-spare-to-more-points", B, "(miss[l][g[l]], -g[l]) > (miss[best][g[best]], -g[best])",
      "(miss[l][g[l]], g[l]) > (miss[best][g[best]], g[best])", BUDGET_PINS),
+    ("allocate-strict-miss-bound", B, "if miss[l][g] <= tau:", "if miss[l][g] < tau:", BUDGET_PINS),
+    ("grid-point-as-sparsity", B, "return 10000 - g * 10000 // (n_points - 1)", "return g * 10000 // (n_points - 1)",
+     BUDGET_PINS),
+    ("miss-curve-kept-as-sparsity", B, "m = _o.budget(nb, top_k, 10000 - keep_bp)", "m = _o.budget(nb, top_k, keep_bp)",
+     BUDGET_PINS),
+    ("miss-curve-half-blocks", B, "missed = sum(1 for i in valid if i // 64 not in chosen)",
+     "missed = sum(1 for i in valid if i // 32 not in chosen)", BUDGET_PINS),
+    ("mean-curve-over-all-requests", B, "return [a / used for a in acc] if used else acc",
+     "return [a / len(nbs) for a in acc] if used else acc", BUDGET_PINS),
+    ("allocate-past-the-grid-top", B, "if g[l] >= G:", "if g[l] > G:", BUDGET_PINS),
     ("mean-curve-counts-empty-requests", B, "        if not any(int(i) >= 0 for i in topk):\n            continue\n",
      "", BUDGET_PINS),
 ]
