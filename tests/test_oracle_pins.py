@@ -672,6 +672,50 @@ def test_rho_zero_step_equals_dense_topk(oracle_mod):
             np.testing.assert_array_equal(out["topk"][r, 0], np.sort(order))
 
 
+def test_mtp_step_scores_the_union_and_replays_the_accepted_rows(oracle_mod):
+    """A whole speculative-decoding step (§3.2.2): the rows' selections (each with its own
+    exploration draws) are unioned, every row is scored over the union, and the EMA replays
+    rows 0..a of the accepted prefix: V = al^(a+1) V0 + (1-al) sum_r al^(a-r) z_r on every
+    scored slot, the same closed form as the replay's own pin, applied to the step's scores."""
+    o = oracle_mod
+    rng = np.random.default_rng(33)
+    R, H, d, n, rows = 2, 2, 8, 1200, 3
+    kw = dict(n_req=R, max_slots=1280, max_rows=4, n_heads=H, head_dim=d, kv_heads=1,
+              q_dtype="f32", k_dtype="f32", top_k=64, rho_bp=6000, gamma_bp=3000, alpha=0.9)
+    cfg = o.make_cfg(**kw)
+    MB = o.max_blocks(cfg)
+    pool = rng.integers(-3, 4, (R * MB, 64, 1, d)).astype(np.float32)
+    bt = np.arange(R * MB, dtype=np.int32).reshape(R, MB)
+    V, D, warm = o.new_state(cfg)
+    V[:] = rng.standard_normal(V.shape)
+    D[:] = rng.standard_normal(D.shape)
+    warm[:] = 1
+    V0 = V.copy()
+    q = rng.integers(-3, 4, (R, rows, H, d)).astype(np.float32)
+    w = rng.integers(0, 3, (R, rows, H)).astype(np.float32)
+    ns = np.array([n, n - 500], np.int32)
+    acc = np.array([2, 1], np.int32)
+    out = o.OracleStep(cfg).run(V, D, warm, q, w, pool, None, bt, ns, ns - 1, rows, 9, 2, accepted=acc)
+    assert out["ok"]
+    differ = False
+    for r in range(R):
+        sel = [set(out["blocks"][r, x, : out["n_blocks"][r, x]].tolist()) for x in range(rows)]
+        scored = out["blist"][r, : out["n_list"][r]].tolist()
+        assert scored == sorted(set().union(*sel))
+        differ |= any(s != sel[0] for s in sel)
+        a = int(acc[r])
+        for k, blk in enumerate(scored):
+            for s in range(64):
+                i = blk * 64 + s
+                if i >= ns[r]:
+                    continue
+                zs = [np.float64(out["scores"][r, x, k * 64 + s]) for x in range(a + 1)]
+                want = 0.9 ** (a + 1) * np.float64(V0[r, i]) + 0.1 * sum(
+                    0.9 ** (a - x) * zs[x] for x in range(a + 1))
+                assert abs(V[r, i] - want) <= 1e-5 * (abs(want) + 1)
+    assert differ  # the rows' own exploration draws make the union larger than row 0's selection
+
+
 # ------------------------------------------------------------- pooling ablations (§4.6)
 
 def _pool_inputs(oracle_mod, pooling, seed, n, combine="max", ints=True):
