@@ -24,6 +24,7 @@ BUDGET_PINS = [os.path.join(ROOT, "tests", "test_budget_pins.py")]
 
 C = "spin_oracle.c"
 B = "budgets.py"
+P = "oracle.py"
 
 # (name, file, text in the oracle, planted replacement, pin suites)
 MUTANTS = [
@@ -136,6 +137,12 @@ MUTANTS = [
     ("replay-reads-row-zero", C, "float z = scores[(((int64_t)req * rows + r) * MB + k) * b + s];",
      "float z = scores[(((int64_t)req * rows) * MB + k) * b + s];", PINS),
     ("reset-keeps-warm", C, "        warm[r] = 0;\n", "", PINS),
+    # the whole step of one layer (select -> score -> top-K -> EMA, §3.2.2 for several rows)
+    ("step-scores-row-zero-selection", P, "            blist, n_list = union, n_union",
+     "            blist, n_list = blocks[:, 0, :], n_blocks[:, 0]", PINS),
+    ("step-ignores-accepted", P,
+     "ok4 = replay_ema(cfg, V, D, warm, scores, blist, n_list, n_slots, q_pos, rows, accepted)",
+     "ok4 = replay_ema(cfg, V, D, warm, scores, blist, n_list, n_slots, q_pos, rows, None)", PINS),
     # per-layer budgets (project page, "Per-layer block budgets")
     ("miss-curve-without-forced", B, "chosen = set(forced) | set(free[: max(m - f, 0)])",
      "chosen = set(free[: max(m - f, 0)])", BUDGET_PINS),
